@@ -1,0 +1,314 @@
+/*
+ * dsa_oracle.c -- plain, slow, float64 CPU definition of one DSA decode step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the oracle that the CUDA library is
+ * checked against.  Only the test suite, the smoke check and the CPU-baseline
+ * leg of the benchmark may load it.  It shares no code, header, table or
+ * constant with the CUDA path (dsa_sparse_attention_lightning_gb300/csrc), and
+ * neither side includes or links the other.
+ *
+ * Every function below is the plain definition of what the step computes,
+ * written out in float64 with no blocking, fusion or reordering:
+ *
+ *   - oracle_e4m3_decode       the OCP FP8 E4M3 ("E4M3FN") value of a byte
+ *   - oracle_indexer_scores    lightning-indexer score of every visible token
+ *   - oracle_topk              top-k positions, ties to the lower token index
+ *   - oracle_sparse_mla        exact softmax attention over the selected rows
+ *
+ * Sources (web pages on Kimi K3.1 Pro's sparse attention):
+ *   [TS]   TokenSpeed post on Kimi K3.1 Pro (lightseek.org), sections
+ *          "Sparse attention in Kimi K3.1 Pro", "Integrating sparse attention
+ *          with the K3 stack" (steps 1-4) and "Storing index keys in the flat
+ *          KV cache".
+ *   [VLLM] "vLLM Day-0 Support for Kimi K3.1 Pro: Sparse Attention, DCP, and
+ *          Zero-Mismatch RL", sections "What Kimi K3.1 Pro changes" (table and
+ *          the paragraph after it) and "Sparse attention cuts long-context
+ *          decode bandwidth".
+ *   [SGL]  "Kimi K3.1 Pro: Day-0 Inference and RL Support with SGLang and
+ *          Miles", section "What's new in Kimi K3.1 Pro".
+ *   [AMD]  "Kimi K3.1 Pro on AMD Instinct GPUs" (dev48.org, in Russian),
+ *          overview table, row "MLA" (KV LoRA rank 512 + 64 RoPE dims).
+ *
+ * The pages do not print the indexer formula; they point to DeepSeek-V3.2 for
+ * it.  The form used here is the DeepSeek-V3.2 lightning indexer:
+ *   score(r, s) = sum_h w[r,h] * ReLU( (q[r,h] . k[s]) * ks[s] )
+ * with the ReLU applied to the scaled dot product, in that literal order.
+ *
+ * Parity pins: every function is pinned by tests/test_oracle_pins.py against
+ * closed forms, library routines and brute force (listed per function).
+ * No function here is parity-unpinned.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Index-key page: 64 tokens x 128 E4M3 values, then 64 fp32 scales. */
+#define ORA_PAGE 64
+#define ORA_IDX_DIM 128
+#define ORA_IDX_HEADS 32
+#define ORA_KEY_PAGE_BYTES (ORA_PAGE * ORA_IDX_DIM + ORA_PAGE * 4)
+/* Latent row: 512 compressed-KV dims + 64 RoPE dims ([AMD] overview, "MLA"). */
+#define ORA_LAT_DIM 576
+#define ORA_V_DIM 512
+
+enum { ORA_OK = 0, ORA_BAD_PAGE = 1, ORA_BAD_INDEX = 2, ORA_BAD_ARG = 3 };
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+/*
+ * E4M3 ("E4M3FN" in the OCP 8-bit floating point specification): one sign
+ * bit, four exponent bits with bias 7, three mantissa bits.  Exponent field 0
+ * encodes subnormals 2^-6 * m/8; the all-ones pattern with mantissa 7 is NaN;
+ * there are no infinities.  [TS] "Storing index keys in the flat KV cache":
+ * each index key is 128 FP8 values plus one four-byte scale.
+ * Pinned by: all 256 codes against torch.float8_e4m3fn -> float32.
+ */
+double oracle_e4m3_decode(uint8_t code) {
+    int sign = (code >> 7) & 1;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double mag;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0)
+        mag = ldexp((double)m / 8.0, -6);
+    else
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* bfloat16 is the upper half of an IEEE binary32; its value is exact in double. */
+static double bf16_to_double(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+static double f32_at(const uint8_t* p) {
+    float f;
+    memcpy(&f, p, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Lightning-indexer scores ([SGL] "What's new": the indexer scores every
+ * earlier token; [VLLM] "What Kimi K3.1 Pro changes": 32 heads x 128 dims,
+ * FP8 keys, one key per token; [TS] step 2 "Score").
+ *
+ *   score[r][s] = sum_{h<32} w[r][h] * max(0, (sum_{d<128} q[r][h][d] *
+ *                 key[s][d]) * ks[s])           for 0 <= s < row_len[r]
+ *
+ * Token s of request b is in page block_table[b][s / 64], slot s % 64 (the
+ * paged cache of [TS] "Storing index keys..."; 64-token pages).  Within a
+ * page: 64 x 128 key bytes, then 64 fp32 scales.
+ *
+ * The query is bf16 (q_bf16 != NULL) or E4M3 with one fp32 scale per (row,
+ * head) (q_e4m3 and q_scale != NULL): q[r][h][d] = dec(q8) * q_scale[r][h].
+ * Entries s >= row_len[r] of scores are left untouched.
+ * Pinned by: dot-product special case vs numpy, q = 0, linearity in w,
+ * scale-factoring identity, float64 einsum cross-check.
+ */
+int oracle_indexer_scores(const uint16_t* q_bf16, const uint8_t* q_e4m3, const float* q_scale,
+                          const float* w, const uint8_t* key_cache, int64_t num_pages,
+                          const int32_t* block_table, int B, int max_pages,
+                          const int32_t* row_req, const int32_t* row_len, int R,
+                          double* scores, int64_t ld) {
+    int status = ORA_OK;
+    if ((q_bf16 == NULL) == (q_e4m3 == NULL)) return ORA_BAD_ARG;
+    if (q_e4m3 != NULL && q_scale == NULL) return ORA_BAD_ARG;
+    for (int r = 0; r < R; ++r) {
+        if (row_req[r] < 0 || row_req[r] >= B) return ORA_BAD_ARG;
+        if (row_len[r] < 0 || (int64_t)row_len[r] > ld ||
+            (int64_t)row_len[r] > (int64_t)max_pages * ORA_PAGE)
+            return ORA_BAD_ARG;
+    }
+    for (int r = 0; r < R; ++r) {
+        const int b = row_req[r];
+        const int64_t len = row_len[r];
+        /* the query of this row, decoded to double once */
+        double q[ORA_IDX_HEADS][ORA_IDX_DIM];
+        for (int h = 0; h < ORA_IDX_HEADS; ++h)
+            for (int d = 0; d < ORA_IDX_DIM; ++d) {
+                size_t off = ((size_t)r * ORA_IDX_HEADS + h) * ORA_IDX_DIM + d;
+                if (q_bf16)
+                    q[h][d] = bf16_to_double(q_bf16[off]);
+                else
+                    q[h][d] = oracle_e4m3_decode(q_e4m3[off]) *
+                              (double)q_scale[(size_t)r * ORA_IDX_HEADS + h];
+            }
+        int row_status = ORA_OK;
+#pragma omp parallel for schedule(static) reduction(max : row_status)
+        for (int64_t s = 0; s < len; ++s) {
+            int64_t page = block_table[(size_t)b * max_pages + s / ORA_PAGE];
+            if (page < 0 || page >= num_pages) {
+                row_status = ORA_BAD_PAGE;
+                continue;
+            }
+            const uint8_t* pg = key_cache + (size_t)page * ORA_KEY_PAGE_BYTES;
+            const uint8_t* kb = pg + (s % ORA_PAGE) * ORA_IDX_DIM;
+            double ks = f32_at(pg + ORA_PAGE * ORA_IDX_DIM + (s % ORA_PAGE) * 4);
+            double key[ORA_IDX_DIM];
+            for (int d = 0; d < ORA_IDX_DIM; ++d) key[d] = oracle_e4m3_decode(kb[d]);
+            double acc = 0.0;
+            for (int h = 0; h < ORA_IDX_HEADS; ++h) {
+                double dot = 0.0;
+                for (int d = 0; d < ORA_IDX_DIM; ++d) dot += q[h][d] * key[d];
+                double x = dot * ks;
+                double relu = x > 0.0 ? x : 0.0;
+                acc += (double)w[(size_t)r * ORA_IDX_HEADS + h] * relu;
+            }
+            scores[(size_t)r * ld + s] = acc;
+        }
+        if (row_status != ORA_OK) status = row_status;
+    }
+    return status;
+}
+
+/* (score descending, token index ascending) */
+typedef struct {
+    double score;
+    int32_t index;
+} ora_item;
+
+static int ora_item_cmp(const void* a, const void* b) {
+    const ora_item* x = (const ora_item*)a;
+    const ora_item* y = (const ora_item*)b;
+    if (x->score > y->score) return -1;
+    if (x->score < y->score) return 1;
+    return (x->index > y->index) - (x->index < y->index);
+}
+
+/*
+ * Top-k selection ([SGL] "What's new": attention reads only the top 2,048;
+ * [TS] step 3 "Select": keep the k highest-scoring positions per query).
+ * Per row: order the visible tokens 0..row_len[r]-1 by score descending, ties
+ * to the lower token index, take the first min(k, row_len[r]) and pad the
+ * rest of idx[r][0..k) with -1.  Output is in that rank order.  -0.0 and
+ * +0.0 compare equal (IEEE), so they tie and the lower index wins.
+ * Pinned by: numpy.lexsort brute force, k >= len, all-equal scores.
+ */
+int oracle_topk(const double* scores, int64_t ld, const int32_t* row_len, int R, int k,
+                int32_t* idx) {
+    if (k < 0) return ORA_BAD_ARG;
+    for (int r = 0; r < R; ++r)
+        if (row_len[r] < 0 || (int64_t)row_len[r] > ld) return ORA_BAD_ARG;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < R; ++r) {
+        const int64_t len = row_len[r];
+        ora_item* items = (ora_item*)malloc(sizeof(ora_item) * (size_t)(len > 0 ? len : 1));
+        for (int64_t s = 0; s < len; ++s) {
+            items[s].score = scores[(size_t)r * ld + s];
+            items[s].index = (int32_t)s;
+        }
+        qsort(items, (size_t)len, sizeof(ora_item), ora_item_cmp);
+        for (int j = 0; j < k; ++j)
+            idx[(size_t)r * k + j] = (j < len) ? items[j].index : -1;
+        free(items);
+    }
+    return ORA_OK;
+}
+
+/*
+ * Sparse MLA over the selected latent rows ([VLLM] "What Kimi K3.1 Pro
+ * changes": MLA attention runs exactly over only those tokens; [TS] "Sparse
+ * attention in Kimi K3.1 Pro": every attention head attends to the selected
+ * tokens; [AMD] overview "MLA": the 576-wide latent is 512 compressed KV +
+ * 64 RoPE dims, the 512 part serving as the value).  MQA form: one latent
+ * row per token is shared by all H heads.
+ *
+ * For row r, head h, and the valid selected tokens j (idx[r][j] >= 0):
+ *   L[j][:]  = dec(latent8[token_j][:]) * latent_scale
+ *   x_j      = softmax_scale * sum_{d<576} q[r][h][d] * L[j][d]
+ *   m        = max_j x_j ;  p_j = exp(x_j - m) ;  Z = sum_j p_j
+ *   out[r][h][:] = (sum_j p_j * L[j][0:512]) / Z ;  lse[r][h] = m + ln Z
+ * With no valid token the output is 0 and lse is -inf.
+ * Latent page layout: [page][64 tokens][576 bytes]; token s of request b is
+ * in page block_table[b][s / 64], slot s % 64.
+ * Pinned by: float64 scaled_dot_product_attention on the dense case, one
+ * selected token, q = 0, split/unsplit LSE merge.
+ */
+int oracle_sparse_mla(const uint16_t* q, int H, double softmax_scale, const uint8_t* latent_cache,
+                      int64_t num_pages, double latent_scale, const int32_t* block_table, int B,
+                      int max_pages, const int32_t* row_req, const int32_t* row_len,
+                      const int32_t* idx, int k, int R, double* out, double* lse) {
+    if (H <= 0 || k < 0) return ORA_BAD_ARG;
+    for (int r = 0; r < R; ++r) {
+        if (row_req[r] < 0 || row_req[r] >= B) return ORA_BAD_ARG;
+        if (row_len[r] < 0 || (int64_t)row_len[r] > (int64_t)max_pages * ORA_PAGE)
+            return ORA_BAD_ARG;
+        for (int j = 0; j < k; ++j) {
+            int32_t t = idx[(size_t)r * k + j];
+            if (t >= row_len[r]) return ORA_BAD_INDEX;
+            if (t >= 0) {
+                int64_t page = block_table[(size_t)row_req[r] * max_pages + t / ORA_PAGE];
+                if (page < 0 || page >= num_pages) return ORA_BAD_PAGE;
+            }
+        }
+    }
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int r = 0; r < R; ++r) {
+        for (int h = 0; h < H; ++h) {
+            const int b = row_req[r];
+            double qh[ORA_LAT_DIM];
+            for (int d = 0; d < ORA_LAT_DIM; ++d)
+                qh[d] = bf16_to_double(q[((size_t)r * H + h) * ORA_LAT_DIM + d]);
+            double* x = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+            double m = -INFINITY;
+            int any = 0;
+            for (int j = 0; j < k; ++j) {
+                int32_t t = idx[(size_t)r * k + j];
+                if (t < 0) continue;
+                int64_t page = block_table[(size_t)b * max_pages + t / ORA_PAGE];
+                const uint8_t* row =
+                    latent_cache + ((size_t)page * ORA_PAGE + (size_t)(t % ORA_PAGE)) * ORA_LAT_DIM;
+                double dot = 0.0;
+                for (int d = 0; d < ORA_LAT_DIM; ++d)
+                    dot += qh[d] * (oracle_e4m3_decode(row[d]) * latent_scale);
+                x[j] = softmax_scale * dot;
+                if (x[j] > m) m = x[j];
+                any = 1;
+            }
+            double* o = out + ((size_t)r * H + h) * ORA_V_DIM;
+            for (int d = 0; d < ORA_V_DIM; ++d) o[d] = 0.0;
+            if (!any) {
+                if (lse) lse[(size_t)r * H + h] = -INFINITY;
+                free(x);
+                continue;
+            }
+            double Z = 0.0;
+            for (int j = 0; j < k; ++j) {
+                int32_t t = idx[(size_t)r * k + j];
+                if (t < 0) continue;
+                int64_t page = block_table[(size_t)b * max_pages + t / ORA_PAGE];
+                const uint8_t* row =
+                    latent_cache + ((size_t)page * ORA_PAGE + (size_t)(t % ORA_PAGE)) * ORA_LAT_DIM;
+                double p = exp(x[j] - m);
+                Z += p;
+                for (int d = 0; d < ORA_V_DIM; ++d)
+                    o[d] += p * (oracle_e4m3_decode(row[d]) * latent_scale);
+            }
+            for (int d = 0; d < ORA_V_DIM; ++d) o[d] /= Z;
+            if (lse) lse[(size_t)r * H + h] = m + log(Z);
+            free(x);
+        }
+    }
+    return ORA_OK;
+}

@@ -1,0 +1,180 @@
+"""Python access to the float64 CPU oracle (``dsa_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  The oracle is the plain definition of one DSA
+decode step (indexer scores, top-k, sparse MLA) that the CUDA library is
+checked against.  Only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this module.  It never imports the
+CUDA package, and the CUDA package never imports it.
+
+``build()`` compiles ``dsa_oracle.c`` with the host C compiler (float64,
+OpenMP) into ``liboracle.so`` next to this file.  The functions below only
+marshal numpy arrays into the C calls; all arithmetic is in the C file.
+``decode_step`` chains the three C calls in the order the pages give (score,
+select, attend), selecting on the float64 scores.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dsa_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+PAGE = 64
+IDX_HEADS = 32
+IDX_DIM = 128
+KEY_PAGE_BYTES = PAGE * IDX_DIM + PAGE * 4
+LAT_DIM = 576
+V_DIM = 512
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into ``liboracle.so`` (skipped when up to date)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    cc = os.environ.get("CC", "gcc")
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = [cc, "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        build()
+        lib = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i32, i64, dbl = ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = dbl
+        lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_set_num_threads.argtypes = [ctypes.c_int]
+        lib.oracle_indexer_scores.argtypes = [P, P, P, P, P, i64, P, i32, i32, P, P, i32, P, i64]
+        lib.oracle_indexer_scores.restype = ctypes.c_int
+        lib.oracle_topk.argtypes = [P, i64, P, i32, i32, P]
+        lib.oracle_topk.restype = ctypes.c_int
+        lib.oracle_sparse_mla.argtypes = [P, i32, dbl, P, i64, dbl, P, i32, i32, P, P, P, i32, i32,
+                                          P, P]
+        lib.oracle_sparse_mla.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _c(a, dtype):
+    """Contiguous numpy array of the given dtype (no copy when already so)."""
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def e4m3_decode(code: int) -> float:
+    return float(_load().oracle_e4m3_decode(int(code) & 0xFF))
+
+
+def indexer_scores(q_idx, w, key_cache, block_table, row_req, row_len, *, q_scale=None,
+                   ld=None):
+    """Float64 scores [R, ld]; entries past row_len are NaN.
+
+    ``q_idx`` is uint16 bf16 bits [R,32,128], or uint8 E4M3 codes [R,32,128]
+    together with ``q_scale`` fp32 [R,32].
+    """
+    lib = _load()
+    q_idx = np.asarray(q_idx)
+    R = int(np.asarray(row_len).shape[0])
+    row_len = _c(row_len, np.int32)
+    row_req = _c(row_req, np.int32)
+    block_table = _c(block_table, np.int32)
+    B, max_pages = block_table.shape
+    ld = int(ld if ld is not None else max(1, int(row_len.max(initial=0))))
+    scores = np.full((R, ld), np.nan, dtype=np.float64)
+    key_cache = _c(key_cache, np.uint8)
+    num_pages = key_cache.size // KEY_PAGE_BYTES
+    w = _c(w, np.float32)
+    if q_idx.dtype == np.uint16:
+        qb, q8, qs = _c(q_idx, np.uint16), None, None
+    else:
+        qb, q8, qs = None, _c(q_idx, np.uint8), _c(q_scale, np.float32)
+    st = lib.oracle_indexer_scores(_ptr(qb), _ptr(q8), _ptr(qs), _ptr(w), _ptr(key_cache),
+                                   num_pages, _ptr(block_table), B, max_pages, _ptr(row_req),
+                                   _ptr(row_len), R, _ptr(scores), ld)
+    if st != 0:
+        raise ValueError(f"oracle_indexer_scores failed with status {st}")
+    return scores
+
+
+def topk(scores, row_len, k):
+    """int32 [R, k] positions in rank order (score desc, index asc), -1 padded."""
+    lib = _load()
+    scores = _c(scores, np.float64)
+    R, ld = scores.shape
+    row_len = _c(row_len, np.int32)
+    idx = np.empty((R, k), dtype=np.int32)
+    st = lib.oracle_topk(_ptr(scores), ld, _ptr(row_len), R, int(k), _ptr(idx))
+    if st != 0:
+        raise ValueError(f"oracle_topk failed with status {st}")
+    return idx
+
+
+def sparse_mla(q, softmax_scale, latent_cache, latent_scale, block_table, row_req, row_len, idx):
+    """Float64 (out [R,H,512], lse [R,H]) of exact attention over the selected rows.
+
+    ``q`` is uint16 bf16 bits [R,H,576]; ``idx`` int32 [R,k] (-1 = unused slot).
+    """
+    lib = _load()
+    q = _c(q, np.uint16)
+    R, H, _ = q.shape
+    idx = _c(idx, np.int32)
+    k = idx.shape[1]
+    block_table = _c(block_table, np.int32)
+    B, max_pages = block_table.shape
+    latent_cache = _c(latent_cache, np.uint8)
+    num_pages = latent_cache.size // (PAGE * LAT_DIM)
+    out = np.zeros((R, H, V_DIM), dtype=np.float64)
+    lse = np.zeros((R, H), dtype=np.float64)
+    st = lib.oracle_sparse_mla(_ptr(q), H, float(softmax_scale), _ptr(latent_cache), num_pages,
+                               float(latent_scale), _ptr(block_table), B, max_pages,
+                               _ptr(_c(row_req, np.int32)), _ptr(_c(row_len, np.int32)), _ptr(idx),
+                               k, R, _ptr(out), _ptr(lse))
+    if st != 0:
+        raise ValueError(f"oracle_sparse_mla failed with status {st}")
+    return out, lse
+
+
+def decode_step(inp, k=2048):
+    """Score -> select -> attend for one decode step, all in the oracle.
+
+    ``inp`` is a mapping of numpy arrays with the keys produced by the input
+    generator (``q_idx``, ``w``, ``key_cache``, ``block_table``, ``row_req``,
+    ``row_len``, ``q``, ``latent_cache``, ``latent_scale``, ``softmax_scale``
+    and optionally ``q_idx_scale``).  Returns (scores, idx, out, lse), all
+    float64 except idx.
+    """
+    scores = indexer_scores(inp["q_idx"], inp["w"], inp["key_cache"], inp["block_table"],
+                            inp["row_req"], inp["row_len"], q_scale=inp.get("q_idx_scale"))
+    idx = topk(np.nan_to_num(scores, nan=0.0), inp["row_len"], k)
+    out, lse = sparse_mla(inp["q"], inp["softmax_scale"], inp["latent_cache"],
+                          inp["latent_scale"], inp["block_table"], inp["row_req"],
+                          inp["row_len"], idx)
+    return scores, idx, out, lse

@@ -1,0 +1,73 @@
+"""The oracle pins have teeth: each planted mistake in a copy of the oracle's C
+source (built on the CPU, in a temporary directory) makes some pin fail."""
+import importlib.util
+import os
+import shutil
+
+import pytest
+
+import test_oracle_pins as pins
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ORACLE_DIR = os.path.join(os.path.dirname(HERE), "oracle")
+
+# (name, original text, planted mistake)
+MUTATIONS = [
+    ("drop_last_head", "for (int h = 0; h < ORA_IDX_HEADS; ++h) {\n                double dot",
+     "for (int h = 0; h < ORA_IDX_HEADS - 1; ++h) {\n                double dot"),
+    ("drop_last_dim", "for (int d = 0; d < ORA_IDX_DIM; ++d) dot +=",
+     "for (int d = 0; d < ORA_IDX_DIM - 1; ++d) dot +="),
+    ("scale_from_next_slot", "(s % ORA_PAGE) * 4);", "((s + 1) % ORA_PAGE) * 4);"),
+    ("relu_dropped", "double relu = x > 0.0 ? x : 0.0;", "double relu = x;"),
+    ("softmax_shift_leaks", "double p = exp(x[j] - m);", "double p = exp(x[j] - m + 0.5);"),
+    ("value_dim_dropped", "for (int d = 0; d < ORA_V_DIM; ++d)\n                    o[d] +=",
+     "for (int d = 1; d < ORA_V_DIM; ++d)\n                    o[d] +="),
+    ("lse_wrong_base", "m + log(Z)", "m + log2(Z)"),
+    ("ties_to_upper_index", "return (x->index > y->index) - (x->index < y->index);",
+     "return (x->index < y->index) - (x->index > y->index);"),
+    ("latent_wrong_slot",
+     "+ (size_t)(t % ORA_PAGE)) * ORA_LAT_DIM;\n                double dot",
+     "+ (size_t)((t + 1) % ORA_PAGE)) * ORA_LAT_DIM;\n                double dot"),
+    ("e4m3_subnormal_exponent", "mag = ldexp((double)m / 8.0, -6);",
+     "mag = ldexp((double)m / 8.0, -7);"),
+    ("e4m3_bias", "mag = ldexp(1.0 + (double)m / 8.0, e - 7);",
+     "mag = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+]
+
+PIN_TESTS = [
+    pins.test_e4m3_all_codes_match_torch,
+    pins.test_indexer_single_head_is_relu_dot,
+    pins.test_indexer_last_dim_and_scale_slot,
+    pins.test_indexer_relu_is_per_head_before_weighting,
+    pins.test_indexer_einsum_crosscheck,
+    lambda m: [pins.test_topk_brute_force_with_ties(m, L, k) for L, k in [(100, 8), (1000, 64)]],
+    pins.test_mla_dense_matches_sdpa,
+    pins.test_mla_single_token_and_zero_query,
+    pins.test_mla_split_merge_by_lse,
+]
+
+
+def _mutated_oracle(tmp_path, name, old, new):
+    src = open(os.path.join(ORACLE_DIR, "dsa_oracle.c")).read()
+    assert src.count(old) == 1, name
+    d = tmp_path / name
+    d.mkdir()
+    shutil.copy(os.path.join(ORACLE_DIR, "oracle.py"), d / "oracle.py")
+    (d / "dsa_oracle.c").write_text(src.replace(old, new))
+    spec = importlib.util.spec_from_file_location(f"oracle_mut_{name}", d / "oracle.py")
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build(force=True)
+    return mod
+
+
+@pytest.mark.parametrize("name,old,new", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_planted_mistake_is_caught(tmp_path, name, old, new):
+    mod = _mutated_oracle(tmp_path, name, old, new)
+    caught = []
+    for t in PIN_TESTS:
+        try:
+            t(mod)
+        except (AssertionError, ValueError):
+            caught.append(getattr(t, "__name__", "topk"))
+    assert caught, f"no pin catches the planted mistake {name}"

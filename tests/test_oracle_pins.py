@@ -1,0 +1,376 @@
+"""Pins for the float64 oracle: closed forms, library routines, brute force.
+
+Each test ties one part of the oracle to something other than the oracle
+itself, chosen so that a plausible slip (a dropped head or dimension, a wrong
+page or slot, the scale read from the wrong token, ReLU in the wrong place, a
+wrong softmax shift or log-sum-exp) fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from dsa_sparse_attention_lightning_gb300 import inputs, traffic
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+PAGE, D, NH, LAT, V = 64, 128, 32, 576, 512
+
+
+def _read_golden(name):
+    rows = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            parts = [p.strip() for p in line.split("|")]
+            rows[parts[0]] = parts[1:]
+    return rows
+
+
+def _bf16_bits(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(
+        np.uint16)
+
+
+def _bf16_vals(bits):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def _e4m3(x):
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def _e4m3_vals(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).double().numpy()
+
+
+def _key_cache(codes, scales):
+    """Pack [ntok,128] codes and [ntok] scales into identity-mapped 64-token pages."""
+    n = codes.shape[0]
+    npg = (n + PAGE - 1) // PAGE
+    cache = np.full((npg, PAGE * D + PAGE * 4), 0x7F, dtype=np.uint8)
+    sc = np.full((npg, PAGE), np.nan, dtype=np.float32)
+    for t in range(n):
+        cache[t // PAGE, (t % PAGE) * D:(t % PAGE + 1) * D] = codes[t]
+        sc[t // PAGE, t % PAGE] = scales[t]
+    cache[:, PAGE * D:] = sc.view(np.uint8).reshape(npg, PAGE * 4)
+    bt = np.arange(npg, dtype=np.int32)[None, :]
+    return cache, bt
+
+
+def _latent_cache(codes):
+    n = codes.shape[0]
+    npg = (n + PAGE - 1) // PAGE
+    cache = np.full((npg, PAGE, LAT), 0x7F, dtype=np.uint8)
+    for t in range(n):
+        cache[t // PAGE, t % PAGE] = codes[t]
+    return cache, np.arange(npg, dtype=np.int32)[None, :]
+
+
+# ---------------------------------------------------------------- E4M3 decode
+def test_e4m3_all_codes_match_torch(oracle_mod):
+    lib = _e4m3_vals(np.arange(256, dtype=np.uint8))
+    ours = np.array([oracle_mod.e4m3_decode(c) for c in range(256)])
+    nan = np.isnan(lib)
+    assert np.array_equal(nan, np.isnan(ours))
+    assert nan.sum() == 2  # 0x7f and 0xff only
+    assert np.array_equal(lib[~nan], ours[~nan])
+    assert np.array_equal(np.signbit(lib[~nan]), np.signbit(ours[~nan]))
+
+
+def test_e4m3_golden_table(oracle_mod):
+    for code, (val,) in _read_golden("e4m3_codes.txt").items():
+        got = oracle_mod.e4m3_decode(int(code, 16))
+        if val == "nan":
+            assert math.isnan(got)
+        else:
+            assert got == float(val) and math.copysign(1, got) == math.copysign(1, float(val))
+
+
+# ------------------------------------------------------------ indexer scores
+def _rand_case(rng, n, scale_spread=True):
+    k = rng.standard_normal((n, D)).astype(np.float32)
+    codes = _e4m3(np.clip(k * 40, -448, 448))
+    scales = (rng.uniform(0.5, 2.0, n) if scale_spread else np.ones(n)).astype(np.float32)
+    return codes, scales
+
+
+def test_indexer_single_head_is_relu_dot(oracle_mod):
+    """w one-hot on head h, scale 1: score = max(0, q_h . k) (numpy float64 dot)."""
+    rng = np.random.default_rng(1)
+    n = 150
+    codes, _ = _rand_case(rng, n)
+    cache, bt = _key_cache(codes, np.ones(n, np.float32))
+    q = _bf16_bits(rng.standard_normal((1, NH, D)))
+    kd = _e4m3_vals(codes)
+    for h in (0, 17, 31):
+        w = np.zeros((1, NH), np.float32)
+        w[0, h] = 1.0
+        s = oracle_mod.indexer_scores(q, w, cache, bt, [0], [n])
+        ref = np.maximum(0.0, kd @ _bf16_vals(q[0, h]))
+        assert np.array_equal(s[0], ref) or np.allclose(s[0], ref, rtol=1e-13, atol=1e-12)
+        assert (ref == 0).sum() > 10 and (ref > 0).sum() > 10   # both ReLU branches hit
+
+
+def test_indexer_last_dim_and_scale_slot(oracle_mod):
+    """Key nonzero only in dim 127, per-token scale 2^t: score = w*relu(q[127]*code)*2^t."""
+    n = 70  # crosses a page boundary
+    codes = np.zeros((n, D), np.uint8)
+    codes[:, D - 1] = 0x38  # 1.0
+    scales = np.array([2.0 ** (t % 7) for t in range(n)], np.float32)
+    cache, bt = _key_cache(codes, scales)
+    qv = np.zeros((1, NH, D), np.float32)
+    qv[0, :, D - 1] = np.linspace(-1, 2, NH)
+    q = _bf16_bits(qv)
+    w = np.full((1, NH), 1.0 / NH, np.float32)
+    s = oracle_mod.indexer_scores(q, w, cache, bt, [0], [n])
+    qd = _bf16_vals(q[0, :, D - 1])
+    per_tok = np.sum(np.float64(w[0]) * np.maximum(0.0, qd)) * scales.astype(np.float64)
+    assert np.allclose(s[0], per_tok, rtol=1e-14)
+
+
+def test_indexer_relu_is_per_head_before_weighting(oracle_mod):
+    """Negative head weight: a head with positive logit contributes w*logit < 0."""
+    n = 3
+    codes = np.zeros((n, D), np.uint8)
+    codes[:, 0] = 0x38
+    cache, bt = _key_cache(codes, np.ones(n, np.float32))
+    qv = np.zeros((1, NH, D), np.float32)
+    qv[0, 0, 0] = 1.0     # head 0: logit +1
+    qv[0, 1, 0] = -3.0    # head 1: logit -3 -> ReLU 0
+    w = np.zeros((1, NH), np.float32)
+    w[0, 0], w[0, 1] = -0.5, 1.0
+    s = oracle_mod.indexer_scores(_bf16_bits(qv), w, cache, bt, [0], [n])
+    assert np.array_equal(s[0], np.full(n, -0.5))   # ReLU of the sum would give 0
+
+
+def test_indexer_zero_query_and_linearity(oracle_mod):
+    rng = np.random.default_rng(2)
+    n = 200
+    codes, scales = _rand_case(rng, n)
+    cache, bt = _key_cache(codes, scales)
+    q = _bf16_bits(rng.standard_normal((1, NH, D)))
+    w = rng.uniform(0.01, 0.1, (1, NH)).astype(np.float32)
+    s1 = oracle_mod.indexer_scores(q, w, cache, bt, [0], [n])
+    s4 = oracle_mod.indexer_scores(q, w * 4, cache, bt, [0], [n])
+    assert np.array_equal(s4, 4 * s1)
+    z = oracle_mod.indexer_scores(np.zeros_like(q), w, cache, bt, [0], [n])
+    assert np.array_equal(z, np.zeros_like(z))
+
+
+def test_indexer_paging_invariance_and_row_lengths(oracle_mod):
+    """Scattering pages through a shuffled block table changes nothing; rows see
+    exactly row_len tokens; entries beyond row_len stay untouched."""
+    wl = inputs.Workload("pin", [300, 130], [3, 1], H=16, k=64, seed=7, paged=True,
+                         shift_frac=0.05)
+    a = inputs.to_numpy(inputs.make_inputs(wl))
+    wl2 = inputs.Workload("pin", [300, 130], [3, 1], H=16, k=64, seed=7, paged=False,
+                          shift_frac=0.05)
+    b = inputs.to_numpy(inputs.make_inputs(wl2))
+    sa = oracle_mod.indexer_scores(a["q_idx"], a["w"], a["key_cache"], a["block_table"],
+                                   a["row_req"], a["row_len"])
+    # rebuild identity-paged caches from the shuffled ones
+    ka, bta = a["key_cache"], a["block_table"]
+    kb = np.concatenate([ka[bta[bi, :(c + 63) // 64]] for bi, c in enumerate(wl.ctx)])
+    starts = np.cumsum([0] + [(c + 63) // 64 for c in wl.ctx])
+    btb = np.full_like(bta, -1)
+    for bi, c in enumerate(wl.ctx):
+        n = (c + 63) // 64
+        btb[bi, :n] = np.arange(starts[bi], starts[bi] + n)
+    sb = oracle_mod.indexer_scores(a["q_idx"], a["w"], kb, btb, a["row_req"], a["row_len"])
+    assert np.array_equal(np.isnan(sa), np.isnan(sb))
+    assert np.array_equal(np.nan_to_num(sa), np.nan_to_num(sb))
+    for r, L in enumerate(a["row_len"]):
+        assert not np.isnan(sa[r, :L]).any()
+        assert np.isnan(sa[r, L:]).all()
+    assert b["block_table"][0, 0] == 0
+
+
+def test_indexer_einsum_crosscheck(oracle_mod):
+    """Full random case against torch float64 einsum with torch's FP8 decode."""
+    wl = inputs.Workload("pin", [257], [2], H=16, k=64, seed=3, shift_frac=0.05)
+    a = inputs.to_numpy(inputs.make_inputs(wl))
+    s = oracle_mod.indexer_scores(a["q_idx"], a["w"], a["key_cache"], a["block_table"],
+                                  a["row_req"], a["row_len"])
+    kc = a["key_cache"]
+    bt = a["block_table"][0]
+    ntok = 257
+    pages = bt[np.arange(ntok) // 64]
+    slots = np.arange(ntok) % 64
+    codes = kc[:, :PAGE * D].reshape(-1, PAGE, D)[pages, slots]
+    scales = kc[:, PAGE * D:].copy().view(np.float32)[pages, slots].astype(np.float64)
+    kd = torch.from_numpy(_e4m3_vals(codes))
+    q = torch.from_numpy(_bf16_vals(a["q_idx"]))
+    logits = torch.einsum("rhd,sd->rhs", q, kd) * torch.from_numpy(scales)
+    ref = (torch.from_numpy(a["w"].astype(np.float64))[:, :, None] * logits.clamp_min(0)).sum(1)
+    for r, L in enumerate(a["row_len"]):
+        assert np.allclose(s[r, :L], ref[r, :L].numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_indexer_fp8_query_scale(oracle_mod):
+    """E4M3 query with a (row, head) scale equals the bf16 path on the decoded values
+    when those values are exact in bf16 (E4M3 values times a power of two are)."""
+    rng = np.random.default_rng(4)
+    n = 90
+    codes, scales = _rand_case(rng, n)
+    cache, bt = _key_cache(codes, scales)
+    q8 = _e4m3(np.clip(rng.standard_normal((1, NH, D)) * 100, -448, 448))
+    qs = (2.0 ** rng.integers(-8, 3, (1, NH))).astype(np.float32)
+    w = rng.uniform(0.01, 0.1, (1, NH)).astype(np.float32)
+    s8 = oracle_mod.indexer_scores(q8, w, cache, bt, [0], [n], q_scale=qs)
+    qb = _bf16_bits(_e4m3_vals(q8) * qs[..., None])
+    sb = oracle_mod.indexer_scores(qb, w, cache, bt, [0], [n])
+    assert np.array_equal(s8, sb)
+
+
+def test_indexer_rejects_bad_page(oracle_mod):
+    codes = np.zeros((10, D), np.uint8)
+    cache, bt = _key_cache(codes, np.ones(10, np.float32))
+    with pytest.raises(ValueError):
+        oracle_mod.indexer_scores(_bf16_bits(np.zeros((1, NH, D))), np.ones((1, NH), np.float32),
+                                  cache, bt + 5, [0], [10])
+
+
+# ----------------------------------------------------------------------- top-k
+def _brute_topk(scores, L, k):
+    order = np.lexsort((np.arange(L), -scores[:L]))
+    out = np.full(k, -1, np.int32)
+    out[:min(k, L)] = order[:k]
+    return out
+
+
+@pytest.mark.parametrize("L,k", [(1, 4), (5, 8), (100, 8), (1000, 64), (4096, 2048)])
+def test_topk_brute_force_with_ties(oracle_mod, L, k):
+    rng = np.random.default_rng(L + k)
+    s = rng.integers(0, 20, (2, max(L, 1))).astype(np.float64)   # many exact ties
+    s[1] = rng.standard_normal(max(L, 1))
+    got = oracle_mod.topk(s, [L, L], k)
+    for r in range(2):
+        assert np.array_equal(got[r], _brute_topk(s[r], L, k))
+
+
+def test_topk_all_equal_and_signed_zero(oracle_mod):
+    s = np.zeros((2, 10))
+    s[1, ::2] = -0.0
+    got = oracle_mod.topk(s, [10, 10], 4)
+    assert np.array_equal(got[0], [0, 1, 2, 3])
+    assert np.array_equal(got[1], [0, 1, 2, 3])
+
+
+def test_topk_len_below_k_and_zero(oracle_mod):
+    s = np.array([[3.0, 1.0, 2.0, 9.0]])
+    assert np.array_equal(oracle_mod.topk(s, [3], 5)[0], [0, 2, 1, -1, -1])
+    assert np.array_equal(oracle_mod.topk(s, [0], 2)[0], [-1, -1])
+
+
+# ------------------------------------------------------------------ sparse MLA
+def _mla_case(rng, n, H):
+    codes = _e4m3(np.clip(rng.standard_normal((n, LAT)) * 100, -448, 448))
+    cache, bt = _latent_cache(codes)
+    q = _bf16_bits(rng.standard_normal((1, H, LAT)))
+    return codes, cache, bt, q
+
+
+def test_mla_dense_matches_sdpa(oracle_mod):
+    """All tokens selected: equals float64 scaled_dot_product_attention."""
+    rng = np.random.default_rng(5)
+    n, H, s_l, sm = 150, 4, 0.0123, 1 / math.sqrt(192)
+    codes, cache, bt, q = _mla_case(rng, n, H)
+    idx = np.arange(n, dtype=np.int32)[None]
+    out, lse = oracle_mod.sparse_mla(q, sm, cache, s_l, bt, [0], [n], idx)
+    L = torch.from_numpy(_e4m3_vals(codes)) * s_l
+    qd = torch.from_numpy(_bf16_vals(q[0]))
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qd[None, :, None, :].expand(1, H, 1, LAT), L[None, None].expand(1, H, n, LAT),
+        L[None, None, :, :V].expand(1, H, n, V), scale=sm)[0, :, 0]
+    assert np.allclose(out[0], ref.numpy(), rtol=1e-10, atol=1e-12)
+    ref_lse = torch.logsumexp(sm * (qd @ L.T), dim=-1)
+    assert np.allclose(lse[0], ref_lse.numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_mla_single_token_and_zero_query(oracle_mod):
+    rng = np.random.default_rng(6)
+    n, H, s_l = 80, 3, 0.5
+    codes, cache, bt, q = _mla_case(rng, n, H)
+    vals = _e4m3_vals(codes) * s_l
+    idx = np.full((1, 8), -1, np.int32)
+    idx[0, 5] = 71
+    out, _ = oracle_mod.sparse_mla(q, 0.1, cache, s_l, bt, [0], [n], idx)
+    assert np.array_equal(out[0], np.broadcast_to(vals[71, :V], (H, V)))
+    sel = np.array([3, 9, 64, 70], np.int32)
+    out0, lse0 = oracle_mod.sparse_mla(np.zeros_like(q), 0.1, cache, s_l, bt, [0], [n], sel[None])
+    assert np.allclose(out0[0], np.broadcast_to(vals[sel, :V].mean(0), (H, V)), rtol=1e-13)
+    assert np.allclose(lse0[0], math.log(4.0), rtol=1e-14)
+
+
+def test_mla_split_merge_by_lse(oracle_mod):
+    """Attention over A u B equals the LSE-weighted merge of A and B (exact softmax)."""
+    rng = np.random.default_rng(8)
+    n, H, s_l, sm = 200, 5, 0.02, 1 / math.sqrt(192)
+    codes, cache, bt, q = _mla_case(rng, n, H)
+    sel = rng.permutation(n)[:96].astype(np.int32)
+    full, lf = oracle_mod.sparse_mla(q, sm, cache, s_l, bt, [0], [n], sel[None])
+    a = np.where(np.arange(96) < 40, sel, -1).astype(np.int32)
+    b = np.where(np.arange(96) >= 40, sel, -1).astype(np.int32)
+    oa, la = oracle_mod.sparse_mla(q, sm, cache, s_l, bt, [0], [n], a[None])
+    ob, lb = oracle_mod.sparse_mla(q, sm, cache, s_l, bt, [0], [n], b[None])
+    lm = np.logaddexp(la, lb)
+    merged = np.exp(la - lm)[..., None] * oa + np.exp(lb - lm)[..., None] * ob
+    assert np.allclose(merged, full, rtol=1e-12, atol=1e-13)
+    assert np.allclose(lm, lf, rtol=1e-13)
+    # order of the selected slots does not matter
+    perm, lp = oracle_mod.sparse_mla(q, sm, cache, s_l, bt, [0], [n], sel[::-1].copy()[None])
+    assert np.allclose(perm, full, rtol=1e-12, atol=1e-13) and np.allclose(lp, lf, rtol=1e-13)
+
+
+def test_mla_empty_row(oracle_mod):
+    rng = np.random.default_rng(9)
+    codes, cache, bt, q = _mla_case(rng, 10, 2)
+    out, lse = oracle_mod.sparse_mla(q, 0.1, cache, 1.0, bt, [0], [0],
+                                     np.full((1, 4), -1, np.int32))
+    assert np.array_equal(out, np.zeros_like(out)) and np.all(np.isneginf(lse))
+
+
+def test_topk_equal_context_is_dense(oracle_mod):
+    """top-k with k >= context selects every token: sparse MLA == dense MLA."""
+    wl = inputs.Workload("pin", [180], [2], H=4, k=256, seed=11)
+    a = inputs.to_numpy(inputs.make_inputs(wl))
+    _, idx, out, lse = oracle_mod.decode_step(a, k=256)
+    dense = np.stack([np.where(np.arange(256) < L, np.arange(256), -1) for L in a["row_len"]])
+    od, ld = oracle_mod.sparse_mla(a["q"], a["softmax_scale"], a["latent_cache"],
+                                   a["latent_scale"], a["block_table"], a["row_req"],
+                                   a["row_len"], dense.astype(np.int32))
+    assert np.allclose(out, od, rtol=1e-12, atol=1e-13) and np.allclose(lse, ld, rtol=1e-13)
+
+
+# ------------------------------------------------------------------ byte model
+def test_byte_model_matches_pages():
+    g = {k: float(v[0]) for k, v in _read_golden("byte_model.txt").items()}
+    assert traffic.KEY_BYTES == g["index_key_bytes_per_token"]
+    assert traffic.LATENT_BYTES == g["latent_bytes_per_token"]
+    assert inputs.IDX_DIM * 2 == g["bf16_index_key_bytes_per_token"]
+    ctx = 131072
+    dense = ctx * traffic.dense_mla_bytes_per_token()
+    dsa = traffic.dsa_bytes(ctx, int(g["selected_tokens"]))
+    assert round(dense / 1e6, 1) == g["dense_bytes_128k"]
+    assert round(dsa / 1e6, 1) == g["dsa_bytes_128k"]
+    assert round(2 * ctx * 4 / 1e6) == g["index_scores_128k"]        # fp32, written + read
+    assert round(dense / dsa) == g["single_row_reduction_128k"]
+    four = ctx * traffic.KEY_BYTES + 4 * 2048 * traffic.LATENT_BYTES
+    assert round(dense / four) == g["four_row_saving_128k"]
+    assert round(traffic.dsa_bytes(1 << 20) / ((1 << 20) * 576), 2) == g[
+        "dsa_share_of_dense_long_context"]
+    assert 24 * traffic.LATENT_BYTES == g["kv_per_token_24_layers_k3_fp8"]
+    assert 24 * (traffic.LATENT_BYTES + traffic.KEY_BYTES) == g["kv_per_token_24_layers_k31_fp8"]
+
+
+def test_workload_bytes():
+    assert traffic.algorithmic_bytes(inputs.config(0)) == 1_763_456
+    assert traffic.algorithmic_bytes(inputs.config(1)) == 154_148_864
+    assert traffic.algorithmic_bytes(inputs.config(2)) == 638_590_976
+    assert traffic.algorithmic_bytes(inputs.config(3)) == 139_739_264
+    assert round(traffic.scan_bytes(inputs.config(2)) / 16 / 1e6, 1) == 34.6
+    assert inputs.config(4).row_lengths()[0] == 126_977    # row i sees tokens <= 126,976 + i
