@@ -1,0 +1,376 @@
+#!/usr/bin/env python
+"""Benchmark of one DSA decode step (indexer scan -> top-2048 -> sparse MLA).
+
+Metric: algorithmic HBM bytes moved per second (GB/s) by dsa_decode_step,
+whole job, inputs resident in HBM; also µs per layer-step and the fraction of
+the HBM roofline.  Algorithmic bytes = 132 B per context token of every
+request (index keys, read once for all its rows) + 576 B per selected latent
+row + queries + bf16 output.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl reference]
+
+N > 1 runs under torchrun, one rank per GPU, each rank stepping its own
+replica of the workload (independent requests: weak scaling, no data-path
+collective).  Rank 0 prints ONE JSON line.  `--impl reference` times the
+float64 CPU oracle instead (the only reference this method has), on a bounded
+sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dsa_sparse_attention_lightning_gb300 import inputs, traffic  # noqa: E402
+
+METRIC = "DSA decode-step µs/layer and achieved HBM GB/s vs 8 TB/s roofline, 1 GB300"
+L2_FLUSH_BYTES = 256 << 20
+KERNELS_PER_STEP = 6   # scan 1, top-k 3 (hist, collect, finalize), MLA 2 (split, combine)
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"dsa_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------- GPU arm
+def _step_fn(dsa, inp, wl, ws, out, lse):
+    def step():
+        dsa.dsa_decode_step(inp["q_idx"], inp["w"], inp["key_cache"], inp["latent_cache"],
+                            inp["latent_scale"], inp["block_table"], inp["row_req"],
+                            inp["row_len"], inp["q"], softmax_scale=inp["softmax_scale"],
+                            k=wl.k, q_scale=inp["q_idx_scale"], out=out, lse=lse, workspace=ws)
+    return step
+
+
+def _time_launches(fn, n, flush, stream):
+    """Mean device time (ms) of fn over n launches, L2 flushed before each."""
+    times = []
+    for _ in range(n):
+        flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.mean(times), times
+
+
+def rank_workload(config: int, rank: int) -> inputs.Workload:
+    """Rank r steps its own replica: same shape, its own seed (independent requests)."""
+    wl = inputs.config(config)
+    wl.seed = wl.seed + 1000 * rank
+    return wl
+
+
+def reduce_max_ms(total_ms: float, device) -> float:
+    """Max over ranks of the timed region (a control-path reduction, not data)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(total_ms)
+    t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step: int, world: int, steps: int, max_total_ms: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time."""
+    return bytes_per_step * world * steps / (max_total_ms * 1e-3) / 1e9
+
+
+def run_gpu(args):
+    rank, world, local = _dist()
+    import dsa_sparse_attention_lightning_gb300 as dsa
+    dsa.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = rank_workload(args.config, rank)
+    inp = inputs.make_inputs(wl, device=dev)
+    R, H = wl.R, wl.H
+    out = torch.empty((R, H, inputs.V_DIM), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(dsa.decode_step_workspace_size(wl.B, R, wl.max_pages, H, wl.k),
+                     dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = _step_fn(dsa, inp, wl, ws, out, lse)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    if dsa.check_device_status(ws) != 0:
+        raise RuntimeError("device status raised during warm-up")
+
+    # ---- timed region: K steps, L2 flushed (untimed) before each -------------
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        step_ms, _ = _time_launches(step, args.steps, flush, stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clock_info = clocks.summary()
+    total_ms = reduce_max_ms(step_ms * args.steps, dev)
+    bytes_step = traffic.algorithmic_bytes(wl)
+    value = whole_job_gbs(bytes_step, world, args.steps, total_ms)
+    ms_per_step = total_ms / args.steps
+
+    # ---- per-kernel timing of the step's stages (same inputs, same launches) --
+    scores = torch.empty((R, wl.max_pages * inputs.PAGE), dtype=torch.float32, device=dev)
+    idx = torch.empty((R, wl.k), dtype=torch.int32, device=dev)
+    ws_s = torch.empty(dsa.indexer_score_workspace_size(R), dtype=torch.uint8, device=dev)
+    ws_t = torch.empty(dsa.topk_workspace_size(R, scores.shape[1], wl.k), dtype=torch.uint8,
+                       device=dev)
+    ws_m = torch.empty(dsa.sparse_mla_workspace_size(R, H, wl.k), dtype=torch.uint8, device=dev)
+    stages = {
+        "indexer_scan": (lambda: dsa.dsa_indexer_score(
+            inp["q_idx"], inp["w"], inp["key_cache"], inp["block_table"], inp["row_req"],
+            inp["row_len"], q_scale=inp["q_idx_scale"], scores=scores, workspace=ws_s),
+            traffic.scan_bytes(wl) + R * inputs.IDX_HEADS * (inputs.IDX_DIM * 2 + 4)),
+        "topk": (lambda: dsa.dsa_topk(scores, inp["row_len"], wl.k, idx=idx, workspace=ws_t),
+                 None),
+        "sparse_mla": (lambda: dsa.dsa_sparse_mla_decode(
+            inp["q"], inp["latent_cache"], inp["latent_scale"], inp["block_table"],
+            inp["row_req"], inp["row_len"], idx, softmax_scale=inp["softmax_scale"], out=out,
+            lse=lse, workspace=ws_m),
+            traffic.gather_bytes(wl) + R * H * (inputs.LAT_DIM + inputs.V_DIM) * 2),
+    }
+    stage_ms = {}
+    for name, (fn, _) in stages.items():
+        for _ in range(3):
+            fn()
+        stage_ms[name] = _time_launches(fn, max(5, min(args.steps, 50)), flush, stream)[0]
+    dominant = max((n for n in stages if stages[n][1] is not None), key=lambda n: stage_ms[n])
+    hbm_peak, _, peak_kind = _peaks()
+    dom_bytes = stages[dominant][1]
+    achieved = dom_bytes / (stage_ms[dominant] * 1e-3) / 1e9
+    roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "stage_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
+                "step_frac_of_8TBs": round(bytes_step / (ms_per_step * 1e-3) / 8e12, 4),
+                "step_frac_of_measured": round(bytes_step / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
+                                               4)}
+
+    # ---- end to end through the public API with host buffers -----------------
+    host = {k: v.cpu().pin_memory() for k, v in inp.items()
+            if k in ("q_idx", "q_idx_scale", "w", "q", "block_table", "row_req", "row_len")
+            and v is not None}
+    dev_in = {k: inp[k] for k in host}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def e2e_step():
+        for k2, t in host.items():
+            dev_in[k2].copy_(t, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = _time_launches(e2e_step, max(5, min(args.steps, 50)), flush, stream)[0]
+    e2e_value = bytes_step * world / (e2e_ms * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, inp)
+
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "us_per_layer_step": round(ms_per_step * 1e3, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "requests": wl.B, "rows": R, "context": wl.ctx[0],
+                   "heads": H, "topk": wl.k, "algorithmic_bytes_per_step": bytes_step,
+                   "l2": "flushed before every timed step (256 MiB write, untimed)",
+                   "parallelism": f"replicas{world}"},
+        "clocks": clock_info,
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
+                "note": "per-step inputs (queries, head weights, block table, rows) copied from "
+                        "pinned host memory and outputs copied back inside the timed region; "
+                        "the KV caches are resident layer state"},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "gpu_launches": KERNELS_PER_STEP * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- CPU oracle
+def _oracle_sample(wl, inp_host, requests):
+    """Host inputs for the rows of the first `requests` requests (caches whole)."""
+    rows = [r for r in range(wl.R) if int(inp_host["row_req"][r]) < requests]
+    h = dict(inp_host)
+    for key in ("q_idx", "q_idx_scale", "w", "row_req", "row_len", "q"):
+        if h.get(key) is not None:
+            h[key] = np.ascontiguousarray(h[key][rows])
+    sample = inputs.Workload(wl.name + "_sample", wl.ctx[:requests], wl.rows[:requests], H=wl.H,
+                             k=wl.k, q_idx_fp8=wl.q_idx_fp8)
+    return h, sample
+
+
+def cpu_baseline(wl, inp, requests=1):
+    from oracle import oracle
+    host = inputs.to_numpy(inp)
+    h, sample = _oracle_sample(wl, host, requests)
+    t0 = time.perf_counter()
+    oracle.decode_step(h, k=wl.k)
+    dt = time.perf_counter() - t0
+    b = traffic.algorithmic_bytes(sample)
+    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"{requests} of {wl.B} requests ({sample.R} rows) of {wl.name}, full "
+                      f"step (scores, top-{wl.k}, attention), float64 C + OpenMP"}
+
+
+def run_reference(args):
+    rank, world, _ = _dist()
+    if rank != 0:
+        return
+    from oracle import oracle
+    oracle.build()
+    wl = inputs.config(args.config)
+    inp = inputs.make_inputs(wl, device="cpu")
+    host = inputs.to_numpy(inp)
+    h, sample = _oracle_sample(wl, host, 1)
+    for _ in range(min(args.warmup, 1)):
+        oracle.decode_step(h, k=wl.k)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.decode_step(h, k=wl.k)
+        times.append(time.perf_counter() - t0)
+    b = traffic.algorithmic_bytes(sample)
+    value = b * len(times) / sum(times) / 1e9
+    cpu = {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+           "kind": "oracle",
+           "sample": f"1 of {wl.B} requests ({sample.R} rows) of {wl.name} per step"}
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.mean(times), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "requests": wl.B, "rows": wl.R, "context": wl.ctx[0],
+                   "heads": wl.H, "topk": wl.k, "sample_requests": 1},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=1,
+                    help="0 tiny, 1 16x4 rows @32K (default), 2 16x4 @256K, 3 1 row @1M")
+    ap.add_argument("--impl", default="dsa", choices=["dsa", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "dsa":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,248 @@
+// dsa_api.cu -- the C ABI of libdsa (declared in include/dsa.h): host-side
+// argument validation, workspace carving and the launch sequence of each
+// entry point.  No allocation, no host synchronisation (except the explicit
+// status read), no global mutable state.
+#include <string.h>
+
+#include "dsa_common.cuh"
+
+using namespace dsa;
+
+namespace {
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+
+inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Scratch of the indexer scan beyond the status word (reserved per row for the
+// converted query and folded head weights).
+inline size_t scan_scratch_bytes(int R) {
+  return align_up((size_t)R * kIdxHeads * kIdxDim * 2) + align_up((size_t)R * kIdxHeads * 4) +
+         align_up((size_t)(R + 1) * 16);
+}
+
+inline int64_t score_ld(int max_pages) { return (int64_t)max_pages * kPage; }
+
+int check_rows(int B, int max_pages, const int32_t* block_table, const int32_t* row_req,
+               const int32_t* row_len, int R) {
+  if (R < 0 || B < 0 || max_pages < 0) return DSA_ERR_INVALID_ARG;
+  if (R > 0 && (B < 1 || !block_table || !row_req || !row_len)) return DSA_ERR_INVALID_ARG;
+  if (R > 65535) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
+}
+
+int check_workspace(void* ws, size_t have, size_t need) {
+  if (!ws || have < need || !aligned(ws, kAlign)) return DSA_ERR_WORKSPACE;
+  return DSA_OK;
+}
+
+int clear_status(void* ws, cudaStream_t st) {
+  return cudaMemsetAsync(ws, 0, 4, st) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+bool supported_heads(int H) { return H == 16 || H == 32 || H == 64 || H == 128; }
+
+}  // namespace
+
+extern "C" {
+
+int dsa_version(void) { return kVersion; }
+
+const char* dsa_status_string(int status) {
+  switch (status) {
+    case DSA_OK: return "ok";
+    case DSA_ERR_INVALID_ARG: return "invalid argument";
+    case DSA_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case DSA_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+    case DSA_ERR_CUDA: return "CUDA error";
+    case DSA_ERR_DEVICE_CHECK: return "a kernel found an out-of-range value in device memory";
+    default: return "unknown status";
+  }
+}
+
+int dsa_device_info(int* num_sms, int* cc_major, int* cc_minor) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+  int v = 0;
+  if (num_sms) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    *num_sms = v;
+  }
+  if (cc_major) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    *cc_major = v;
+  }
+  if (cc_minor) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    *cc_minor = v;
+  }
+  return DSA_OK;
+}
+
+// ---------------------------------------------------------------- Score
+size_t dsa_indexer_score_workspace_size(int R) {
+  if (R < 0) return 0;
+  return kStatusBytes + scan_scratch_bytes(R);
+}
+
+int dsa_indexer_score(const void* q_idx, int q_dtype, const float* q_scale, const float* w,
+                      const uint8_t* key_cache, int64_t num_pages, const int32_t* block_table,
+                      int B, int max_pages, const int32_t* row_req, const int32_t* row_len,
+                      int R, float* scores, int64_t ld, void* workspace, size_t ws_bytes,
+                      void* stream) {
+  int s = check_rows(B, max_pages, block_table, row_req, row_len, R);
+  if (s) return s;
+  if (q_dtype != DSA_BF16 && q_dtype != DSA_E4M3) return DSA_ERR_UNSUPPORTED;
+  if (R > 0 && (!q_idx || !w || !key_cache || !scores)) return DSA_ERR_INVALID_ARG;
+  if (q_dtype == DSA_E4M3 && R > 0 && !q_scale) return DSA_ERR_INVALID_ARG;
+  if (num_pages < 0 || ld < score_ld(max_pages) || ld % 4 != 0) return DSA_ERR_INVALID_ARG;
+  if (scores && !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
+  if (key_cache && !aligned(key_cache, 16)) return DSA_ERR_INVALID_ARG;
+  s = check_workspace(workspace, ws_bytes, dsa_indexer_score_workspace_size(R));
+  if (s) return s;
+  cudaStream_t st = as_stream(stream);
+  if ((s = clear_status(workspace, st))) return s;
+  if (R == 0) return DSA_OK;
+  ScanArgs a{q_idx, q_dtype, q_scale, w, key_cache, num_pages, block_table, B, max_pages,
+             row_req, row_len, R, scores, ld, static_cast<uint32_t*>(workspace)};
+  return to_status(launch_indexer_scan(a, st));
+}
+
+// ---------------------------------------------------------------- Select
+size_t dsa_topk_workspace_size(int R, int64_t max_len, int k) {
+  if (R < 0 || max_len < 0 || k < 1) return 0;
+  return kStatusBytes + TopkLayout(R, max_len).bytes;
+}
+
+int dsa_topk(const float* scores, int64_t ld, const int32_t* row_len, int R, int64_t max_len,
+             int k, int32_t* idx, void* workspace, size_t ws_bytes, void* stream) {
+  if (R < 0 || max_len < 0 || ld < max_len || ld % 4 != 0) return DSA_ERR_INVALID_ARG;
+  if (k < 1) return DSA_ERR_INVALID_ARG;
+  if (k > kMaxTopk) return DSA_ERR_UNSUPPORTED;
+  if (max_len > ((int64_t)1 << 31) - 1) return DSA_ERR_UNSUPPORTED;
+  if (R > 65535) return DSA_ERR_UNSUPPORTED;
+  if (R > 0 && (!scores || !row_len || !idx)) return DSA_ERR_INVALID_ARG;
+  if (scores && !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
+  int s = check_workspace(workspace, ws_bytes, dsa_topk_workspace_size(R, max_len, k));
+  if (s) return s;
+  cudaStream_t st = as_stream(stream);
+  if ((s = clear_status(workspace, st))) return s;
+  if (R == 0) return DSA_OK;
+  TopkArgs a{scores, ld, row_len, R, max_len, k, idx,
+             static_cast<uint8_t*>(workspace) + kStatusBytes, static_cast<uint32_t*>(workspace)};
+  return to_status(launch_topk(a, st));
+}
+
+// ---------------------------------------------------------------- Attend
+size_t dsa_sparse_mla_workspace_size(int R, int H, int k) {
+  if (R < 0 || H < 1 || k < 1) return 0;
+  return kStatusBytes + MlaLayout(R, H, k).bytes;
+}
+
+int dsa_sparse_mla_decode(const void* q, int H, float softmax_scale, const uint8_t* latent_cache,
+                          int64_t num_pages, float latent_scale, const int32_t* block_table,
+                          int B, int max_pages, const int32_t* row_req, const int32_t* row_len,
+                          const int32_t* idx, int k, int R, void* out, float* lse,
+                          void* workspace, size_t ws_bytes, void* stream) {
+  int s = check_rows(B, max_pages, block_table, row_req, row_len, R);
+  if (s) return s;
+  if (!supported_heads(H)) return DSA_ERR_UNSUPPORTED;
+  if (k < 1) return DSA_ERR_INVALID_ARG;
+  if (k > kMaxTopk) return DSA_ERR_UNSUPPORTED;
+  if (num_pages < 0) return DSA_ERR_INVALID_ARG;
+  if (R > 0 && (!q || !latent_cache || !idx || !out)) return DSA_ERR_INVALID_ARG;
+  if ((q && !aligned(q, 16)) || (latent_cache && !aligned(latent_cache, 16)) ||
+      (out && !aligned(out, 16)))
+    return DSA_ERR_INVALID_ARG;
+  s = check_workspace(workspace, ws_bytes, dsa_sparse_mla_workspace_size(R, H, k));
+  if (s) return s;
+  cudaStream_t st = as_stream(stream);
+  if ((s = clear_status(workspace, st))) return s;
+  if (R == 0) return DSA_OK;
+  MlaArgs a{q, H, softmax_scale, latent_cache, num_pages, latent_scale, block_table, B,
+            max_pages, row_req, row_len, idx, k, R, out, lse,
+            static_cast<uint8_t*>(workspace) + kStatusBytes, static_cast<uint32_t*>(workspace)};
+  return to_status(launch_sparse_mla(a, st));
+}
+
+// ---------------------------------------------------------------- fused step
+namespace {
+struct StepLayout {
+  size_t scores, idx, topk, mla, scan, bytes;
+  StepLayout(int R, int max_pages, int H, int k) {
+    size_t o = kStatusBytes;
+    scores = o; o = align_up(o + (size_t)R * score_ld(max_pages) * 4);
+    idx = o;    o = align_up(o + (size_t)R * k * 4);
+    scan = o;   o = align_up(o + scan_scratch_bytes(R));
+    topk = o;   o = align_up(o + TopkLayout(R, score_ld(max_pages)).bytes);
+    mla = o;    o = align_up(o + MlaLayout(R, H, k).bytes);
+    bytes = o;
+  }
+};
+}  // namespace
+
+size_t dsa_decode_step_workspace_size(int B, int R, int max_pages, int H, int k) {
+  if (B < 0 || R < 0 || max_pages < 0 || H < 1 || k < 1) return 0;
+  return StepLayout(R, max_pages, H, k).bytes;
+}
+
+int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const float* w,
+                    const uint8_t* key_cache, const uint8_t* latent_cache, int64_t num_pages,
+                    float latent_scale, const int32_t* block_table, int B, int max_pages,
+                    const int32_t* row_req, const int32_t* row_len, int R, const void* q, int H,
+                    float softmax_scale, int k, void* out, float* lse, int32_t* idx_out,
+                    void* workspace, size_t ws_bytes, void* stream) {
+  int s = check_rows(B, max_pages, block_table, row_req, row_len, R);
+  if (s) return s;
+  if (q_dtype != DSA_BF16 && q_dtype != DSA_E4M3) return DSA_ERR_UNSUPPORTED;
+  if (!supported_heads(H)) return DSA_ERR_UNSUPPORTED;
+  if (k < 1) return DSA_ERR_INVALID_ARG;
+  if (k > kMaxTopk) return DSA_ERR_UNSUPPORTED;
+  if (num_pages < 0) return DSA_ERR_INVALID_ARG;
+  if (R > 0 && (!q_idx || !w || !key_cache || !latent_cache || !q || !out))
+    return DSA_ERR_INVALID_ARG;
+  if (q_dtype == DSA_E4M3 && R > 0 && !q_scale) return DSA_ERR_INVALID_ARG;
+  if ((key_cache && !aligned(key_cache, 16)) || (latent_cache && !aligned(latent_cache, 16)) ||
+      (q && !aligned(q, 16)) || (out && !aligned(out, 16)))
+    return DSA_ERR_INVALID_ARG;
+  const StepLayout L(R, max_pages, H, k);
+  s = check_workspace(workspace, ws_bytes, L.bytes);
+  if (s) return s;
+  cudaStream_t st = as_stream(stream);
+  if ((s = clear_status(workspace, st))) return s;
+  if (R == 0) return DSA_OK;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint32_t* status = reinterpret_cast<uint32_t*>(ws);
+  float* scores = reinterpret_cast<float*>(ws + L.scores);
+  int32_t* idx = idx_out ? idx_out : reinterpret_cast<int32_t*>(ws + L.idx);
+  const int64_t ld = score_ld(max_pages);
+
+  ScanArgs sa{q_idx, q_dtype, q_scale, w, key_cache, num_pages, block_table, B, max_pages,
+              row_req, row_len, R, scores, ld, status};
+  cudaError_t e = launch_indexer_scan(sa, st);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  TopkArgs ta{scores, ld, row_len, R, ld, k, idx, ws + L.topk, status};
+  e = launch_topk(ta, st);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  MlaArgs ma{q, H, softmax_scale, latent_cache, num_pages, latent_scale, block_table, B,
+             max_pages, row_req, row_len, idx, k, R, out, lse, ws + L.mla, status};
+  return to_status(launch_sparse_mla(ma, st));
+}
+
+int dsa_check_device_status(const void* workspace, void* stream, uint32_t* bits) {
+  if (!workspace) return DSA_ERR_WORKSPACE;
+  uint32_t v = 0;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return DSA_ERR_CUDA;
+  if (cudaMemcpy(&v, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
+  if (bits) *bits = v;
+  return v ? DSA_ERR_DEVICE_CHECK : DSA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,127 @@
+// dsa_common.cuh -- shapes, workspace layout and small device helpers shared
+// by the kernels of libdsa (sm_103a).  Nothing here is shared with the CPU
+// oracle.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+
+namespace dsa {
+
+constexpr int kPage = DSA_PAGE_TOKENS;         // tokens per cache page
+constexpr int kIdxHeads = DSA_INDEX_HEADS;     // indexer heads
+constexpr int kIdxDim = DSA_INDEX_DIM;         // indexer head dim
+constexpr int kKeyPageBytes = DSA_KEY_PAGE_BYTES;
+constexpr int kKeyScaleOffset = kPage * kIdxDim;   // scales follow the 64 x 128 key bytes
+constexpr int kLatDim = DSA_LATENT_DIM;
+constexpr int kVDim = DSA_V_DIM;
+constexpr int kMaxTopk = DSA_MAX_TOPK;
+constexpr size_t kAlign = 256;
+constexpr size_t kStatusBytes = 256;           // device status word lives here
+
+// ---- top-k partitioning ------------------------------------------------
+constexpr int kTopkChunk = 4096;               // scores per collecting CTA
+constexpr int kTopkBins1 = 2048;               // first radix digit: key bits 31..21
+constexpr int kTopkBins2 = 2048;               // second digit: bits 20..10
+constexpr int kTopkBins3 = 1024;               // third digit: bits 9..0
+
+inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
+
+// Byte offsets of the top-k scratch inside a workspace region.
+struct TopkLayout {
+  size_t hist, thr, seg_count, items, bytes;
+  int nchunks;
+  TopkLayout(int R, int64_t max_len) {
+    nchunks = (int)((max_len + kTopkChunk - 1) / kTopkChunk);
+    if (nchunks < 1) nchunks = 1;
+    size_t o = 0;
+    hist = o;      o = align_up(o + (size_t)R * kTopkBins1 * 4);
+    thr = o;       o = align_up(o + (size_t)R * 8);
+    seg_count = o; o = align_up(o + (size_t)R * nchunks * 4);
+    items = o;     o = align_up(o + (size_t)R * nchunks * kTopkChunk * 8);
+    bytes = o;
+  }
+};
+
+// Split of the selected-token dimension over CTAs in sparse MLA: a fixed
+// function of (R, k) so that results do not depend on the device.
+inline int mla_num_splits(int R, int k) {
+  int by_rows = (304 + R - 1) / R;               // about two CTAs per SM of a 152-SM part
+  int by_k = (k + 63) / 64;                      // at least 64 slots per split
+  int s = by_rows < by_k ? by_rows : by_k;
+  if (s > 32) s = 32;
+  return s < 1 ? 1 : s;
+}
+
+struct MlaLayout {
+  size_t part_o, part_lse, bytes;
+  int nsplit;
+  MlaLayout(int R, int H, int k) {
+    nsplit = mla_num_splits(R, k);
+    size_t o = 0;
+    part_o = o;   o = align_up(o + (size_t)R * nsplit * H * kVDim * 4);
+    part_lse = o; o = align_up(o + (size_t)R * nsplit * H * 4);
+    bytes = o;
+  }
+};
+
+// ---- device helpers ----------------------------------------------------
+__device__ __forceinline__ void raise_dev(uint32_t* status, uint32_t bit) {
+  if (status) atomicOr(status, bit);
+}
+
+// Two E4M3 bytes (low byte first) -> two floats, exact (E4M3 is a subset of f16).
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t v) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
+  __half2 hh = *reinterpret_cast<__half2*>(&h);
+  return __half22float2(hh);
+}
+
+__device__ __forceinline__ float e4m3_to_float(uint8_t v) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)v, __NV_E4M3);
+  return __half2float(*reinterpret_cast<__half*>(&h));
+}
+
+// Order-preserving map of a finite fp32 to uint32 (larger value -> larger key);
+// -0 maps like +0.
+__device__ __forceinline__ uint32_t ordered_key(float f) {
+  uint32_t u = __float_as_uint(f);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+}  // namespace dsa
+
+// ---- launchers (host side, one per kernel family) --------------------------
+namespace dsa {
+
+struct ScanArgs {
+  const void* q_idx; int q_dtype; const float* q_scale; const float* w;
+  const uint8_t* key_cache; int64_t num_pages; const int32_t* block_table; int B; int max_pages;
+  const int32_t* row_req; const int32_t* row_len; int R; float* scores; int64_t ld;
+  uint32_t* status;
+};
+cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st);
+
+struct TopkArgs {
+  const float* scores; int64_t ld; const int32_t* row_len; int R; int64_t max_len; int k;
+  int32_t* idx; uint8_t* scratch;  // TopkLayout(R, max_len).bytes bytes
+  uint32_t* status;
+};
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st);
+
+struct MlaArgs {
+  const void* q; int H; float softmax_scale; const uint8_t* latent_cache; int64_t num_pages;
+  float latent_scale; const int32_t* block_table; int B; int max_pages; const int32_t* row_req;
+  const int32_t* row_len; const int32_t* idx; int k; int R; void* out; float* lse;
+  uint8_t* scratch;  // MlaLayout(R, H, k).bytes bytes
+  uint32_t* status;
+};
+cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t st);
+
+}  // namespace dsa

@@ -1,0 +1,197 @@
+/*
+ * dsa.h -- C ABI of libdsa: one decode step of a DSA (DeepSeek-style sparse
+ * attention) layer, as in Kimi K3.1 Pro's Gated Sparse-MLA layers, on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The step is the pages' Score -> Select -> Attend (TokenSpeed post on Kimi
+ * K3.1 Pro, "Integrating sparse attention with the K3 stack", steps 2-4):
+ *   1. the lightning indexer scores every visible token of a query row with
+ *      32 heads x 128 dims against one FP8 E4M3 index key per token (vLLM
+ *      Day-0 post, "What Kimi K3.1 Pro changes"), in the DeepSeek-V3.2 form
+ *        score(r, s) = sum_h w[r,h] * ReLU( (q[r,h] . k[s]) * ks[s] );
+ *   2. the k = 2048 best tokens of each row are kept, ties to the lower
+ *      token index (SGLang Day-0 post, "What's new in Kimi K3.1 Pro");
+ *   3. exact MLA attention, MQA style, runs over only the selected tokens'
+ *      576-wide FP8 latent rows, the first 512 dims doubling as the value
+ *      (AMD Instinct post, overview table "MLA"; vLLM post, "What Kimi K3.1
+ *      Pro changes": attention runs exactly over only those tokens).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer argument is DEVICE memory owned by the caller unless a
+ *    comment says otherwise.  The library never allocates, frees or keeps a
+ *    pointer after a call returns.  Inputs are only read; outputs never alias
+ *    inputs.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Every call only enqueues work on that stream and returns; it
+ *    never synchronises, except dsa_check_device_status.
+ *  - Scratch memory comes from the caller's `workspace` (device memory, 256-byte
+ *    aligned) of at least the size the matching *_workspace_size function
+ *    returns.  A workspace must not be shared by calls that may overlap on the
+ *    GPU.  Its first 256 bytes hold the device-side status word.
+ *  - Every call returns a status (DSA_OK = 0).  Arguments are validated on the
+ *    host before anything is launched; an invalid argument launches nothing.
+ *    Values that live in device memory (row lengths, request ids, block-table
+ *    entries, selected indices) are checked by the kernels: an out-of-range
+ *    value is skipped, never dereferenced, and raises a bit in the workspace
+ *    status word, read back with dsa_check_device_status.
+ *
+ * Cache layouts (token s of request b lives in page block_table[b][s / 64],
+ * slot s % 64; both caches share one block table, as the TokenSpeed post's
+ * "Storing index keys in the flat KV cache" keeps the index-key plane next to
+ * the latent rows of the same page):
+ *  - key_cache    uint8 [num_pages][8448]: 64 x 128 E4M3 key bytes (token
+ *                 major), then 64 fp32 key scales (little endian).  132 B per
+ *                 token: 128 FP8 values and one four-byte scale.
+ *  - latent_cache uint8 [num_pages][64][576]: E4M3 latent rows; one fp32
+ *                 scale `latent_scale` for the whole cache.
+ *  - block_table  int32 [B][max_pages], row-major.
+ * Query rows: row_req[R] (request of each row) and row_len[R] (tokens row r
+ * sees: 0 <= row_len[r] <= max_pages * 64).  Rows of one request that are
+ * adjacent in the row order share one read of the request's index keys.
+ */
+#ifndef DSA_H
+#define DSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define DSA_OK 0
+#define DSA_ERR_INVALID_ARG 1  /* null pointer, negative size, bad stride   */
+#define DSA_ERR_UNSUPPORTED 2  /* shape not built (H, k, dtype)              */
+#define DSA_ERR_WORKSPACE 3    /* workspace missing, too small or unaligned  */
+#define DSA_ERR_CUDA 4         /* a CUDA launch or query failed              */
+#define DSA_ERR_DEVICE_CHECK 5 /* a kernel found an out-of-range device value */
+
+/* bits of the device status word (dsa_check_device_status) */
+#define DSA_DEV_BAD_ROW 0x1   /* row_req outside [0,B) or row_len outside [0, max_pages*64] */
+#define DSA_DEV_BAD_PAGE 0x2  /* block-table entry outside [0, num_pages)   */
+#define DSA_DEV_BAD_INDEX 0x4 /* selected index >= row_len                   */
+
+/* ---- fixed shapes ------------------------------------------------------ */
+#define DSA_PAGE_TOKENS 64
+#define DSA_INDEX_HEADS 32
+#define DSA_INDEX_DIM 128
+#define DSA_KEY_PAGE_BYTES 8448
+#define DSA_LATENT_DIM 576
+#define DSA_V_DIM 512
+#define DSA_MAX_TOPK 2048
+
+/* indexer query element types */
+#define DSA_BF16 0 /* bf16 [R][32][128]                                     */
+#define DSA_E4M3 1 /* E4M3 [R][32][128] with one fp32 scale per (row, head) */
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int dsa_version(void);
+
+/* Static, human-readable text for a status code. */
+const char* dsa_status_string(int status);
+
+/* Number of SMs and whether the current device is an sm_103 part; host-only
+ * query of the current device.  Returns DSA_OK or DSA_ERR_CUDA. */
+int dsa_device_info(int* num_sms, int* cc_major, int* cc_minor);
+
+/* ------------------------------------------------------------------------
+ * dsa_indexer_score -- step 1 alone (Score).
+ *
+ * scores[r][s] = sum_{h<32} w[r][h] * max(0, (q[r][h] . key[s]) * ks[s]) for
+ * 0 <= s < row_len[r], fp32, where key[s] is the E4M3 key of token s of
+ * request row_req[r] and ks[s] its fp32 scale (TokenSpeed post, step 2
+ * "Score"; vLLM post, "What Kimi K3.1 Pro changes": 32 heads x 128 dims).
+ *
+ *  q_idx    [R][32][128] bf16 (q_dtype DSA_BF16) or E4M3 (DSA_E4M3).
+ *  q_scale  fp32 [R][32] for DSA_E4M3 (q = code * q_scale), NULL for bf16.
+ *  w        fp32 [R][32] head weights (any sign).
+ *  scores   fp32 [R][ld], ld >= max_pages * 64 and a multiple of 4; only
+ *           entries s < row_len[r] are written.
+ *  workspace >= dsa_indexer_score_workspace_size(R) bytes.
+ * Errors: DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED (unknown q_dtype),
+ * DSA_ERR_WORKSPACE, DSA_ERR_CUDA; device-side DSA_DEV_BAD_ROW/BAD_PAGE.
+ * ---------------------------------------------------------------------- */
+size_t dsa_indexer_score_workspace_size(int R);
+int dsa_indexer_score(const void* q_idx, int q_dtype, const float* q_scale, const float* w,
+                      const uint8_t* key_cache, int64_t num_pages, const int32_t* block_table,
+                      int B, int max_pages, const int32_t* row_req, const int32_t* row_len,
+                      int R, float* scores, int64_t ld, void* workspace, size_t ws_bytes,
+                      void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsa_topk -- step 2 alone (Select).
+ *
+ * For each row r: the min(k, row_len[r]) positions s in [0, row_len[r]) with
+ * the largest scores[r][s], ties broken towards the lower position (a
+ * radix top-k keeps the k highest-scoring positions per query: TokenSpeed
+ * post, step 3 "Select").  Scores compare as fp32 values; -0 equals +0.
+ * idx[r][0..k) receives the selected positions in ASCENDING position order,
+ * followed by -1 padding.  The result is unique, so it is deterministic.
+ *
+ *  scores  fp32 [R][ld] (only [0, row_len[r]) is read); inputs must be finite.
+ *  max_len upper bound of row_len (host value), <= ld.
+ *  k       1..2048.
+ *  idx     int32 [R][k].
+ * Errors: DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED (k > 2048),
+ * DSA_ERR_WORKSPACE, DSA_ERR_CUDA; device-side DSA_DEV_BAD_ROW.
+ * ---------------------------------------------------------------------- */
+size_t dsa_topk_workspace_size(int R, int64_t max_len, int k);
+int dsa_topk(const float* scores, int64_t ld, const int32_t* row_len, int R, int64_t max_len,
+             int k, int32_t* idx, void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsa_sparse_mla_decode -- step 3 alone (Attend).
+ *
+ * For row r, head h and the valid selected tokens j (0 <= idx[r][j] <
+ * row_len[r]; negative entries are padding and are skipped):
+ *   L_j = dec(latent_cache row of token idx[r][j]) * latent_scale
+ *   x_j = softmax_scale * (q[r][h] . L_j)           (576 dims)
+ *   out[r][h][:] = sum_j softmax(x)_j * L_j[0:512]   (bf16, round to nearest)
+ *   lse[r][h]    = ln sum_j exp(x_j)                  (fp32, natural log)
+ * (vLLM post, "What Kimi K3.1 Pro changes": MLA attention runs exactly over
+ * only the selected tokens; TokenSpeed post, "Sparse attention in Kimi K3.1
+ * Pro": every attention head attends to the selected tokens.)  A row with no
+ * valid token gets out = 0 and lse = -inf.
+ *
+ *  q       bf16 [R][H][576]; H in {16, 32, 64, 128}.
+ *  idx     int32 [R][k], k in 1..2048 (e.g. the output of dsa_topk).
+ *  out     bf16 [R][H][512].   lse  fp32 [R][H] or NULL.
+ * Errors: DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED (H or k), DSA_ERR_WORKSPACE,
+ * DSA_ERR_CUDA; device-side DSA_DEV_BAD_ROW/BAD_PAGE/BAD_INDEX.
+ * ---------------------------------------------------------------------- */
+size_t dsa_sparse_mla_workspace_size(int R, int H, int k);
+int dsa_sparse_mla_decode(const void* q, int H, float softmax_scale, const uint8_t* latent_cache,
+                          int64_t num_pages, float latent_scale, const int32_t* block_table,
+                          int B, int max_pages, const int32_t* row_req, const int32_t* row_len,
+                          const int32_t* idx, int k, int R, void* out, float* lse,
+                          void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsa_decode_step -- the whole step (Score -> Select -> Attend), fused into
+ * one launch sequence on `stream` with no host round trip.  Arguments mean
+ * what they mean above; the scores never leave the workspace.
+ *  idx_out  optional int32 [R][k]: receives the selection (ascending, -1
+ *           padded), e.g. for tests; NULL to skip.
+ *  workspace >= dsa_decode_step_workspace_size(B, R, max_pages, H, k).
+ * ---------------------------------------------------------------------- */
+size_t dsa_decode_step_workspace_size(int B, int R, int max_pages, int H, int k);
+int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const float* w,
+                    const uint8_t* key_cache, const uint8_t* latent_cache, int64_t num_pages,
+                    float latent_scale, const int32_t* block_table, int B, int max_pages,
+                    const int32_t* row_req, const int32_t* row_len, int R, const void* q, int H,
+                    float softmax_scale, int k, void* out, float* lse, int32_t* idx_out,
+                    void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, then reads the device status word in `workspace`
+ * (bits DSA_DEV_*, written by the kernels of the last call that used this
+ * workspace) into *bits (may be NULL).  Returns DSA_OK when no bit is set,
+ * DSA_ERR_DEVICE_CHECK when one is, DSA_ERR_CUDA when the copy fails. */
+int dsa_check_device_status(const void* workspace, void* stream, uint32_t* bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H */

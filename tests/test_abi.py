@@ -1,0 +1,99 @@
+"""CPU-only checks of the C ABI: the library builds, loads and exports every
+symbol include/dsa.h declares, workspace sizes are consistent, and invalid
+arguments are rejected on the host before anything touches a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dsa_sparse_attention_lightning_gb300 import _build, _lib
+    _build.build()
+    return _lib.load()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(dsa_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_entry_points():
+    names = declared_symbols()
+    for n in ("dsa_indexer_score", "dsa_topk", "dsa_sparse_mla_decode", "dsa_decode_step",
+              "dsa_topk_workspace_size", "dsa_check_device_status"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from dsa_sparse_attention_lightning_gb300 import _lib
+    bound = {n for n, _, _ in _lib.SIGNATURES}
+    for name in declared_symbols():
+        assert hasattr(lib, name), f"libdsa.so does not export {name}"
+        assert name in bound, f"python binding does not bind {name}"
+
+
+def test_version_and_status_strings(lib):
+    assert lib.dsa_version() >= 10000
+    for s in range(6):
+        assert lib.dsa_status_string(s)
+    assert lib.dsa_status_string(0) == b"ok"
+
+
+def test_workspace_sizes(lib):
+    assert lib.dsa_topk_workspace_size(4, 1000, 64) >= 256 + 4 * 2048 * 4
+    assert lib.dsa_topk_workspace_size(8, 1 << 20, 2048) > lib.dsa_topk_workspace_size(8, 1 << 10, 2048)
+    assert lib.dsa_sparse_mla_workspace_size(64, 64, 2048) >= 64 * 64 * 512 * 4
+    assert lib.dsa_decode_step_workspace_size(16, 64, 512, 64, 2048) >= \
+        lib.dsa_topk_workspace_size(64, 512 * 64, 2048)
+    assert lib.dsa_indexer_score_workspace_size(-1) == 0
+    assert lib.dsa_topk_workspace_size(4, 100, 0) == 0
+
+
+FAKE = ctypes.c_void_p(1 << 20)   # aligned, never dereferenced: validation fails first
+
+
+def test_topk_rejects_bad_arguments(lib):
+    ws_need = lib.dsa_topk_workspace_size(2, 128, 16)
+    # k out of range
+    assert lib.dsa_topk(FAKE, 128, FAKE, 2, 128, 0, FAKE, FAKE, ws_need, None) == 1
+    assert lib.dsa_topk(FAKE, 128, FAKE, 2, 128, 4096, FAKE, FAKE, ws_need, None) == 2
+    # ld smaller than max_len, or not a multiple of 4
+    assert lib.dsa_topk(FAKE, 64, FAKE, 2, 128, 16, FAKE, FAKE, ws_need, None) == 1
+    assert lib.dsa_topk(FAKE, 130, FAKE, 2, 128, 16, FAKE, FAKE, ws_need, None) == 1
+    # missing pointers, missing or small workspace
+    assert lib.dsa_topk(None, 128, FAKE, 2, 128, 16, FAKE, FAKE, ws_need, None) == 1
+    assert lib.dsa_topk(FAKE, 128, FAKE, 2, 128, 16, FAKE, None, ws_need, None) == 3
+    assert lib.dsa_topk(FAKE, 128, FAKE, 2, 128, 16, FAKE, FAKE, ws_need - 1, None) == 3
+    assert lib.dsa_topk(FAKE, 128, FAKE, 2, 128, 16, FAKE, ctypes.c_void_p((1 << 20) + 8),
+                        ws_need, None) == 3
+
+
+def test_mla_and_step_reject_bad_shapes(lib):
+    ws = lib.dsa_sparse_mla_workspace_size(1, 64, 64)
+    args = lambda H, k: (FAKE, H, 0.1, FAKE, 4, 1.0, FAKE, 1, 4, FAKE, FAKE, FAKE, k, 1, FAKE,
+                         None, FAKE, ws, None)
+    assert lib.dsa_sparse_mla_decode(*args(48, 64)) == 2       # H not built
+    assert lib.dsa_sparse_mla_decode(*args(64, 4096)) == 2     # k > 2048
+    assert lib.dsa_sparse_mla_decode(*args(64, 0)) == 1
+    wss = lib.dsa_decode_step_workspace_size(1, 1, 4, 64, 64)
+    step = lambda qt, H: (FAKE, qt, None, FAKE, FAKE, FAKE, 4, 1.0, FAKE, 1, 4, FAKE, FAKE, 1,
+                          FAKE, H, 0.1, 64, FAKE, None, None, FAKE, wss, None)
+    assert lib.dsa_decode_step(*step(7, 64)) == 2              # unknown q dtype
+    assert lib.dsa_decode_step(*step(1, 64)) == 1              # E4M3 without q_scale
+    assert lib.dsa_decode_step(*step(0, 24)) == 2
+    assert lib.dsa_indexer_score(FAKE, 0, None, FAKE, FAKE, 4, FAKE, 1, 4, FAKE, FAKE, 1, FAKE,
+                                 100, FAKE, 1 << 20, None) == 1   # ld < max_pages * 64
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from dsa_sparse_attention_lightning_gb300 import _lib
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(ImportError):
+        _lib.load()

@@ -1,0 +1,257 @@
+"""GPU parity: every entry point of the C ABI against the float64 oracle on the
+same seeded inputs, element by element at sizes the oracle finishes in
+seconds (several tiles, ragged tails), and on sampled rows at the
+benchmark's full sizes."""
+import numpy as np
+import pytest
+import torch
+
+import helpers
+from dsa_sparse_attention_lightning_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import dsa_sparse_attention_lightning_gb300 as m
+    from dsa_sparse_attention_lightning_gb300 import _build
+    _build.build()
+    m.load()
+    return m
+
+
+DEV = "cuda"
+
+SMALL = [
+    inputs.Workload("one_row_4k", [4096], [1], H=16, seed=0, paged=False),
+    inputs.Workload("ragged_multi", [3000, 700, 5000, 64], [2, 1, 4, 1], H=64, k=512, seed=1,
+                    shift_frac=0.05),
+    inputs.Workload("short_rows", [1, 63, 65, 2047, 2049], [1, 1, 2, 1, 3], H=32, seed=2),
+    inputs.Workload("h128", [9000], [3], H=128, k=1024, seed=3, shift_frac=0.05),
+    inputs.Workload("fp8_query", [6000, 2500], [4, 2], H=64, k=2048, seed=4, q_idx_fp8=True),
+]
+
+
+def _sub(host, rows):
+    """Host inputs restricted to the given rows (caches and block table unchanged)."""
+    h = dict(host)
+    for key in ("q_idx", "q_idx_scale", "w", "row_req", "row_len", "q"):
+        if h.get(key) is not None:
+            h[key] = np.ascontiguousarray(h[key][rows])
+    return h
+
+
+def _run_step(dsa, inp, k, **kw):
+    R = inp["row_len"].shape[0]
+    idx = torch.full((R, k), -7, dtype=torch.int32, device=DEV)
+    out, lse = dsa.dsa_decode_step(inp["q_idx"], inp["w"], inp["key_cache"], inp["latent_cache"],
+                                   inp["latent_scale"], inp["block_table"], inp["row_req"],
+                                   inp["row_len"], inp["q"], softmax_scale=inp["softmax_scale"],
+                                   k=k, q_scale=inp["q_idx_scale"], idx_out=idx, **kw)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+# ------------------------------------------------------------------ scores
+@pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
+def test_indexer_scores_match_oracle(dsa, oracle_mod, wl):
+    inp = inputs.make_inputs(wl, device=DEV)
+    scores = dsa.dsa_indexer_score(inp["q_idx"], inp["w"], inp["key_cache"], inp["block_table"],
+                                   inp["row_req"], inp["row_len"], q_scale=inp["q_idx_scale"])
+    torch.cuda.synchronize()
+    host = inputs.to_numpy(inp)
+    ora = oracle_mod.indexer_scores(host["q_idx"], host["w"], host["key_cache"],
+                                    host["block_table"], host["row_req"], host["row_len"],
+                                    q_scale=host["q_idx_scale"])
+    helpers.assert_scores_close(scores.cpu().numpy(), ora, host["row_len"])
+
+
+# ------------------------------------------------------------------- top-k
+def _topk_bitexact(dsa, oracle_mod, scores32, row_len, k):
+    R, ld = scores32.shape
+    ld4 = (ld + 3) // 4 * 4
+    buf = np.zeros((R, ld4), np.float32)
+    buf[:, :ld] = scores32
+    g = dsa.dsa_topk(torch.from_numpy(buf).to(DEV), torch.tensor(row_len, dtype=torch.int32,
+                                                                 device=DEV), k)
+    torch.cuda.synchronize()
+    g = g.cpu().numpy()
+    o = oracle_mod.topk(buf.astype(np.float64), row_len, k)
+    for r in range(R):
+        gs = g[r]
+        n = min(k, row_len[r])
+        assert np.all(gs[n:] == -1), f"row {r}: padding"
+        assert np.all(np.diff(gs[:n]) > 0), f"row {r}: not ascending"
+        assert np.array_equal(gs[:n], np.sort(o[r, :n])), f"row {r}: selection differs"
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
+def test_topk_bitexact_on_oracle_scores(dsa, oracle_mod, wl):
+    host = inputs.to_numpy(inputs.make_inputs(wl, device="cpu"))
+    ora = oracle_mod.indexer_scores(host["q_idx"], host["w"], host["key_cache"],
+                                    host["block_table"], host["row_req"], host["row_len"],
+                                    q_scale=host["q_idx_scale"])
+    s32 = np.nan_to_num(ora, nan=0.0).astype(np.float32)
+    _topk_bitexact(dsa, oracle_mod, s32, list(host["row_len"]), wl.k)
+
+
+def test_topk_ties_signs_and_edges(dsa, oracle_mod):
+    rng = np.random.default_rng(0)
+    L = 20000
+    rows = [
+        rng.integers(0, 50, L).astype(np.float32),          # heavy exact ties at the cut
+        np.zeros(L, np.float32),                            # all equal
+        np.where(rng.random(L) < 0.5, -0.0, 0.0).astype(np.float32),
+        -np.abs(rng.standard_normal(L)).astype(np.float32),  # all negative
+        rng.standard_normal(L).astype(np.float32),
+        np.full(L, 3.0, np.float32),
+        rng.standard_normal(L).astype(np.float32) * 1e-30,  # subnormal-adjacent scale
+        rng.integers(0, 3, L).astype(np.float32) * 1e6,
+    ]
+    s = np.stack(rows)
+    lens = [L, L, L, L, 2048, 2049, 4097, 1]
+    for k in (2048, 1, 7, 1000):
+        _topk_bitexact(dsa, oracle_mod, s, lens, k)
+    _topk_bitexact(dsa, oracle_mod, s[:2], [0, 5], 16)
+
+
+def test_topk_long_row_split_over_chunks(dsa, oracle_mod):
+    rng = np.random.default_rng(1)
+    L = 1 << 20
+    s = rng.standard_normal((1, L)).astype(np.float32)
+    s[0, rng.choice(L, 3000, replace=False)] = 5.5      # 3000 exact ties straddling the cut
+    _topk_bitexact(dsa, oracle_mod, s, [L], 2048)
+
+
+# --------------------------------------------------------------- sparse MLA
+@pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
+def test_sparse_mla_matches_oracle(dsa, oracle_mod, wl):
+    inp = inputs.make_inputs(wl, device=DEV)
+    host = inputs.to_numpy(inp)
+    rng = np.random.default_rng(wl.seed)
+    idx = np.full((wl.R, wl.k), -1, np.int32)
+    for r, L in enumerate(host["row_len"]):
+        n = min(wl.k, L)
+        sel = rng.choice(L, n, replace=False).astype(np.int32) if L else np.zeros(0, np.int32)
+        pos = rng.choice(wl.k, n, replace=False)       # valid ids scattered among -1 slots
+        idx[r, pos] = sel
+    out, lse = dsa.dsa_sparse_mla_decode(inp["q"], inp["latent_cache"], inp["latent_scale"],
+                                         inp["block_table"], inp["row_req"], inp["row_len"],
+                                         torch.from_numpy(idx).to(DEV),
+                                         softmax_scale=inp["softmax_scale"])
+    torch.cuda.synchronize()
+    oo, ol = oracle_mod.sparse_mla(host["q"], host["softmax_scale"], host["latent_cache"],
+                                   host["latent_scale"], host["block_table"], host["row_req"],
+                                   host["row_len"], idx)
+    helpers.assert_out_close(out.float().cpu().numpy(), oo)
+    lg = lse.cpu().numpy()
+    fin = np.isfinite(ol)
+    assert np.array_equal(fin, np.isfinite(lg))
+    assert np.allclose(lg[fin], ol[fin], rtol=1e-4, atol=1e-4)
+
+
+def test_sparse_mla_dense_equivalence(dsa, oracle_mod):
+    """k >= context: the step's sparse attention equals dense MLA over every token."""
+    wl = inputs.Workload("dense", [1500, 900], [2, 1], H=64, k=2048, seed=9)
+    inp = inputs.make_inputs(wl, device=DEV)
+    idx, out, lse = _run_step(dsa, inp, wl.k)
+    host = inputs.to_numpy(inp)
+    dense = np.full((wl.R, wl.k), -1, np.int32)
+    for r, L in enumerate(host["row_len"]):
+        dense[r, :L] = np.arange(L)
+        assert np.array_equal(idx[r], dense[r])
+    od, ld = oracle_mod.sparse_mla(host["q"], host["softmax_scale"], host["latent_cache"],
+                                   host["latent_scale"], host["block_table"], host["row_req"],
+                                   host["row_len"], dense)
+    helpers.assert_out_close(out, od)
+    assert np.allclose(lse, ld, rtol=1e-4, atol=1e-4)
+
+
+# ------------------------------------------------------------ fused step
+@pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
+def test_decode_step_matches_oracle(dsa, oracle_mod, wl):
+    inp = inputs.make_inputs(wl, device=DEV)
+    idx, out, lse = _run_step(dsa, inp, wl.k)
+    host = inputs.to_numpy(inp)
+    scores, oidx, oout, olse = oracle_mod.decode_step(host, k=wl.k)
+    helpers.assert_topk_equal_outside_near_ties(idx, oidx, scores, host["row_len"], wl.k)
+    # attention is compared on the GPU's own selection (the oracle attends over it)
+    oo, ol = oracle_mod.sparse_mla(host["q"], host["softmax_scale"], host["latent_cache"],
+                                   host["latent_scale"], host["block_table"], host["row_req"],
+                                   host["row_len"], idx)
+    helpers.assert_out_close(out, oo)
+    for r in range(wl.R):
+        if helpers.selected(idx[r]) == helpers.selected(oidx[r]):
+            helpers.assert_out_close(out[r], oout[r])
+
+
+def test_decode_step_deterministic_and_batch_invariant(dsa):
+    wl = inputs.Workload("inv", [5000, 3000, 7000], [4, 1, 2], H=64, seed=12, shift_frac=0.05)
+    inp = inputs.make_inputs(wl, device=DEV)
+    a = _run_step(dsa, inp, wl.k)
+    b = _run_step(dsa, inp, wl.k)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+    # rows 4 (request 1) alone: same selection, same output
+    sub = dict(inp)
+    for key in ("q_idx", "w", "row_req", "row_len", "q"):
+        sub[key] = inp[key][4:5].contiguous()
+    c = _run_step(dsa, sub, wl.k)
+    assert np.array_equal(c[0][0], a[0][4])
+    assert np.abs(c[1][0] - a[1][4]).max() <= 1e-2
+
+
+def test_device_checks_flag_bad_values(dsa):
+    wl = inputs.Workload("bad", [300], [1], H=16, k=64, seed=13)
+    inp = inputs.make_inputs(wl, device=DEV)
+    ws = torch.empty(dsa.decode_step_workspace_size(1, 1, wl.max_pages, 16, 64), dtype=torch.uint8,
+                     device=DEV)
+    bt = inp["block_table"].clone()
+    bt[0, 2] = 10_000_000                        # page id out of range
+    dsa.dsa_decode_step(inp["q_idx"], inp["w"], inp["key_cache"], inp["latent_cache"],
+                        inp["latent_scale"], bt, inp["row_req"], inp["row_len"], inp["q"],
+                        softmax_scale=inp["softmax_scale"], k=64, workspace=ws)
+    assert dsa.check_device_status(ws) & 0x2
+    idx = torch.tensor([[0, 5, 299, 300, -1]], dtype=torch.int32, device=DEV)   # 300 >= len
+    wsm = torch.empty(dsa.sparse_mla_workspace_size(1, 16, 5), dtype=torch.uint8, device=DEV)
+    dsa.dsa_sparse_mla_decode(inp["q"], inp["latent_cache"], inp["latent_scale"],
+                              inp["block_table"], inp["row_req"], inp["row_len"], idx,
+                              softmax_scale=inp["softmax_scale"], workspace=wsm)
+    assert dsa.check_device_status(wsm) & 0x4
+    # a clean call clears the word
+    dsa.dsa_decode_step(inp["q_idx"], inp["w"], inp["key_cache"], inp["latent_cache"],
+                        inp["latent_scale"], inp["block_table"], inp["row_req"], inp["row_len"],
+                        inp["q"], softmax_scale=inp["softmax_scale"], k=64, workspace=ws)
+    assert dsa.check_device_status(ws) == 0
+
+
+# ----------------------------------------------- full benchmark sizes, sampled
+FULL = [1, 2, 3]
+
+
+@pytest.mark.parametrize("ci", FULL, ids=[inputs.config(i).name for i in FULL])
+def test_full_size_sampled_rows(dsa, oracle_mod, ci):
+    wl = inputs.config(ci)
+    inp = inputs.make_inputs(wl, device=DEV)
+    idx, out, lse = _run_step(dsa, inp, wl.k)
+    host = inputs.to_numpy(inp)
+    rows = sorted({0, wl.R - 1, wl.R // 2, 1 % wl.R})
+    sub = _sub(host, rows)
+    scores, oidx, _, _ = oracle_mod.decode_step(sub, k=wl.k)
+    helpers.assert_topk_equal_outside_near_ties(idx[rows], oidx, scores, sub["row_len"], wl.k)
+    oo, ol = oracle_mod.sparse_mla(sub["q"], sub["softmax_scale"], sub["latent_cache"],
+                                   sub["latent_scale"], sub["block_table"], sub["row_req"],
+                                   sub["row_len"], idx[rows])
+    helpers.assert_out_close(out[rows], oo)
+    assert np.allclose(lse[rows], ol, rtol=1e-4, atol=1e-4)
+    # every row: selection size, ascending ids, finite output
+    for r in range(wl.R):
+        n = min(wl.k, int(host["row_len"][r]))
+        assert np.all(np.diff(idx[r, :n]) > 0) and np.all(idx[r, n:] == -1)
+    assert np.isfinite(out).all()
+    if wl.planted:
+        planted = set(host["planted"][0].tolist())
+        assert helpers.selected(idx[0]) == planted
