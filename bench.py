@@ -70,7 +70,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -118,8 +118,11 @@ def _step_fn(dsa, inp, wl, ws, out, lse):
 
 
 def _time_launches(fn, n, flush, stream):
-    """Mean device time (ms) of fn over n launches, L2 flushed before each."""
-    times = []
+    """Mean device time (ms) of fn over n launches, L2 flushed (untimed) before each.
+
+    Each launch is bracketed by its own pair of CUDA events on `stream`; the
+    host synchronises once at the end."""
+    evs = []
     for _ in range(n):
         flush()
         a = torch.cuda.Event(enable_timing=True)
@@ -127,8 +130,9 @@ def _time_launches(fn, n, flush, stream):
         a.record(stream)
         fn()
         b.record(stream)
-        b.synchronize()
-        times.append(a.elapsed_time(b))
+        evs.append((a, b))
+    evs[-1][1].synchronize()
+    times = [a.elapsed_time(b) for a, b in evs]
     return statistics.mean(times), times
 
 
@@ -224,7 +228,7 @@ def run_gpu(args):
     for name, (fn, _) in stages.items():
         for _ in range(3):
             fn()
-        stage_ms[name] = _time_launches(fn, max(5, min(args.steps, 50)), flush, stream)[0]
+        stage_ms[name] = _time_launches(fn, max(20, min(args.steps, 200)), flush, stream)[0]
     dominant = max((n for n in stages if stages[n][1] is not None), key=lambda n: stage_ms[n])
     hbm_peak, _, peak_kind = _peaks()
     dom_bytes = stages[dominant][1]
@@ -257,7 +261,7 @@ def run_gpu(args):
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = _time_launches(e2e_step, max(5, min(args.steps, 50)), flush, stream)[0]
+    e2e_ms = _time_launches(e2e_step, max(20, min(args.steps, 200)), flush, stream)[0]
     e2e_value = bytes_step * world / (e2e_ms * 1e-3) / 1e9
 
     cpu = None
@@ -304,13 +308,19 @@ def _oracle_sample(wl, inp_host, requests):
     return h, sample
 
 
-def cpu_baseline(wl, inp, requests=1):
+def cpu_baseline(wl, inp, target_s=10.0):
+    """Oracle on the first n requests, n grown until the run takes about target_s."""
     from oracle import oracle
     host = inputs.to_numpy(inp)
-    h, sample = _oracle_sample(wl, host, requests)
-    t0 = time.perf_counter()
-    oracle.decode_step(h, k=wl.k)
-    dt = time.perf_counter() - t0
+    requests = 1
+    while True:
+        h, sample = _oracle_sample(wl, host, requests)
+        t0 = time.perf_counter()
+        oracle.decode_step(h, k=wl.k)
+        dt = time.perf_counter() - t0
+        if dt >= target_s or requests >= wl.B:
+            break
+        requests = min(wl.B, max(requests + 1, int(requests * target_s / max(dt, 1e-3))))
     b = traffic.algorithmic_bytes(sample)
     return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
             "kind": "oracle", "seconds": round(dt, 3),
@@ -357,7 +367,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=1,
                     help="0 tiny, 1 16x4 rows @32K (default), 2 16x4 @256K, 3 1 row @1M")

@@ -34,6 +34,8 @@ P, I32, I64, SZ, F32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_s
 SIGNATURES = [
     ("dsa_version", I32, []),
     ("dsa_status_string", ctypes.c_char_p, [I32]),
+    ("dsa_last_cuda_error", I32, []),
+    ("dsa_last_cuda_error_string", ctypes.c_char_p, []),
     ("dsa_device_info", I32, [P, P, P]),
     ("dsa_indexer_score_workspace_size", SZ, [I32]),
     ("dsa_indexer_score", I32, [P, I32, P, P, P, I64, P, I32, I32, P, P, I32, P, I64, P, SZ, P]),
@@ -81,7 +83,10 @@ def status_string(status: int) -> str:
 
 def _check(fn: str, status: int) -> None:
     if status != DSA_OK:
-        raise DSAError(fn, status, status_string(status))
+        text = status_string(status)
+        if status == 4:
+            text += ": " + load().dsa_last_cuda_error_string().decode()
+        raise DSAError(fn, status, text)
 
 
 def _ptr(t: Optional[torch.Tensor]):

@@ -16,13 +16,6 @@ inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-// Scratch of the indexer scan beyond the status word (reserved per row for the
-// converted query and folded head weights).
-inline size_t scan_scratch_bytes(int R) {
-  return align_up((size_t)R * kIdxHeads * kIdxDim * 2) + align_up((size_t)R * kIdxHeads * 4) +
-         align_up((size_t)(R + 1) * 16);
-}
-
 inline int64_t score_ld(int max_pages) { return (int64_t)max_pages * kPage; }
 
 int check_rows(int B, int max_pages, const int32_t* block_table, const int32_t* row_req,
@@ -38,11 +31,17 @@ int check_workspace(void* ws, size_t have, size_t need) {
   return DSA_OK;
 }
 
-int clear_status(void* ws, cudaStream_t st) {
-  return cudaMemsetAsync(ws, 0, 4, st) == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
-}
+int to_status(cudaError_t e);
 
-int to_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+int clear_status(void* ws, cudaStream_t st) { return to_status(cudaMemsetAsync(ws, 0, 4, st)); }
+
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+int to_status(cudaError_t e) {
+  if (e == cudaSuccess) return DSA_OK;
+  t_last_cuda_error = e;
+  return DSA_ERR_CUDA;
+}
 
 bool supported_heads(int H) { return H == 16 || H == 32 || H == 64 || H == 128; }
 
@@ -51,6 +50,10 @@ bool supported_heads(int H) { return H == 16 || H == 32 || H == 64 || H == 128; 
 extern "C" {
 
 int dsa_version(void) { return kVersion; }
+
+int dsa_last_cuda_error(void) { return (int)t_last_cuda_error; }
+
+const char* dsa_last_cuda_error_string(void) { return cudaGetErrorString(t_last_cuda_error); }
 
 const char* dsa_status_string(int status) {
   switch (status) {
@@ -66,21 +69,19 @@ const char* dsa_status_string(int status) {
 
 int dsa_device_info(int* num_sms, int* cc_major, int* cc_minor) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return DSA_ERR_CUDA;
+  int s = to_status(cudaGetDevice(&dev));
+  if (s) return s;
   int v = 0;
   if (num_sms) {
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return DSA_ERR_CUDA;
+    if ((s = to_status(cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev)))) return s;
     *num_sms = v;
   }
   if (cc_major) {
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
-      return DSA_ERR_CUDA;
+    if ((s = to_status(cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMajor, dev)))) return s;
     *cc_major = v;
   }
   if (cc_minor) {
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-      return DSA_ERR_CUDA;
+    if ((s = to_status(cudaDeviceGetAttribute(&v, cudaDevAttrComputeCapabilityMinor, dev)))) return s;
     *cc_minor = v;
   }
   return DSA_OK;
@@ -111,7 +112,8 @@ int dsa_indexer_score(const void* q_idx, int q_dtype, const float* q_scale, cons
   if ((s = clear_status(workspace, st))) return s;
   if (R == 0) return DSA_OK;
   ScanArgs a{q_idx, q_dtype, q_scale, w, key_cache, num_pages, block_table, B, max_pages,
-             row_req, row_len, R, scores, ld, static_cast<uint32_t*>(workspace)};
+             row_req, row_len, R, scores, ld, static_cast<uint8_t*>(workspace) + kStatusBytes,
+             static_cast<uint32_t*>(workspace)};
   return to_status(launch_indexer_scan(a, st));
 }
 
@@ -225,12 +227,12 @@ int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const 
   const int64_t ld = score_ld(max_pages);
 
   ScanArgs sa{q_idx, q_dtype, q_scale, w, key_cache, num_pages, block_table, B, max_pages,
-              row_req, row_len, R, scores, ld, status};
+              row_req, row_len, R, scores, ld, ws + L.scan, status};
   cudaError_t e = launch_indexer_scan(sa, st);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  if (e != cudaSuccess) return to_status(e);
   TopkArgs ta{scores, ld, row_len, R, ld, k, idx, ws + L.topk, status};
   e = launch_topk(ta, st);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  if (e != cudaSuccess) return to_status(e);
   MlaArgs ma{q, H, softmax_scale, latent_cache, num_pages, latent_scale, block_table, B,
              max_pages, row_req, row_len, idx, k, R, out, lse, ws + L.mla, status};
   return to_status(launch_sparse_mla(ma, st));
@@ -239,8 +241,9 @@ int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const 
 int dsa_check_device_status(const void* workspace, void* stream, uint32_t* bits) {
   if (!workspace) return DSA_ERR_WORKSPACE;
   uint32_t v = 0;
-  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return DSA_ERR_CUDA;
-  if (cudaMemcpy(&v, workspace, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return DSA_ERR_CUDA;
+  int s = to_status(cudaStreamSynchronize(as_stream(stream)));
+  if (s) return s;
+  if ((s = to_status(cudaMemcpy(&v, workspace, 4, cudaMemcpyDeviceToHost)))) return s;
   if (bits) *bits = v;
   return v ? DSA_ERR_DEVICE_CHECK : DSA_OK;
 }

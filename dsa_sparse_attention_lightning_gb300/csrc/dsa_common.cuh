@@ -104,8 +104,10 @@ struct ScanArgs {
   const void* q_idx; int q_dtype; const float* q_scale; const float* w;
   const uint8_t* key_cache; int64_t num_pages; const int32_t* block_table; int B; int max_pages;
   const int32_t* row_req; const int32_t* row_len; int R; float* scores; int64_t ld;
+  uint8_t* scratch;  // scan_scratch_bytes(R) bytes
   uint32_t* status;
 };
+size_t scan_scratch_bytes(int R);
 cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st);
 
 struct TopkArgs {

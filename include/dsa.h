@@ -72,6 +72,8 @@ extern "C" {
 #define DSA_DEV_BAD_ROW 0x1   /* row_req outside [0,B) or row_len outside [0, max_pages*64] */
 #define DSA_DEV_BAD_PAGE 0x2  /* block-table entry outside [0, num_pages)   */
 #define DSA_DEV_BAD_INDEX 0x4 /* selected index >= row_len                   */
+#define DSA_DEV_TIMEOUT 0x8   /* a bounded wait inside a kernel gave up (about 2 s);
+                                 the kernel drained and returned, results are invalid */
 
 /* ---- fixed shapes ------------------------------------------------------ */
 #define DSA_PAGE_TOKENS 64
@@ -91,6 +93,12 @@ int dsa_version(void);
 
 /* Static, human-readable text for a status code. */
 const char* dsa_status_string(int status);
+
+/* The cudaError_t (as int) behind the most recent DSA_ERR_CUDA returned on the
+ * calling host thread, and its text; 0 / "no error" if there was none.  Kept
+ * per host thread; a call that succeeds does not clear it. */
+int dsa_last_cuda_error(void);
+const char* dsa_last_cuda_error_string(void);
 
 /* Number of SMs and whether the current device is an sm_103 part; host-only
  * query of the current device.  Returns DSA_OK or DSA_ERR_CUDA. */
