@@ -48,24 +48,35 @@ struct TopkLayout {
   }
 };
 
-// Split of the selected-token dimension over CTAs in sparse MLA: a fixed
-// function of (R, k) so that results do not depend on the device.
+// Sparse MLA works on tiles of 128 selected slots.  The slots of a row are
+// split over CTAs in whole tiles; the split is a fixed function of (R, k) so
+// that results do not depend on the device.
+constexpr int kMlaTile = 128;
+
+inline int mla_tiles_per_split(int R, int k) {
+  const int tiles = (k + kMlaTile - 1) / kMlaTile;
+  int target = (152 + R - 1) / R;                // about one CTA per SM of a 152-SM part
+  if (target > tiles) target = tiles;
+  if (target < 1) target = 1;
+  return (tiles + target - 1) / target;
+}
+
 inline int mla_num_splits(int R, int k) {
-  int by_rows = (304 + R - 1) / R;               // about two CTAs per SM of a 152-SM part
-  int by_k = (k + 63) / 64;                      // at least 64 slots per split
-  int s = by_rows < by_k ? by_rows : by_k;
-  if (s > 32) s = 32;
-  return s < 1 ? 1 : s;
+  const int tiles = (k + kMlaTile - 1) / kMlaTile;
+  const int per = mla_tiles_per_split(R, k);
+  return (tiles + per - 1) / per;
 }
 
 struct MlaLayout {
-  size_t part_o, part_lse, bytes;
+  size_t part_o, part_lse, q8, qc, bytes;
   int nsplit;
   MlaLayout(int R, int H, int k) {
     nsplit = mla_num_splits(R, k);
     size_t o = 0;
     part_o = o;   o = align_up(o + (size_t)R * nsplit * H * kVDim * 4);
     part_lse = o; o = align_up(o + (size_t)R * nsplit * H * 4);
+    q8 = o;       o = align_up(o + (size_t)R * H * 2 * kLatDim);   // E4M3 hi, lo per head
+    qc = o;       o = align_up(o + (size_t)R * H * 4);             // per-head logit factor
     bytes = o;
   }
 };
