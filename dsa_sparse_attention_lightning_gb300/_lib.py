@@ -39,6 +39,8 @@ SIGNATURES = [
     ("dsa_device_info", I32, [P, P, P]),
     ("dsa_indexer_score_workspace_size", SZ, [I32]),
     ("dsa_indexer_score", I32, [P, I32, P, P, P, I64, P, I32, I32, P, P, I32, P, I64, P, SZ, P]),
+    ("dsa_indexer_score_noalloc", I32, [P, I32, P, P, P, I64, P, I32, I32, P, P, I32, P, I64, P,
+                                        P]),
     ("dsa_topk_workspace_size", SZ, [I32, I64, I32]),
     ("dsa_topk", I32, [P, I64, P, I32, I64, I32, P, P, SZ, P]),
     ("dsa_sparse_mla_workspace_size", SZ, [I32, I32, I32]),

@@ -129,6 +129,32 @@ int dsa_indexer_score(const void* q_idx, int q_dtype, const float* q_scale, cons
                       void* stream);
 
 /* ------------------------------------------------------------------------
+ * dsa_indexer_score_noalloc -- dsa_indexer_score for callers that cannot
+ * provide a workspace.  The pages have no counterpart: this entry point
+ * exists for callers that may not allocate device memory when they call the
+ * scan -- code capturing a stream into a CUDA graph (allocation is not
+ * allowed during capture), decode loops that must not enter the allocator
+ * (it can synchronise the device), and hosts that hand a library only the
+ * operation's tensors.
+ *
+ * Same arguments and results as dsa_indexer_score, minus the workspace; the
+ * scratch is a fixed array inside the library (1 MiB per GPU, held until the
+ * process exits), so R <= DSA_NOALLOC_MAX_ROWS (else DSA_ERR_UNSUPPORTED).
+ *  dev_status optional device pointer to one uint32 that receives the
+ *             DSA_DEV_* bits of this call (cleared first); NULL to ignore them.
+ * All calls on one GPU share the array: calls that may overlap on the GPU
+ * race and must be ordered by the caller (one stream, or events).  The first
+ * call on a device looks up the array's device address with that device
+ * current; make it before any stream capture.  Nothing is allocated.
+ * ---------------------------------------------------------------------- */
+#define DSA_NOALLOC_MAX_ROWS 64
+int dsa_indexer_score_noalloc(const void* q_idx, int q_dtype, const float* q_scale,
+                              const float* w, const uint8_t* key_cache, int64_t num_pages,
+                              const int32_t* block_table, int B, int max_pages,
+                              const int32_t* row_req, const int32_t* row_len, int R,
+                              float* scores, int64_t ld, uint32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * dsa_topk -- step 2 alone (Select).
  *
  * For each row r: the min(k, row_len[r]) positions s in [0, row_len[r]) with
