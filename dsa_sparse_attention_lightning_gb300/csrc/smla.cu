@@ -18,24 +18,37 @@
 // decode context parallelism", step 4).
 //
 // Per 128-slot tile, one CTA (a query row, a split, up to 64 heads):
-//  1. gather the 128 selected 576-byte FP8 latent rows (paged) into shared
-//     memory with cp.async, in the K-major 128-byte-swizzle layout (the
-//     576 bytes span 4.5 swizzle atoms; the half atom is padded);
-//  2. S^T[token, (term, head)] = L8 . Q8^T on tcgen05 kind::f8f6f4, M = 128
-//     tokens, N = 2 x heads, K = 576.  The bf16 query is split exactly into
-//     two E4M3 terms per (row, head): q * 2^a = hi + lo / 32 (a power of two
-//     per head puts its absmax in [128, 256); both terms carry 4 significant
-//     bits, a bf16 value has 8);
-//  3. softmax across the tile's tokens per head in the log2 domain, with a
-//     running maximum that is only moved (and the accumulator rescaled) when
-//     a tile's maximum exceeds it by more than 8, so P = 2^(y - m) <= 256
-//     fits E4M3; P is written to shared memory as two E4M3 terms, P = P_hi +
-//     P_lo (about 8 significant bits), and the running sum takes the fp32 P;
+//  1. one warp gathers the 128 selected 576-byte FP8 latent rows (paged) into
+//     one of two shared-memory buffers with TMA tile::gather4 (four arbitrary
+//     rows x 128 bytes per instruction, landing in the K-major 128-byte-swizzle
+//     layout; 576 bytes span 4.5 swizzle atoms, the tail of the fifth box is
+//     past the row and zero-filled), while the previous tile is computed.
+//     Masked slots use an out-of-range row, which TMA fills with zeros;
+//  2. S[(head, term), token] = Q8 . L8^T on tcgen05 kind::f8f6f4, M = 128,
+//     N = 128 tokens, K = 576.  The bf16 query is split exactly into two E4M3
+//     terms per (row, head): q * 2^a = hi + lo / 32 (a power of two per head
+//     puts its absmax in [128, 256); both terms carry 4 significant bits, a
+//     bf16 value has 8).  The query sits in tensor memory as the A operand
+//     for dims 0..511 (the RoPE dims 512..575 come from shared memory), which
+//     leaves shared memory for the second latent buffer;
+//  3. softmax per head along the TMEM lane in the log2 domain: the two terms
+//     of a head are adjacent lanes of one warp (combined by a shuffle), the
+//     maximum over the tile is a per-thread loop plus one exchange between the
+//     two warps that hold the tile's token halves.  The running maximum only
+//     moves (and the accumulator is rescaled) when a tile's maximum exceeds it
+//     by more than 8, so P = 2^(y - m) <= 256 fits E4M3; P goes to shared
+//     memory as two E4M3 terms, P = P_hi + P_lo (about 8 significant bits),
+//     and the running sum takes the fp32 P;
 //  4. O^T[dim, head] += V^T . P_hi^T + V^T . P_lo^T, kind::f8f6f4, M = 4 x 128
 //     dims, N = heads, K = 128 tokens; V^T is the same shared-memory latent
 //     tile read as an MN-major operand, so V is never copied.
-// Accumulators (S^T and O^T) live in tensor memory.
+// Accumulators (S and O^T) live in tensor memory; an MMA warp pipelines S of
+// tile i + 1 against the softmax and P.V of tile i through mbarriers.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math.h>
+
+#include <mutex>
 
 #include "dsa_common.cuh"
 #include "sm100_ptx.cuh"
@@ -45,34 +58,11 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 256;
 constexpr int kLatAtoms = 5;                          // 576 B = 4.5 x 128 B, padded
 constexpr int kAtom = kMlaTile * 128;                 // 128 token rows x 128 B
-constexpr int kLatChunks = kLatDim / 16;              // 36 chunks of 16 B per row
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleT = 8.f;                      // log2 headroom of P before a rescale
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kOCol = 256;                       // O^T columns start here; S^T at 0
-
-template <int HG>
-struct MlaSmem {
-  static constexpr int lat = 0;
-  static constexpr int q = kLatAtoms * kAtom;                        // [5][2HG][128]
-  static constexpr int p = q + kLatAtoms * 2 * HG * 128;             // [2][HG][128] hi, lo
-  static constexpr int tok = p + 2 * HG * 128;                       // [128] int64
-  static constexpr int red = tok + kMlaTile * 8;                     // max, sum: [2][4][32] each
-  static constexpr int hs = red + 2 * 8 * 32 * 4;                    // m, l, corr, qc [4][HG]
-  static constexpr int flag = hs + 4 * HG * 4;
-  static constexpr int bar = (flag + 16 + 7) / 8 * 8;                // s_done, o_done
-  static constexpr int tmem = bar + 16;
-  static constexpr int bytes = tmem + 16;
-  static constexpr int alloc = bytes + 1024;
-};
-
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
-}
 
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -148,32 +138,83 @@ mla_qprep_kernel(const __nv_bfloat16* __restrict__ q, int R, int H, float softma
 }
 
 // ---------------------------------------------------------------------------
+// Warp roles: warp 0 issues the MMAs and owns tensor memory; warp 1 gathers
+// latent rows with TMA (double-buffered); warps 2-9 run the softmax: warp w
+// reads TMEM lane quarter (w & 3) and token half (w - 2) / 4 of S.
+constexpr int kThreads2 = 320;
+constexpr int kSmWarp0 = 2;                           // first softmax warp
+constexpr int kSmThreads = 256;
+constexpr uint32_t kQCol = 0;                         // A operand: Q (dims 0..511), 128 cols
+constexpr uint32_t kSCol = 128;                       // S: [(head, term)] x [128 tokens]
+constexpr uint32_t kOCol2 = 256;                      // O^T: 4 blocks x HG cols
+
+template <int HG>
+struct Mla2Smem {
+  static constexpr int lat = 0;                                      // [2][5][128][128]
+  static constexpr int qrope = 2 * kLatAtoms * kAtom;                // [128 rows][128 B]
+  static constexpr int p = qrope + kMlaTile * 128;                   // [2 terms][HG][128]
+  static constexpr int corr = p + 2 * HG * 128;                      // [64] f32
+  static constexpr int red = corr + 64 * 4;                          // [2 halves][64] f32
+  static constexpr int lsum = red + 2 * 64 * 4;                      // [2 halves][64] f32
+  static constexpr int flag = lsum + 2 * 64 * 4;                     // [2] int
+  static constexpr int bar = (flag + 8 + 7) / 8 * 8;                 // 8 mbarriers
+  static constexpr int tmem = bar + 8 * 8;
+  static constexpr int bytes = tmem + 16;
+  static constexpr int alloc = bytes + 1024;
+};
+
+// TMA gather of four rows (y0..y3) x one box of the 2-D tensor map starting at
+// column x; completes on the mbarrier with the box bytes.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* tmap, int x, int y0,
+                                            int y1, int y2, int y3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool wwait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, status);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// Pack four floats into four E4M3 bytes (RNE, saturating).
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(lo) : "f"(a), "f"(b));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %2, %1;" : "=h"(hi) : "f"(c), "f"(d));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
 template <int HG>  // heads per CTA: 16, 32 or 64
-__global__ void __launch_bounds__(kThreads, 1)
-smla_tc_kernel(const uint8_t* __restrict__ q8, const float* __restrict__ qc, int H,
-               const uint8_t* __restrict__ latent_cache, int64_t num_pages, float latent_scale,
-               const int32_t* __restrict__ block_table, int B, int max_pages,
-               const int32_t* __restrict__ row_req, const int32_t* __restrict__ row_len,
-               const int32_t* __restrict__ idx, int k, int tiles_per_split, int nsplit,
-               float* __restrict__ part_o, float* __restrict__ part_lse, uint32_t* status) {
-  using L = MlaSmem<HG>;
-  constexpr int CW = HG < 32 ? HG : 32;               // heads per softmax chunk
+__global__ void __launch_bounds__(kThreads2, 1)
+smla2_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restrict__ q8,
+             const float* __restrict__ qc, int H, int64_t num_pages, float latent_scale,
+             const int32_t* __restrict__ block_table, int B, int max_pages,
+             const int32_t* __restrict__ row_req, const int32_t* __restrict__ row_len,
+             const int32_t* __restrict__ idx, int k, int tiles_per_split, int nsplit,
+             float* __restrict__ part_o, float* __restrict__ part_lse, uint32_t* status) {
+  using L = Mla2Smem<HG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* lat = smem + L::lat;
-  uint8_t* qs = smem + L::q;
+  uint8_t* qrope = smem + L::qrope;
   uint8_t* ps = smem + L::p;
-  int64_t* tok_off = reinterpret_cast<int64_t*>(smem + L::tok);
-  float* red_max = reinterpret_cast<float*>(smem + L::red);          // [half][quarter][32]
-  float* red_sum = red_max + 8 * 32;                                  // [half][quarter][32]
-  float* m_s = reinterpret_cast<float*>(smem + L::hs);               // running max (log2)
-  float* l_s = m_s + HG;                                              // running sum
-  float* corr_s = l_s + HG;                                           // this tile's rescale
-  float* qc_s = corr_s + HG;
+  float* corr_s = reinterpret_cast<float*>(smem + L::corr);
+  float* red_s = reinterpret_cast<float*>(smem + L::red);
+  float* lsum_s = reinterpret_cast<float*>(smem + L::lsum);
   int* flag_s = reinterpret_cast<int*>(smem + L::flag);
-  uint64_t* s_done = reinterpret_cast<uint64_t*>(smem + L::bar);
-  uint64_t* o_done = s_done + 1;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar);
+  uint64_t* lat_full = bars;          // [2]
+  uint64_t* lat_empty = bars + 2;     // [2]
+  uint64_t* s_full = bars + 4;
+  uint64_t* s_empty = bars + 5;
+  uint64_t* p_full = bars + 6;
+  uint64_t* p_empty = bars + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem);
 
   const int split = blockIdx.x, r = blockIdx.y, hg0 = blockIdx.z * HG;
@@ -188,225 +229,330 @@ smla_tc_kernel(const uint8_t* __restrict__ q8, const float* __restrict__ qc, int
   const int ntiles = (slot1 - slot0 + kMlaTile - 1) / kMlaTile;
 
   if (tid == 0) {
-    mbar_init(s_done, 1);
-    mbar_init(o_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&lat_full[b], 1);
+      mbar_init(&lat_empty[b], 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, 8);
+    mbar_init(p_full, 8);
+    mbar_init(p_empty, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
-  // query terms -> shared (K-major, 128B swizzle; row n = term * HG + head)
-  for (int id = tid; id < 2 * HG * kLatChunks; id += kThreads) {
-    const int n = id / kLatChunks, c = id % kLatChunks;
-    const int term = n / HG, h = n % HG;
-    const uint4 v = *reinterpret_cast<const uint4*>(
-        q8 + (((size_t)r * H + hg0 + h) * 2 + term) * kLatDim + c * 16);
-    *reinterpret_cast<uint4*>(qs + (c >> 3) * (2 * HG * 128) + n * 128 +
-                              (((c & 7) ^ (n & 7)) << 4)) = v;
-  }
-  for (int h = tid; h < HG; h += kThreads) {
-    m_s[h] = -INFINITY;
-    l_s[h] = 0.f;
-    qc_s[h] = qc[(size_t)r * H + hg0 + h];
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t idesc_s = idesc_e4m3_f32(kMlaTile, 2 * HG, false, false);
+
+  // softmax-thread geometry: TMEM lane m = 32 * quarter + lane holds row m of S:
+  // head 16 * quarter + (lane & 15), term lane >> 4 (0: hi, 1: lo)
+  const bool sm_warp = warp >= kSmWarp0;
+  const int quarter = warp & 3;
+  const int th = sm_warp ? (warp - kSmWarp0) >> 2 : 0;
+  const int hl = 16 * quarter + (lane & 15);          // head within the group
+  const bool head_ok = hl < HG;
+
+  // ---- Q: rows (head, term) -> TMEM columns [0, 128) (dims 0..511) and the
+  // RoPE dims 512..575 -> shared (A operand of the last two K steps)
+  if (sm_warp && th == 0) {
+    const int term = lane >> 4;
+    const uint4* src = reinterpret_cast<const uint4*>(
+        q8 + (((size_t)r * H + hg0 + (head_ok ? hl : 0)) * 2 + term) * kLatDim);
+#pragma unroll
+    for (int c4 = 0; c4 < 4; ++c4) {                  // 4 x 32 columns = 512 bytes
+      uint32_t v[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint4 x = head_ok ? __ldg(src + c4 * 8 + u) : make_uint4(0, 0, 0, 0);
+        v[4 * u + 0] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+      }
+      tmem_st_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + kQCol + c4 * 32, v);
+    }
+    const int m = quarter * 32 + lane;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const uint4 x = head_ok ? __ldg(src + 32 + c) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(qrope + m * 128 + ((c ^ (m & 7)) << 4)) = x;
+    }
+    tmem_wait_st();
+    fence_proxy_async_smem();
+  }
+  if (tid < 2) flag_s[tid] = 0;
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t idesc_s = idesc_e4m3_f32(kMlaTile, kMlaTile, false, false);
   const uint32_t idesc_o = idesc_e4m3_f32(kMlaTile, HG, true, false);
-  const bool epi_warp = warp >= 4;        // rescale and final epilogue: warps 4-7
-  const int quarter = warp & 3;           // TMEM lane quarter of this warp
-  const int half = warp >> 2;             // softmax: heads [half * HG / 2, (half + 1) * HG / 2)
   bool alive = true;
 
-  for (int t = 0; t < ntiles && alive; ++t) {
-    // the previous tile's P.V has finished reading the latent tile and P
-    if (t > 0 && !mbar_wait(o_done, (uint32_t)(t - 1) & 1, status)) alive = false;
-    if (__syncthreads_or(!alive)) break;
-    // ---- token row offsets of this tile (-1: masked slot)
-    if (tid < kMlaTile) {
-      const int j = slot0 + t * kMlaTile + tid;
-      int64_t off = -1;
-      if (row_valid && j < slot1) {
-        const int tok = idx[(size_t)r * k + j];
-        if (tok >= len) {
-          raise_dev(status, DSA_DEV_BAD_INDEX);
-        } else if (tok >= 0) {
-          const int page = block_table[(size_t)req * max_pages + tok / kPage];
-          if (page < 0 || (int64_t)page >= num_pages)
-            raise_dev(status, DSA_DEV_BAD_PAGE);
-          else
-            off = ((int64_t)page * kPage + (tok % kPage)) * kLatDim;
-        }
+  if (warp == 0) {
+    // ================= MMA issuer
+    auto issue_s = [&](int i) {
+      const uint32_t lb = smem_u32(lat + (i & 1) * (kLatAtoms * kAtom));
+#pragma unroll
+      for (int j = 0; j < kIdxDim * 4 / 32; ++j)      // dims 0..511 from TMEM
+        mma_e4m3_ts(tmem_base + kSCol, tmem_base + kQCol + (uint32_t)(j * 8),
+                    desc_kmajor_sw128(lb + (j >> 2) * kAtom + (j & 3) * 32), idesc_s,
+                    j > 0 ? 1u : 0u);
+#pragma unroll
+      for (int j = 0; j < 2; ++j)                     // dims 512..575 from shared
+        mma_e4m3_ss(tmem_base + kSCol, desc_kmajor_sw128(smem_u32(qrope) + j * 32),
+                    desc_kmajor_sw128(lb + 4 * kAtom + j * 32), idesc_s, 1u);
+      mma_commit(s_full);
+    };
+    if (ntiles > 0) {
+      if (!wwait(&lat_full[0], 0, status)) alive = false;
+      if (alive) {
+        tc_fence_after();
+        if (lane == 0) issue_s(0);
+        __syncwarp();
       }
-      tok_off[tid] = off;
     }
-    __syncthreads();
-    // ---- gather: 128 rows x 36 chunks; masked rows are zero (P = 0 must meet finite V)
-    for (int id = tid; id < kMlaTile * kLatChunks; id += kThreads) {
-      const int row = id / kLatChunks, c = id % kLatChunks;
-      uint8_t* dst = lat + (c >> 3) * kAtom + row * 128 + (((c & 7) ^ (row & 7)) << 4);
-      const int64_t off = tok_off[row];
-      if (off >= 0)
-        cp_async16(dst, latent_cache + off + c * 16);
-      else
-        *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-    }
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-    fence_proxy_async_smem();
-    if (tid == 0) flag_s[0] = 0;
-    __syncthreads();
-    // ---- S^T = L8 . Q8^T
-    if (tid == 0) {
+    for (int i = 0; i < ntiles && alive; ++i) {
+      if (i + 1 < ntiles) {
+        if (!wwait(&lat_full[(i + 1) & 1], (uint32_t)((i + 1) >> 1) & 1, status)) break;
+        if (!wwait(s_empty, (uint32_t)i & 1, status)) break;   // softmax(i) has read S
+        tc_fence_after();
+        if (lane == 0) issue_s(i + 1);
+        __syncwarp();
+      }
+      if (!wwait(p_full, (uint32_t)i & 1, status)) break;
       tc_fence_after();
-      const uint32_t a0 = smem_u32(lat), b0 = smem_u32(qs);
-#pragma unroll
-      for (int j = 0; j < kLatDim / 32; ++j) {
-        const uint64_t ad = desc_kmajor_sw128(a0 + (j >> 2) * kAtom + (j & 3) * 32);
-        const uint64_t bd = desc_kmajor_sw128(b0 + (j >> 2) * (2 * HG * 128) + (j & 3) * 32);
-        mma_e4m3_ss(tmem_base, ad, bd, idesc_s, j > 0 ? 1u : 0u);
-      }
-      mma_commit(s_done);
-    }
-    // ---- softmax, all 8 warps: thread = token 32 * quarter + lane, warp half
-    // `half` takes half of the heads; warps of one half reduce through smem.
-    {
-      constexpr int CWH = HG / 2;
-      if (!mbar_wait(s_done, (uint32_t)t & 1, status)) alive = false;
-      tc_fence_after();
-      const int tt = quarter * 32 + lane;
-      const bool valid = tok_off[tt] >= 0;
-      const int h0 = half * CWH;
-      uint32_t dh[32], dl[32];
-      const uint32_t ta = tmem_base + ((uint32_t)(quarter * 32) << 16);
-      tmem_ld_32x32b_x32(ta + (uint32_t)h0, dh);
-      tmem_ld_32x32b_x32(ta + (uint32_t)(HG + h0), dl);
-      tmem_wait_ld();
-      float y[CWH], v[CWH];
-#pragma unroll
-      for (int i = 0; i < CWH; ++i) {
-        y[i] = valid ? (__uint_as_float(dh[i]) + __uint_as_float(dl[i]) * (1.f / 32.f)) *
-                           qc_s[h0 + i]
-                     : -INFINITY;
-        v[i] = y[i];
-      }
-      const float wmax = reduce_scatter<CWH, true>(v, lane);
-      if (lane < CWH) red_max[(half * 4 + quarter) * 32 + lane] = wmax;
-      named_sync(1, kThreads);
-      if (quarter == 0 && lane < CWH) {
-        const int h = h0 + lane;
-        const float* rm = red_max + half * 4 * 32 + lane;
-        const float tmax = fmaxf(fmaxf(rm[0], rm[32]), fmaxf(rm[64], rm[96]));
-        const float m_old = m_s[h];
-        float c = 1.f;
-        if (tmax > m_old + kRescaleT) {               // m_old = -inf on the first valid tile
-          c = fast_exp2(m_old - tmax);
-          m_s[h] = tmax;
-          flag_s[0] = 1;
-        }
-        corr_s[h] = c;
-      }
-      named_sync(1, kThreads);
-      float pf[CWH];
-#pragma unroll
-      for (int i = 0; i < CWH; ++i) {
-        const int h = h0 + i;
-        const float m = m_s[h];
-        const float p = (valid && m > -INFINITY) ? fast_exp2(y[i] - m) : 0.f;
-        const uint8_t p_hi = f32_to_e4m3(p);
-        const uint8_t p_lo = f32_to_e4m3(p - e4m3_to_float(p_hi));
-        pf[i] = p;
-        // P^T is K-major: row = head, byte = token, 16-byte chunks swizzled by row
-        const int off = h * 128 + ((((tt >> 4) ^ (h & 7))) << 4) + (tt & 15);
-        ps[off] = p_hi;
-        ps[HG * 128 + off] = p_lo;
-      }
-      const float wsum = reduce_scatter<CWH, false>(pf, lane);
-      if (lane < CWH) red_sum[(half * 4 + quarter) * 32 + lane] = wsum;
-      named_sync(1, kThreads);
-      if (quarter == 0 && lane < CWH) {
-        const int h = h0 + lane;
-        const float* rs = red_sum + half * 4 * 32 + lane;
-        l_s[h] = l_s[h] * corr_s[h] + rs[0] + rs[32] + rs[64] + rs[96];
-      }
-      // rescale the O^T accumulator when a running maximum moved (never on tile 0:
-      // the first P.V overwrites the accumulator); warps 4-7 cover all heads
-      if (t > 0 && flag_s[0] && epi_warp) {
+      if (lane == 0) {
+        const uint32_t lb = smem_u32(lat + (i & 1) * (kLatAtoms * kAtom));
+        const uint32_t pb = smem_u32(ps);
 #pragma unroll
         for (int a = 0; a < kVDim / kMlaTile; ++a) {
 #pragma unroll
-          for (int c0 = 0; c0 < HG; c0 += CW) {
-            uint32_t d[32];
-            const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + kOCol +
-                                (uint32_t)(a * HG + c0);
-            tmem_ld_32x32b_x32(tb, d);
-            tmem_wait_ld();
+          for (int kk = 0; kk < kMlaTile / 32; ++kk) {
+            const uint64_t ad = desc_kmajor_sw128(lb + a * kAtom + kk * 4096);   // 32 token rows
+            const uint32_t d = tmem_base + kOCol2 + (uint32_t)(a * HG);
+            mma_e4m3_ss(d, ad, desc_kmajor_sw128(pb + kk * 32), idesc_o,
+                        (i > 0 || kk > 0) ? 1u : 0u);
+            mma_e4m3_ss(d, ad, desc_kmajor_sw128(pb + HG * 128 + kk * 32), idesc_o, 1u);
+          }
+        }
+        mma_commit(p_empty);
+        mma_commit(&lat_empty[i & 1]);
+      }
+      __syncwarp();
+    }
+  } else if (warp == 1) {
+    // ================= TMA gather: lane g fetches tile rows 4g..4g+3 (5 boxes each)
+    int y[4];
+    auto lookup = [&](int i) {
 #pragma unroll
-            for (int i = 0; i < CW; ++i) d[i] = __float_as_uint(__uint_as_float(d[i]) * corr_s[c0 + i]);
-            tmem_st_32x32b_x32(tb, d);
+      for (int u = 0; u < 4; ++u) {
+        const int row = 4 * lane + u;
+        const int j = slot0 + i * kMlaTile + row;
+        int yy = -1;                                  // out of range: zero-filled by TMA
+        if (row_valid && j < slot1) {
+          const int tok = idx[(size_t)r * k + j];
+          if (tok >= len) {
+            raise_dev(status, DSA_DEV_BAD_INDEX);
+          } else if (tok >= 0) {
+            const int page = block_table[(size_t)req * max_pages + tok / kPage];
+            if (page < 0 || (int64_t)page >= num_pages)
+              raise_dev(status, DSA_DEV_BAD_PAGE);
+            else
+              yy = page * kPage + (tok % kPage);
+          }
+        }
+        y[u] = yy;
+      }
+    };
+    if (ntiles > 0) lookup(0);
+    for (int i = 0; i < ntiles; ++i) {
+      const int b = i & 1;
+      if (!wwait(&lat_empty[b], ((uint32_t)(i >> 1) & 1) ^ 1, status)) break;
+      if (lane == 0) mbar_arrive_expect_tx(&lat_full[b], kLatAtoms * kAtom);
+      __syncwarp();
+      uint8_t* lt = lat + b * (kLatAtoms * kAtom) + 4 * lane * 128;
+#pragma unroll
+      for (int a = 0; a < kLatAtoms; ++a)
+        tma_gather4(lt + a * kAtom, &lat_map, a * 128, y[0], y[1], y[2], y[3], &lat_full[b]);
+      if (i + 1 < ntiles) lookup(i + 1);
+    }
+    // no copy may still be landing in shared memory when the CTA exits
+    if (ntiles > 0) {
+      const int last = ntiles - 1;
+      wwait(&lat_full[last & 1], (uint32_t)(last >> 1) & 1, status);
+      if (ntiles > 1) wwait(&lat_full[(last - 1) & 1], (uint32_t)((last - 1) >> 1) & 1, status);
+    }
+  } else {
+    // ================= softmax (warps 4-11)
+    const float qcf = head_ok ? qc[(size_t)r * H + hg0 + hl] : 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+    // validity of this warp's 64 tokens (tokens th*64 + lane and th*64 + 32 + lane):
+    // the selected ids are loaded a tile ahead and turned into bit masks late
+    auto load_ids = [&](int i, int& a, int& b) {
+      const int j = slot0 + i * kMlaTile + th * 64 + lane;
+      a = (row_valid && j < slot1) ? __ldg(idx + (size_t)r * k + j) : -1;
+      b = (row_valid && j + 32 < slot1) ? __ldg(idx + (size_t)r * k + j + 32) : -1;
+    };
+    auto valid_bits = [&](int a, int b, uint32_t& lo_bits, uint32_t& hi_bits) {
+      lo_bits = __ballot_sync(0xffffffffu, a >= 0 && a < len);
+      hi_bits = __ballot_sync(0xffffffffu, b >= 0 && b < len);
+    };
+    uint32_t vlo = 0, vhi = 0;
+    int ida = -1, idb = -1;
+    if (ntiles > 0) {
+      load_ids(0, ida, idb);
+      valid_bits(ida, idb, vlo, vhi);
+    }
+    for (int i = 0; i < ntiles; ++i) {
+      // ---- S rows -> registers, then S may be overwritten by the next tile's MMA
+      if (!wwait(s_full, (uint32_t)i & 1, status)) { alive = false; }
+      tc_fence_after();
+      uint32_t s0[32], s1[32];
+      const uint32_t ta = tmem_base + ((uint32_t)(quarter * 32) << 16) + kSCol + th * 64;
+      if (alive) {
+        tmem_ld_32x32b_x32(ta, s0);
+        tmem_ld_32x32b_x32(ta + 32, s1);
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty);
+      if (i + 1 < ntiles) load_ids(i + 1, ida, idb);
+      // ---- combine the two query terms: lane < 16 keeps tokens 0..31 of this
+      // warp's half, lane >= 16 tokens 32..63; the partner lane (lane ^ 16)
+      // holds the other term
+      const bool hi_lane = lane < 16;
+      const uint32_t vb = hi_lane ? vlo : vhi;
+      float y[32];
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float send = __uint_as_float(hi_lane ? s1[j] : s0[j]);
+        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+        const float hi_t = hi_lane ? __uint_as_float(s0[j]) : recv;
+        const float lo_t = hi_lane ? recv : __uint_as_float(s1[j]);
+        y[j] = ((vb >> j) & 1u) ? (hi_t + lo_t * (1.f / 32.f)) * qcf : -INFINITY;
+        tmax = fmaxf(tmax, y[j]);
+      }
+      tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
+      if (hi_lane && head_ok) red_s[th * 64 + hl] = tmax;
+      named_sync(1, kSmThreads);
+      // every softmax warp is past tile i - 1 here: its flag slot can be reused
+      if (tid == kSmWarp0 * 32) flag_s[(i + 1) & 1] = 0;
+      if (head_ok) tmax = fmaxf(tmax, red_s[(th ^ 1) * 64 + hl]);
+      float corr = 1.f;
+      if (tmax > m_run + kRescaleT) {                 // m_run = -inf on the first valid tile
+        corr = fast_exp2(m_run - tmax);
+        m_run = tmax;
+      }
+      if (th == 0 && hi_lane && head_ok) {
+        corr_s[hl] = corr;
+        if (corr != 1.f) flag_s[i & 1] = 1;
+      }
+      // ---- P (two E4M3 terms) -> shared, once the previous P.V has finished with it
+      if (!wwait(p_empty, ((uint32_t)i & 1) ^ 1, status)) alive = false;
+      named_sync(1, kSmThreads);                      // corr_s / flag visible
+      float psum = 0.f;
+      uint32_t whi[8], wlo[8];
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        float p[4], pl[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float v = y[4 * j4 + u];
+          p[u] = (m_run > -INFINITY && v > -INFINITY) ? fast_exp2(v - m_run) : 0.f;
+          psum += p[u];
+        }
+        whi[j4] = pack_e4m3x4(p[0], p[1], p[2], p[3]);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          pl[u] = p[u] - e4m3_to_float((uint8_t)(whi[j4] >> (8 * u)));
+        wlo[j4] = pack_e4m3x4(pl[0], pl[1], pl[2], pl[3]);
+      }
+      l_run = l_run * corr + psum;
+      if (head_ok) {
+        // this thread's 32 tokens = two 16-byte chunks of row hl of P^T (K-major, swizzled)
+        const int t0 = th * 64 + (hi_lane ? 0 : 32);
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int chunk = (t0 >> 4) + c;
+          const int off = hl * 128 + ((chunk ^ (hl & 7)) << 4);
+          *reinterpret_cast<uint4*>(ps + off) =
+              make_uint4(whi[4 * c], whi[4 * c + 1], whi[4 * c + 2], whi[4 * c + 3]);
+          *reinterpret_cast<uint4*>(ps + HG * 128 + off) =
+              make_uint4(wlo[4 * c], wlo[4 * c + 1], wlo[4 * c + 2], wlo[4 * c + 3]);
+        }
+      }
+      // ---- rescale O^T when a running maximum moved (O(i-1) is complete: p_empty)
+      if (i > 0 && flag_s[i & 1] && alive) {
+        constexpr int CWO = HG < 32 ? HG : 32;
+#pragma unroll
+        for (int a = 2 * th; a < 2 * th + 2; ++a) {
+#pragma unroll
+          for (int c0 = 0; c0 < HG; c0 += CWO) {
+            const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + kOCol2 +
+                                (uint32_t)(a * HG + c0);
+            if (CWO == 32) {
+              uint32_t d[32];
+              tmem_ld_32x32b_x32(tb, d);
+              tmem_wait_ld();
+#pragma unroll
+              for (int u = 0; u < 32; ++u) d[u] = __float_as_uint(__uint_as_float(d[u]) * corr_s[c0 + u]);
+              tmem_st_32x32b_x32(tb, d);
+            } else {
+              uint32_t d[16];
+              tmem_ld_32x32b_x16(tb, d);
+              tmem_wait_ld();
+#pragma unroll
+              for (int u = 0; u < 16; ++u) d[u] = __float_as_uint(__uint_as_float(d[u]) * corr_s[c0 + u]);
+              tmem_st_32x32b_x16(tb, d);
+            }
           }
         }
         tmem_wait_st();
       }
       fence_proxy_async_smem();
       tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+      if (i + 1 < ntiles) valid_bits(ida, idb, vlo, vhi);
     }
-    if (__syncthreads_or(!alive)) break;
-    // ---- O^T += V^T . P_hi^T + V^T . P_lo^T
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t a0 = smem_u32(lat), b0 = smem_u32(ps);
-#pragma unroll
-      for (int a = 0; a < kVDim / kMlaTile; ++a) {
-#pragma unroll
-        for (int kk = 0; kk < kMlaTile / 32; ++kk) {
-          const uint64_t ad = desc_kmajor_sw128(a0 + a * kAtom + kk * 4096);   // 32 token rows
-          const uint32_t d = tmem_base + kOCol + (uint32_t)(a * HG);
-          mma_e4m3_ss(d, ad, desc_kmajor_sw128(b0 + kk * 32), idesc_o,
-                      (t > 0 || kk > 0) ? 1u : 0u);
-          mma_e4m3_ss(d, ad, desc_kmajor_sw128(b0 + HG * 128 + kk * 32), idesc_o, 1u);
-        }
-      }
-      mma_commit(o_done);
-    }
-  }
-
-  // ---- epilogue: O^T / l -> partial output, lse
-  if (alive && ntiles > 0) {
-    if (!mbar_wait(o_done, (uint32_t)(ntiles - 1) & 1, status)) alive = false;
-  }
-  if (epi_warp) {
+    // ---- epilogue: l over the 4 threads of a head, then O^T / l -> partial output
+    if (ntiles > 0 && !wwait(p_empty, (uint32_t)(ntiles - 1) & 1, status)) alive = false;
     tc_fence_after();
+    const float lpair = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
+    if (lane < 16 && head_ok) lsum_s[th * 64 + hl] = lpair;
+    named_sync(1, kSmThreads);
     const size_t pbase = ((size_t)r * nsplit + split) * H + hg0;
+    constexpr int CWO = HG < 32 ? HG : 32;
 #pragma unroll
-    for (int a = 0; a < kVDim / kMlaTile; ++a) {
+    for (int a = 2 * th; a < 2 * th + 2; ++a) {
 #pragma unroll
-      for (int h0 = 0; h0 < HG; h0 += CW) {
+      for (int c0 = 0; c0 < HG; c0 += CWO) {
         uint32_t d[32];
+        const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + kOCol2 +
+                            (uint32_t)(a * HG + c0);
         if (alive && ntiles > 0) {
-          tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + kOCol +
-                                 (uint32_t)(a * HG + h0),
-                             d);
+          tmem_ld_32x32b_x32(tb, d);
           tmem_wait_ld();
         }
 #pragma unroll
-        for (int i = 0; i < CW; ++i) {
-          const float l = l_s[h0 + i];
-          const float o = (alive && ntiles > 0 && l > 0.f) ? __uint_as_float(d[i]) * (latent_scale / l)
+        for (int u = 0; u < CWO; ++u) {
+          const int h = c0 + u;
+          const float l = lsum_s[h] + lsum_s[64 + h];
+          const float o = (alive && ntiles > 0 && l > 0.f) ? __uint_as_float(d[u]) * (latent_scale / l)
                                                             : 0.f;
-          part_o[(pbase + h0 + i) * kVDim + a * kMlaTile + quarter * 32 + lane] = o;
+          part_o[(pbase + h) * kVDim + a * kMlaTile + quarter * 32 + lane] = o;
         }
       }
     }
-    if (quarter == 0) {
-      for (int h = lane; h < HG; h += 32) {
-        const float l = l_s[h], m = m_s[h];
-        part_lse[pbase + h] =
-            (alive && l > 0.f && m > -INFINITY) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
-      }
+    if (th == 0 && (lane & 16) == 0 && head_ok) {
+      const float l = lsum_s[hl] + lsum_s[64 + hl];
+      part_lse[pbase + hl] = (alive && l > 0.f && m_run > -INFINITY)
+                                 ? (m_run + log2f(l)) * 0.6931471805599453f
+                                 : -INFINITY;
     }
   }
   tc_fence_before();
@@ -450,15 +596,52 @@ mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ p
   if (lse && threadIdx.x == 0) lse[(size_t)r * H + h] = Z > 0.f ? M + logf(Z) : -INFINITY;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// The latent cache as a 2-D tensor of 576-byte rows (one per token slot); a box
+// is 128 bytes of one row, stored with the 128-byte swizzle.
+cudaError_t latent_tensor_map(CUtensorMap* map, const uint8_t* cache, int64_t num_pages) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  // Row coordinates are signed 32-bit.  With no pages every lookup is rejected
+  // before a coordinate is formed, so a one-page map is never dereferenced.
+  if (num_pages * kPage > INT32_MAX) return cudaErrorInvalidValue;
+  const int64_t rows = (num_pages > 0 ? num_pages : 1) * kPage;
+  const cuuint64_t dims[2] = {(cuuint64_t)kLatDim, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kLatDim};
+  const cuuint32_t box[2] = {128, 1};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(cache), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int HG>
 cudaError_t launch_smla_group(const MlaArgs& a, const MlaLayout& L, cudaStream_t st) {
-  using S = MlaSmem<HG>;
-  cudaError_t e = cudaFuncSetAttribute(smla_tc_kernel<HG>,
+  using S = Mla2Smem<HG>;
+  alignas(64) CUtensorMap map;
+  cudaError_t me = latent_tensor_map(&map, a.latent_cache, a.num_pages);
+  if (me != cudaSuccess) return me;
+  cudaError_t e = cudaFuncSetAttribute(smla2_kernel<HG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, S::alloc);
   if (e != cudaSuccess) return e;
   dim3 grid(L.nsplit, a.R, a.H / HG);
-  smla_tc_kernel<HG><<<grid, kThreads, S::alloc, st>>>(
-      a.scratch + L.q8, reinterpret_cast<const float*>(a.scratch + L.qc), a.H, a.latent_cache,
+  smla2_kernel<HG><<<grid, kThreads2, S::alloc, st>>>(
+      map, a.scratch + L.q8, reinterpret_cast<const float*>(a.scratch + L.qc), a.H,
       a.num_pages, a.latent_scale, a.block_table, a.B, a.max_pages, a.row_req, a.row_len, a.idx, a.k,
       mla_tiles_per_split(a.R, a.k), L.nsplit, reinterpret_cast<float*>(a.scratch + L.part_o),
       reinterpret_cast<float*>(a.scratch + L.part_lse), a.status);
