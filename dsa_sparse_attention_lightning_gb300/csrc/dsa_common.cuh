@@ -48,33 +48,40 @@ struct TopkLayout {
   }
 };
 
-// Sparse MLA works on tiles of 128 selected slots.  The slots of a row are
-// split over CTAs in whole tiles; the split is a fixed function of (R, k) so
-// that results do not depend on the device.
+// Sparse MLA works on tiles of 128 selected slots.  A unit is one query row
+// and one group of up to 64 heads; unit u = row * groups + group has
+// NT = ceil(k / 128) tiles.  The U * NT tiles are cut into G = min(152, U * NT)
+// contiguous ranges of near-equal length, one per CTA (one CTA per SM of a
+// 152-SM part); the cut is a fixed function of (R, H, k) so that results do
+// not depend on the device.  A CTA's range covers whole units (written
+// straight to the output) and at most two cut units, whose partials it leaves
+// in slots 2c (its first unit) and 2c + 1 (its last) for the combine.
 constexpr int kMlaTile = 128;
+constexpr int kMlaGrid = 152;
 
-inline int mla_tiles_per_split(int R, int k) {
-  const int tiles = (k + kMlaTile - 1) / kMlaTile;
-  int target = (152 + R - 1) / R;                // about one CTA per SM of a 152-SM part
-  if (target > tiles) target = tiles;
-  if (target < 1) target = 1;
-  return (tiles + target - 1) / target;
-}
+__host__ __device__ inline int mla_heads_per_cta(int H) { return H < 64 ? H : 64; }
 
-inline int mla_num_splits(int R, int k) {
-  const int tiles = (k + kMlaTile - 1) / kMlaTile;
-  const int per = mla_tiles_per_split(R, k);
-  return (tiles + per - 1) / per;
-}
+struct MlaWork {
+  int64_t U, NT, T;
+  int G;
+  __host__ __device__ MlaWork(int R, int H, int k) {
+    U = (int64_t)R * (H / mla_heads_per_cta(H));
+    NT = (k + kMlaTile - 1) / kMlaTile;
+    T = U * NT;
+    G = (int)(T < kMlaGrid ? T : kMlaGrid);
+  }
+  __host__ __device__ int64_t begin(int64_t c) const { return c * T / G; }   // first tile of CTA c
+  __host__ __device__ int cta_of(int64_t t) const { return (int)(((t + 1) * G - 1) / T); }
+};
 
 struct MlaLayout {
   size_t part_o, part_lse, q8, qc, bytes;
-  int nsplit;
   MlaLayout(int R, int H, int k) {
-    nsplit = mla_num_splits(R, k);
+    const MlaWork w(R, H, k);
+    const size_t slots = 2 * (size_t)w.G, hg = (size_t)mla_heads_per_cta(H);
     size_t o = 0;
-    part_o = o;   o = align_up(o + (size_t)R * nsplit * H * kVDim * 4);
-    part_lse = o; o = align_up(o + (size_t)R * nsplit * H * 4);
+    part_o = o;   o = align_up(o + slots * hg * kVDim * 4);
+    part_lse = o; o = align_up(o + slots * hg * 4);
     q8 = o;       o = align_up(o + (size_t)R * H * 2 * kLatDim);   // E4M3 hi, lo per head
     qc = o;       o = align_up(o + (size_t)R * H * 4);             // per-head logit factor
     bytes = o;

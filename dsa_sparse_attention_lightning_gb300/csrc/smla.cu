@@ -138,27 +138,32 @@ mla_qprep_kernel(const __nv_bfloat16* __restrict__ q, int R, int H, float softma
 }
 
 // ---------------------------------------------------------------------------
-// Warp roles: warp 0 issues the MMAs and owns tensor memory; warp 1 gathers
-// latent rows with TMA (double-buffered); warps 2-9 run the softmax: warp w
-// reads TMEM lane quarter (w & 3) and token half (w - 2) / 4 of S.
-constexpr int kThreads2 = 320;
-constexpr int kSmWarp0 = 2;                           // first softmax warp
+// Warp roles (512 threads): warp 0 issues the MMAs and owns tensor memory;
+// warps 1-7 gather latent rows with TMA (double-buffered; 160 gather4 loads per
+// tile spread one per lane, since one warp's loads issue one lane at a time);
+// warps 8-15 run the softmax and the epilogues: warp w reads TMEM lane quarter
+// (w & 3) and token half (w - 8) / 4 of S.
+constexpr int kThreads = 512;
+constexpr int kGatherLanes = 23;                       // 7 x 23 >= 160 loads per tile
+constexpr int kSmWarp0 = 8;                            // first softmax warp
 constexpr int kSmThreads = 256;
-constexpr uint32_t kQCol = 0;                         // A operand: Q (dims 0..511), 128 cols
-constexpr uint32_t kSCol = 128;                       // S: [(head, term)] x [128 tokens]
-constexpr uint32_t kOCol2 = 256;                      // O^T: 4 blocks x HG cols
+constexpr uint32_t kPollNs = 128;                      // MMA warp's suspend limit per probe
+constexpr int kTileBytes = kLatAtoms * kAtom;          // one latent buffer
+constexpr uint32_t kQCol = 0;                          // A operand: Q (dims 0..511), 128 cols
+constexpr uint32_t kSCol = 128;                        // S: [(head, term)] x [128 tokens]
+constexpr uint32_t kOCol = 256;                        // O^T: 4 blocks x HG cols
 
 template <int HG>
-struct Mla2Smem {
+struct MlaSmem {
   static constexpr int lat = 0;                                      // [2][5][128][128]
-  static constexpr int qrope = 2 * kLatAtoms * kAtom;                // [128 rows][128 B]
+  static constexpr int qrope = 2 * kTileBytes;                       // [128 rows][128 B]
   static constexpr int p = qrope + kMlaTile * 128;                   // [2 terms][HG][128]
   static constexpr int corr = p + 2 * HG * 128;                      // [64] f32
   static constexpr int red = corr + 64 * 4;                          // [2 halves][64] f32
   static constexpr int lsum = red + 2 * 64 * 4;                      // [2 halves][64] f32
   static constexpr int flag = lsum + 2 * 64 * 4;                     // [2] int
-  static constexpr int bar = (flag + 8 + 7) / 8 * 8;                 // 8 mbarriers
-  static constexpr int tmem = bar + 8 * 8;
+  static constexpr int bar = (flag + 8 + 7) / 8 * 8;                 // 9 mbarriers
+  static constexpr int tmem = bar + 9 * 8;
   static constexpr int bytes = tmem + 16;
   static constexpr int alloc = bytes + 1024;
 };
@@ -189,15 +194,33 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// Walks a CTA's tiles in order: unit u (row u / groups, head group u % groups)
+// and tile lt within the unit; `first` / `last` mark the ends of a segment (a
+// run of the CTA's tiles in one unit).
+struct TileIt {
+  int u, lt, i;
+  __device__ __forceinline__ void next(int NT) {
+    ++i;
+    if (++lt == NT) { lt = 0; ++u; }
+  }
+  __device__ __forceinline__ int row(int groups) const { return groups == 1 ? u : u >> 1; }
+  __device__ __forceinline__ int hg0(int groups, int HG) const {
+    return groups == 1 ? 0 : (u & 1) * HG;
+  }
+  __device__ __forceinline__ bool first() const { return i == 0 || lt == 0; }
+  __device__ __forceinline__ bool last(int n, int NT) const { return i == n - 1 || lt == NT - 1; }
+};
+
 template <int HG>  // heads per CTA: 16, 32 or 64
-__global__ void __launch_bounds__(kThreads2, 1)
-smla2_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restrict__ q8,
-             const float* __restrict__ qc, int H, int64_t num_pages, float latent_scale,
-             const int32_t* __restrict__ block_table, int B, int max_pages,
-             const int32_t* __restrict__ row_req, const int32_t* __restrict__ row_len,
-             const int32_t* __restrict__ idx, int k, int tiles_per_split, int nsplit,
-             float* __restrict__ part_o, float* __restrict__ part_lse, uint32_t* status) {
-  using L = Mla2Smem<HG>;
+__global__ void __launch_bounds__(kThreads, 1)
+smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restrict__ q8,
+            const float* __restrict__ qc, int H, int64_t num_pages, float latent_scale,
+            const int32_t* __restrict__ block_table, int B, int max_pages,
+            const int32_t* __restrict__ row_req, const int32_t* __restrict__ row_len,
+            const int32_t* __restrict__ idx, int k, int R, float* __restrict__ part_o,
+            float* __restrict__ part_lse, __nv_bfloat16* __restrict__ out,
+            float* __restrict__ lse_out, uint32_t* status) {
+  using L = MlaSmem<HG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -209,24 +232,24 @@ smla2_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restr
   float* lsum_s = reinterpret_cast<float*>(smem + L::lsum);
   int* flag_s = reinterpret_cast<int*>(smem + L::flag);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar);
-  uint64_t* lat_full = bars;          // [2]
-  uint64_t* lat_empty = bars + 2;     // [2]
-  uint64_t* s_full = bars + 4;
-  uint64_t* s_empty = bars + 5;
-  uint64_t* p_full = bars + 6;
-  uint64_t* p_empty = bars + 7;
+  uint64_t* lat_full = bars;          // [2] gathered tile landed
+  uint64_t* lat_empty = bars + 2;     // [2] P.V of the tile finished with the buffer
+  uint64_t* s_full = bars + 4;        // S of a tile is in TMEM
+  uint64_t* s_empty = bars + 5;       // S read (and Q in place) for the next score MMA
+  uint64_t* p_full = bars + 6;        // P in shared memory, O rescaled
+  uint64_t* p_empty = bars + 7;       // P.V finished (O complete up to this tile)
+  uint64_t* mma_done = bars + 8;      // every issued MMA finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem);
 
-  const int split = blockIdx.x, r = blockIdx.y, hg0 = blockIdx.z * HG;
+  const int groups = H / HG;
+  const MlaWork w(R, H, k);
+  const int c = blockIdx.x;
+  const int64_t t0 = w.begin(c);
+  const int n = (int)(w.begin(c + 1) - t0);
+  const int NT = (int)w.NT;
+  const int u_first = (int)(t0 / w.NT);
+  const TileIt it0{u_first, (int)(t0 - (int64_t)u_first * w.NT), 0};
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int req = row_req[r];
-  const int len = row_len[r];
-  const bool row_valid =
-      req >= 0 && req < B && len >= 0 && (int64_t)len <= (int64_t)max_pages * kPage;
-  if (!row_valid && split == 0 && blockIdx.z == 0 && tid == 0) raise_dev(status, DSA_DEV_BAD_ROW);
-  const int slot0 = split * tiles_per_split * kMlaTile;
-  const int slot1 = min(k, slot0 + tiles_per_split * kMlaTile);
-  const int ntiles = (slot1 - slot0 + kMlaTile - 1) / kMlaTile;
 
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -237,7 +260,10 @@ smla2_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restr
     mbar_init(s_empty, 8);
     mbar_init(p_full, 8);
     mbar_init(p_empty, 1);
+    mbar_init(mma_done, 1);
     fence_mbar_init();
+    flag_s[0] = 0;
+    flag_s[1] = 0;
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -248,52 +274,14 @@ smla2_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restr
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // softmax-thread geometry: TMEM lane m = 32 * quarter + lane holds row m of S:
-  // head 16 * quarter + (lane & 15), term lane >> 4 (0: hi, 1: lo)
-  const bool sm_warp = warp >= kSmWarp0;
-  const int quarter = warp & 3;
-  const int th = sm_warp ? (warp - kSmWarp0) >> 2 : 0;
-  const int hl = 16 * quarter + (lane & 15);          // head within the group
-  const bool head_ok = hl < HG;
-
-  // ---- Q: rows (head, term) -> TMEM columns [0, 128) (dims 0..511) and the
-  // RoPE dims 512..575 -> shared (A operand of the last two K steps)
-  if (sm_warp && th == 0) {
-    const int term = lane >> 4;
-    const uint4* src = reinterpret_cast<const uint4*>(
-        q8 + (((size_t)r * H + hg0 + (head_ok ? hl : 0)) * 2 + term) * kLatDim);
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {                  // 4 x 32 columns = 512 bytes
-      uint32_t v[32];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const uint4 x = head_ok ? __ldg(src + c4 * 8 + u) : make_uint4(0, 0, 0, 0);
-        v[4 * u + 0] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
-      }
-      tmem_st_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + kQCol + c4 * 32, v);
-    }
-    const int m = quarter * 32 + lane;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const uint4 x = head_ok ? __ldg(src + 32 + c) : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(qrope + m * 128 + ((c ^ (m & 7)) << 4)) = x;
-    }
-    tmem_wait_st();
-    fence_proxy_async_smem();
-  }
-  if (tid < 2) flag_s[tid] = 0;
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-
   const uint32_t idesc_s = idesc_e4m3_f32(kMlaTile, kMlaTile, false, false);
   const uint32_t idesc_o = idesc_e4m3_f32(kMlaTile, HG, true, false);
-  bool alive = true;
 
   if (warp == 0) {
-    // ================= MMA issuer
+    // ================= MMA issuer: S(i) once tile i has landed and S(i - 1)
+    // has been read; O(i) once P(i) is in place -- whichever is ready first
     auto issue_s = [&](int i) {
-      const uint32_t lb = smem_u32(lat + (i & 1) * (kLatAtoms * kAtom));
+      const uint32_t lb = smem_u32(lat + (i & 1) * kTileBytes);
 #pragma unroll
       for (int j = 0; j < kIdxDim * 4 / 32; ++j)      // dims 0..511 from TMEM
         mma_e4m3_ts(tmem_base + kSCol, tmem_base + kQCol + (uint32_t)(j * 8),
@@ -305,53 +293,78 @@ smla2_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restr
                     desc_kmajor_sw128(lb + 4 * kAtom + j * 32), idesc_s, 1u);
       mma_commit(s_full);
     };
-    if (ntiles > 0) {
-      if (!wwait(&lat_full[0], 0, status)) alive = false;
-      if (alive) {
-        tc_fence_after();
-        if (lane == 0) issue_s(0);
-        __syncwarp();
-      }
-    }
-    for (int i = 0; i < ntiles && alive; ++i) {
-      if (i + 1 < ntiles) {
-        if (!wwait(&lat_full[(i + 1) & 1], (uint32_t)((i + 1) >> 1) & 1, status)) break;
-        if (!wwait(s_empty, (uint32_t)i & 1, status)) break;   // softmax(i) has read S
-        tc_fence_after();
-        if (lane == 0) issue_s(i + 1);
-        __syncwarp();
-      }
-      if (!wwait(p_full, (uint32_t)i & 1, status)) break;
-      tc_fence_after();
-      if (lane == 0) {
-        const uint32_t lb = smem_u32(lat + (i & 1) * (kLatAtoms * kAtom));
-        const uint32_t pb = smem_u32(ps);
+    auto issue_o = [&](int i, bool first) {
+      const uint32_t lb = smem_u32(lat + (i & 1) * kTileBytes);
+      const uint32_t pb = smem_u32(ps);
 #pragma unroll
-        for (int a = 0; a < kVDim / kMlaTile; ++a) {
+      for (int a = 0; a < kVDim / kMlaTile; ++a) {
 #pragma unroll
-          for (int kk = 0; kk < kMlaTile / 32; ++kk) {
-            const uint64_t ad = desc_kmajor_sw128(lb + a * kAtom + kk * 4096);   // 32 token rows
-            const uint32_t d = tmem_base + kOCol2 + (uint32_t)(a * HG);
-            mma_e4m3_ss(d, ad, desc_kmajor_sw128(pb + kk * 32), idesc_o,
-                        (i > 0 || kk > 0) ? 1u : 0u);
-            mma_e4m3_ss(d, ad, desc_kmajor_sw128(pb + HG * 128 + kk * 32), idesc_o, 1u);
-          }
+        for (int kk = 0; kk < kMlaTile / 32; ++kk) {
+          const uint64_t ad = desc_kmajor_sw128(lb + a * kAtom + kk * 4096);   // 32 token rows
+          const uint32_t d = tmem_base + kOCol + (uint32_t)(a * HG);
+          mma_e4m3_ss(d, ad, desc_kmajor_sw128(pb + kk * 32), idesc_o,
+                      (!first || kk > 0) ? 1u : 0u);
+          mma_e4m3_ss(d, ad, desc_kmajor_sw128(pb + HG * 128 + kk * 32), idesc_o, 1u);
         }
-        mma_commit(p_empty);
-        mma_commit(&lat_empty[i & 1]);
       }
-      __syncwarp();
+      mma_commit(p_empty);
+      mma_commit(&lat_empty[i & 1]);
+    };
+    if (lane == 0 && n > 0) {
+      int si = 0, oi = 0;
+      TileIt ot = it0;                                // tile of the next O
+      long long t_last = clock64();
+      while (oi < n) {
+        bool prog = false;
+        // probes sleep in hardware (a busy poll would steal the shared-memory
+        // pipe from the softmax warps)
+        if (si < n && si <= oi + 1 &&
+            mbar_try_wait_ns(&lat_full[si & 1], (uint32_t)(si >> 1) & 1, kPollNs) &&
+            mbar_try_wait_ns(s_empty, (uint32_t)si & 1, kPollNs)) {
+          tc_fence_after();
+          issue_s(si);
+          ++si;
+          prog = true;
+        }
+        if (oi < si && mbar_try_wait_ns(p_full, (uint32_t)oi & 1, kPollNs)) {
+          tc_fence_after();
+          issue_o(oi, ot.first());
+          ot.next(NT);
+          ++oi;
+          prog = true;
+        }
+        if (prog) {
+          t_last = clock64();
+        } else if (clock64() - t_last > kWaitCycles) {
+          raise_dev(status, DSA_DEV_TIMEOUT);
+          break;
+        }
+      }
+      mma_commit(mma_done);                           // tensor memory is freed only after this
+      mbar_wait(mma_done, 0, status);
     }
-  } else if (warp == 1) {
-    // ================= TMA gather: lane g fetches tile rows 4g..4g+3 (5 boxes each)
-    int y[4];
-    auto lookup = [&](int i) {
+    __syncwarp();
+  } else if (warp < kSmWarp0) {
+    // ================= TMA gather: lane op = (group g of 4 tile rows, box a of 5)
+    const int op = (warp - 1) * kGatherLanes + lane;
+    const bool op_ok = lane < kGatherLanes && op < 32 * kLatAtoms;
+    const int g = op & 31, a = op >> 5;
+    int y[4] = {-1, -1, -1, -1};
+    TileIt gt = it0;                                  // tile of the next lookup
+    auto lookup = [&]() {
+      const int r = gt.row(groups);
+      const int req = row_req[r];
+      const int len = row_len[r];
+      const bool row_valid =
+          req >= 0 && req < B && len >= 0 && (int64_t)len <= (int64_t)max_pages * kPage;
+      if (!row_valid && gt.lt == 0 && gt.hg0(groups, HG) == 0 && op == 0)
+        raise_dev(status, DSA_DEV_BAD_ROW);
+      const int slot0 = gt.lt * kMlaTile;
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        const int row = 4 * lane + u;
-        const int j = slot0 + i * kMlaTile + row;
+        const int j = slot0 + 4 * g + u;
         int yy = -1;                                  // out of range: zero-filled by TMA
-        if (row_valid && j < slot1) {
+        if (row_valid && j < k) {
           const int tok = idx[(size_t)r * k + j];
           if (tok >= len) {
             raise_dev(status, DSA_DEV_BAD_INDEX);
@@ -365,85 +378,152 @@ smla2_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restr
         }
         y[u] = yy;
       }
+      gt.next(NT);
     };
-    if (ntiles > 0) lookup(0);
-    for (int i = 0; i < ntiles; ++i) {
+    if (op_ok && n > 0) lookup();
+    for (int i = 0; i < n; ++i) {
       const int b = i & 1;
       if (!wwait(&lat_empty[b], ((uint32_t)(i >> 1) & 1) ^ 1, status)) break;
-      if (lane == 0) mbar_arrive_expect_tx(&lat_full[b], kLatAtoms * kAtom);
-      __syncwarp();
-      uint8_t* lt = lat + b * (kLatAtoms * kAtom) + 4 * lane * 128;
-#pragma unroll
-      for (int a = 0; a < kLatAtoms; ++a)
-        tma_gather4(lt + a * kAtom, &lat_map, a * 128, y[0], y[1], y[2], y[3], &lat_full[b]);
-      if (i + 1 < ntiles) lookup(i + 1);
+      // complete_tx of other warps may land before this arrive: the phase
+      // cannot complete until the single arrival has come
+      if (warp == 1 && lane == 0) mbar_arrive_expect_tx(&lat_full[b], kTileBytes);
+      if (op_ok) {
+        tma_gather4(lat + b * kTileBytes + a * kAtom + g * 512, &lat_map, a * 128, y[0], y[1],
+                    y[2], y[3], &lat_full[b]);
+        if (i + 1 < n) lookup();
+      }
     }
     // no copy may still be landing in shared memory when the CTA exits
-    if (ntiles > 0) {
-      const int last = ntiles - 1;
+    if (warp == 1 && n > 0) {
+      const int last = n - 1;
       wwait(&lat_full[last & 1], (uint32_t)(last >> 1) & 1, status);
-      if (ntiles > 1) wwait(&lat_full[(last - 1) & 1], (uint32_t)((last - 1) >> 1) & 1, status);
+      if (n > 1) wwait(&lat_full[(last - 1) & 1], (uint32_t)((last - 1) >> 1) & 1, status);
     }
   } else {
-    // ================= softmax (warps 4-11)
-    const float qcf = head_ok ? qc[(size_t)r * H + hg0 + hl] : 0.f;
-    float m_run = -INFINITY, l_run = 0.f;
-    // validity of this warp's 64 tokens (tokens th*64 + lane and th*64 + 32 + lane):
-    // the selected ids are loaded a tile ahead and turned into bit masks late
-    auto load_ids = [&](int i, int& a, int& b) {
-      const int j = slot0 + i * kMlaTile + th * 64 + lane;
-      a = (row_valid && j < slot1) ? __ldg(idx + (size_t)r * k + j) : -1;
-      b = (row_valid && j + 32 < slot1) ? __ldg(idx + (size_t)r * k + j + 32) : -1;
+    // ================= softmax + epilogues
+    const int sw = warp - kSmWarp0;
+    const int quarter = warp & 3;
+    const int th = sw >> 2;                            // token half of the tile
+    const int hl = 16 * quarter + (lane & 15);          // head within the group
+    const bool head_ok = hl < HG;
+    const int stid = tid - kSmWarp0 * 32;
+    bool alive = true;
+
+    // Q of unit u: rows (head, term) -> TMEM columns [0, 128) (dims 0..511)
+    // and the RoPE dims 512..575 -> shared (A operand of the last two K steps)
+    auto load_q = [&](int r, int hg0) {
+      if (th != 0) return;
+      const int term = lane >> 4;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          q8 + (((size_t)r * H + hg0 + (head_ok ? hl : 0)) * 2 + term) * kLatDim);
+#pragma unroll 1
+      for (int c8 = 0; c8 < 8; ++c8) {                // 8 x 16 columns = 512 bytes
+        uint32_t v[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 x = head_ok ? __ldg(src + c8 * 4 + u) : make_uint4(0, 0, 0, 0);
+          v[4 * u + 0] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+        }
+        tmem_st_32x32b_x16(tmem_base + ((uint32_t)(quarter * 32) << 16) + kQCol + c8 * 16, v);
+      }
+      const int m = quarter * 32 + lane;
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const uint4 x = head_ok ? __ldg(src + 32 + c4) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qrope + m * 128 + ((c4 ^ (m & 7)) << 4)) = x;
+      }
+      tmem_wait_st();
+      fence_proxy_async_smem();
     };
-    auto valid_bits = [&](int a, int b, uint32_t& lo_bits, uint32_t& hi_bits) {
-      lo_bits = __ballot_sync(0xffffffffu, a >= 0 && a < len);
-      hi_bits = __ballot_sync(0xffffffffu, b >= 0 && b < len);
+    auto load_qc = [&](int r, int hg0) {
+      return head_ok ? __ldg(qc + (size_t)r * H + hg0 + hl) : 0.f;
+    };
+
+    float m_run = -INFINITY, l_run = 0.f, qcf = 0.f;
+    int seg_lt0 = 0;                                  // first tile (within its unit) of the segment
+    // validity of this warp's 64 tokens (tokens th*64 + lane and th*64 + 32 + lane).
+    // The ids are loaded a tile ahead from clamped addresses, so that nothing
+    // consumes a load before the end of the tile; len_ok is -1 for an invalid row.
+    int len_ok = -1;                                  // row length of the prepared tile's unit
+    auto unit_len = [&](const TileIt& t) {
+      const int r = t.row(groups);
+      const int req = row_req[r];
+      const int len = row_len[r];
+      const bool row_valid =
+          req >= 0 && req < B && len >= 0 && (int64_t)len <= (int64_t)max_pages * kPage;
+      return row_valid ? len : -1;
+    };
+    auto load_ids = [&](const TileIt& t, int& ia, int& ib) {
+      const int* rowp = idx + (size_t)t.row(groups) * k;
+      const int j = t.lt * kMlaTile + th * 64 + lane;
+      ia = __ldg(rowp + min(j, k - 1));
+      ib = __ldg(rowp + min(j + 32, k - 1));
+    };
+    auto valid_bits = [&](const TileIt& t, int ia, int ib, uint32_t& lo_bits, uint32_t& hi_bits) {
+      const int j = t.lt * kMlaTile + th * 64 + lane;
+      lo_bits = __ballot_sync(0xffffffffu, j < k && ia >= 0 && ia < len_ok);
+      hi_bits = __ballot_sync(0xffffffffu, j + 32 < k && ib >= 0 && ib < len_ok);
     };
     uint32_t vlo = 0, vhi = 0;
     int ida = -1, idb = -1;
-    if (ntiles > 0) {
-      load_ids(0, ida, idb);
-      valid_bits(ida, idb, vlo, vhi);
-    }
-    for (int i = 0; i < ntiles; ++i) {
-      // ---- S rows -> registers, then S may be overwritten by the next tile's MMA
-      if (!wwait(s_full, (uint32_t)i & 1, status)) { alive = false; }
-      tc_fence_after();
-      uint32_t s0[32], s1[32];
-      const uint32_t ta = tmem_base + ((uint32_t)(quarter * 32) << 16) + kSCol + th * 64;
-      if (alive) {
-        tmem_ld_32x32b_x32(ta, s0);
-        tmem_ld_32x32b_x32(ta + 32, s1);
-        tmem_wait_ld();
-      }
+    TileIt ta = it0;                                  // current tile
+    if (n > 0) {
+      load_q(ta.row(groups), ta.hg0(groups, HG));
+      qcf = load_qc(ta.row(groups), ta.hg0(groups, HG));
+      seg_lt0 = ta.lt;
+      len_ok = unit_len(ta);
+      load_ids(ta, ida, idb);
+      valid_bits(ta, ida, idb, vlo, vhi);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(s_empty);
-      if (i + 1 < ntiles) load_ids(i + 1, ida, idb);
-      // ---- combine the two query terms: lane < 16 keeps tokens 0..31 of this
-      // warp's half, lane >= 16 tokens 32..63; the partner lane (lane ^ 16)
-      // holds the other term
+      if (lane == 0) mbar_arrive(s_empty);            // Q in place for S(0)
+    }
+    for (int i = 0; i < n; ++i, ta.next(NT)) {
+      TileIt tn = ta;                                 // the tile after this one
+      tn.next(NT);
+      const bool seg_last = ta.last(n, NT);
+      // ---- S rows -> registers, then S may be overwritten by the next tile's MMA
+      if (!wwait(s_full, (uint32_t)i & 1, status)) alive = false;
+      tc_fence_after();
+      // rows 32q + j hold the hi term of head 16q + j, rows 32q + 16 + j the lo
+      // term: thread t gets both for head 16q + (t & 15) and 32 tokens
+      // (t < 16: tokens 0..31 of the warp's half, t >= 16: tokens 32..63)
+      const uint32_t tq = tmem_base + ((uint32_t)(quarter * 32) << 16);
       const bool hi_lane = lane < 16;
       const uint32_t vb = hi_lane ? vlo : vhi;
       float y[32];
       float tmax = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float send = __uint_as_float(hi_lane ? s1[j] : s0[j]);
-        const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-        const float hi_t = hi_lane ? __uint_as_float(s0[j]) : recv;
-        const float lo_t = hi_lane ? recv : __uint_as_float(s1[j]);
-        y[j] = ((vb >> j) & 1u) ? (hi_t + lo_t * (1.f / 32.f)) * qcf : -INFINITY;
-        tmax = fmaxf(tmax, y[j]);
+      for (int h16 = 0; h16 < 2; ++h16) {             // 16 tokens at a time
+        uint32_t s_hi[16], s_lo[16];
+        if (alive) {
+          tmem_ld_16x32bx2_x16<32>(tq + kSCol + th * 64 + h16 * 16, s_hi);
+          tmem_ld_16x32bx2_x16<32>(tq + (16u << 16) + kSCol + th * 64 + h16 * 16, s_lo);
+          tmem_wait_ld();
+        }
+        // ---- the two query terms -> log2-domain logits
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float x = __uint_as_float(s_hi[j]) + __uint_as_float(s_lo[j]) * (1.f / 32.f);
+          const int jj = h16 * 16 + j;
+          y[jj] = ((vb >> jj) & 1u) ? x * qcf : -INFINITY;
+          tmax = fmaxf(tmax, y[jj]);
+        }
       }
+      if (seg_last && i + 1 < n && alive)              // next tile starts a new unit: its Q
+        load_q(tn.row(groups), tn.hg0(groups, HG));
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(s_empty);
+      if (i + 1 < n) load_ids(tn, ida, idb);
       tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, 16));
       if (hi_lane && head_ok) red_s[th * 64 + hl] = tmax;
       named_sync(1, kSmThreads);
       // every softmax warp is past tile i - 1 here: its flag slot can be reused
-      if (tid == kSmWarp0 * 32) flag_s[(i + 1) & 1] = 0;
+      if (stid == 0) flag_s[(i + 1) & 1] = 0;
       if (head_ok) tmax = fmaxf(tmax, red_s[(th ^ 1) * 64 + hl]);
       float corr = 1.f;
-      if (tmax > m_run + kRescaleT) {                 // m_run = -inf on the first valid tile
+      if (tmax > m_run + kRescaleT) {                 // m_run = -inf on a segment's first tile
         corr = fast_exp2(m_run - tmax);
         m_run = tmax;
       }
@@ -474,26 +554,25 @@ smla2_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restr
       l_run = l_run * corr + psum;
       if (head_ok) {
         // this thread's 32 tokens = two 16-byte chunks of row hl of P^T (K-major, swizzled)
-        const int t0 = th * 64 + (hi_lane ? 0 : 32);
+        const int tt = th * 64 + (hi_lane ? 0 : 32);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const int chunk = (t0 >> 4) + c;
+        for (int c2 = 0; c2 < 2; ++c2) {
+          const int chunk = (tt >> 4) + c2;
           const int off = hl * 128 + ((chunk ^ (hl & 7)) << 4);
           *reinterpret_cast<uint4*>(ps + off) =
-              make_uint4(whi[4 * c], whi[4 * c + 1], whi[4 * c + 2], whi[4 * c + 3]);
+              make_uint4(whi[4 * c2], whi[4 * c2 + 1], whi[4 * c2 + 2], whi[4 * c2 + 3]);
           *reinterpret_cast<uint4*>(ps + HG * 128 + off) =
-              make_uint4(wlo[4 * c], wlo[4 * c + 1], wlo[4 * c + 2], wlo[4 * c + 3]);
+              make_uint4(wlo[4 * c2], wlo[4 * c2 + 1], wlo[4 * c2 + 2], wlo[4 * c2 + 3]);
         }
       }
       // ---- rescale O^T when a running maximum moved (O(i-1) is complete: p_empty)
-      if (i > 0 && flag_s[i & 1] && alive) {
+      if (!ta.first() && flag_s[i & 1] && alive) {
         constexpr int CWO = HG < 32 ? HG : 32;
-#pragma unroll
+#pragma unroll 1
         for (int a = 2 * th; a < 2 * th + 2; ++a) {
-#pragma unroll
+#pragma unroll 1
           for (int c0 = 0; c0 < HG; c0 += CWO) {
-            const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + kOCol2 +
-                                (uint32_t)(a * HG + c0);
+            const uint32_t tb = tq + kOCol + (uint32_t)(a * HG + c0);
             if (CWO == 32) {
               uint32_t d[32];
               tmem_ld_32x32b_x32(tb, d);
@@ -517,74 +596,106 @@ smla2_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restr
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
-      if (i + 1 < ntiles) valid_bits(ida, idb, vlo, vhi);
-    }
-    // ---- epilogue: l over the 4 threads of a head, then O^T / l -> partial output
-    if (ntiles > 0 && !wwait(p_empty, (uint32_t)(ntiles - 1) & 1, status)) alive = false;
-    tc_fence_after();
-    const float lpair = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
-    if (lane < 16 && head_ok) lsum_s[th * 64 + hl] = lpair;
-    named_sync(1, kSmThreads);
-    const size_t pbase = ((size_t)r * nsplit + split) * H + hg0;
-    constexpr int CWO = HG < 32 ? HG : 32;
+      if (i + 1 < n) {
+        if (tn.lt == 0) len_ok = unit_len(tn);        // the next tile starts a unit
+        valid_bits(tn, ida, idb, vlo, vhi);
+      }
+      if (!seg_last) continue;
+
+      // ---- end of a segment: O complete -> normalised output (whole unit) or
+      // a partial for the combine (unit cut by the CTA range)
+      if (!wwait(p_empty, (uint32_t)i & 1, status)) alive = false;
+      tc_fence_after();
+      const float lpair = l_run + __shfl_xor_sync(0xffffffffu, l_run, 16);
+      if (lane < 16 && head_ok) lsum_s[th * 64 + hl] = lpair;
+      named_sync(1, kSmThreads);
+      if (th == 0 && lane < 16 && head_ok) {          // output factor of head hl
+        const float l = lsum_s[hl] + lsum_s[64 + hl];
+        corr_s[hl] = (alive && l > 0.f) ? latent_scale / l : 0.f;
+      }
+      named_sync(1, kSmThreads);
+      const bool whole = seg_lt0 == 0 && ta.lt == NT - 1;
+      const int slot = 2 * c + (ta.u == u_first ? 0 : 1);
+      const int r = ta.row(groups), hg0 = ta.hg0(groups, HG);
+      constexpr int CWO = HG < 32 ? HG : 32;
+#pragma unroll 1
+      for (int a = 2 * th; a < 2 * th + 2; ++a) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < HG; c0 += CWO) {
+          uint32_t d[32];
+          const uint32_t tb = tq + kOCol + (uint32_t)(a * HG + c0);
+          if (alive) {
+            if constexpr (CWO == 32) tmem_ld_32x32b_x32(tb, d);
+            else tmem_ld_32x32b_x16(tb, *reinterpret_cast<uint32_t(*)[16]>(d));
+            tmem_wait_ld();
+          }
+          const int dim = a * kMlaTile + quarter * 32 + lane;
 #pragma unroll
-    for (int a = 2 * th; a < 2 * th + 2; ++a) {
-#pragma unroll
-      for (int c0 = 0; c0 < HG; c0 += CWO) {
-        uint32_t d[32];
-        const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16) + kOCol2 +
-                            (uint32_t)(a * HG + c0);
-        if (alive && ntiles > 0) {
-          tmem_ld_32x32b_x32(tb, d);
-          tmem_wait_ld();
-        }
-#pragma unroll
-        for (int u = 0; u < CWO; ++u) {
-          const int h = c0 + u;
-          const float l = lsum_s[h] + lsum_s[64 + h];
-          const float o = (alive && ntiles > 0 && l > 0.f) ? __uint_as_float(d[u]) * (latent_scale / l)
-                                                            : 0.f;
-          part_o[(pbase + h) * kVDim + a * kMlaTile + quarter * 32 + lane] = o;
+          for (int u = 0; u < CWO; ++u) {
+            const int h = c0 + u;
+            const float o = alive ? __uint_as_float(d[u]) * corr_s[h] : 0.f;
+            if (whole)
+              out[((size_t)r * H + hg0 + h) * kVDim + dim] = __float2bfloat16_rn(o);
+            else
+              part_o[((size_t)slot * HG + h) * kVDim + dim] = o;
+          }
         }
       }
-    }
-    if (th == 0 && (lane & 16) == 0 && head_ok) {
-      const float l = lsum_s[hl] + lsum_s[64 + hl];
-      part_lse[pbase + hl] = (alive && l > 0.f && m_run > -INFINITY)
-                                 ? (m_run + log2f(l)) * 0.6931471805599453f
-                                 : -INFINITY;
+      if (th == 0 && (lane & 16) == 0 && head_ok) {
+        const float l = lsum_s[hl] + lsum_s[64 + hl];
+        const float ls = (alive && l > 0.f && m_run > -INFINITY)
+                             ? (m_run + log2f(l)) * 0.6931471805599453f
+                             : -INFINITY;
+        if (!whole) part_lse[(size_t)slot * HG + hl] = ls;
+        else if (lse_out) lse_out[(size_t)r * H + hg0 + hl] = ls;
+      }
+      tc_fence_before();
+      m_run = -INFINITY;
+      l_run = 0.f;
+      if (i + 1 < n) {
+        qcf = load_qc(tn.row(groups), tn.hg0(groups, HG));
+        seg_lt0 = tn.lt;
+      }
     }
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
-    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-// One CTA per (row, head): merge the splits' partials by log-sum-exp.
+// One CTA per (row, head) of a unit cut by CTA ranges: merge its partials by
+// log-sum-exp.  Units held whole by one CTA were written by the main kernel.
 __global__ void __launch_bounds__(128)
-mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int H,
-                   int nsplit, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
+mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int R,
+                   int H, int k, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   const int r = blockIdx.x / H, h = blockIdx.x % H;
+  const int HG = mla_heads_per_cta(H);
+  const int u = r * (H / HG) + h / HG, hl = h % HG;
+  const MlaWork w(R, H, k);
   float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, part_lse[((size_t)r * nsplit + s) * H + h]);
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   float Z = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < nsplit; ++s) {
-      const size_t pb = ((size_t)r * nsplit + s) * H + h;
-      const float ls = part_lse[pb];
-      if (ls == -INFINITY) continue;
-      const float ws = __expf(ls - M);
-      Z += ws;
-      const float4 v = __ldg(reinterpret_cast<const float4*>(part_o + pb * kVDim) + threadIdx.x);
-      acc[0] = fmaf(ws, v.x, acc[0]);
-      acc[1] = fmaf(ws, v.y, acc[1]);
-      acc[2] = fmaf(ws, v.z, acc[2]);
-      acc[3] = fmaf(ws, v.w, acc[3]);
+  if (w.T > 0) {
+    const int c0 = w.cta_of((int64_t)u * w.NT), c1 = w.cta_of((int64_t)(u + 1) * w.NT - 1);
+    if (c0 == c1) return;
+    auto slot = [&](int c) { return 2 * c + (w.begin(c) / w.NT == u ? 0 : 1); };
+    for (int c = c0; c <= c1; ++c) M = fmaxf(M, part_lse[(size_t)slot(c) * HG + hl]);
+    if (M != -INFINITY) {
+      for (int c = c0; c <= c1; ++c) {
+        const size_t pb = (size_t)slot(c) * HG + hl;
+        const float ls = part_lse[pb];
+        if (ls == -INFINITY) continue;
+        const float ws = __expf(ls - M);
+        Z += ws;
+        const float4 v = __ldg(reinterpret_cast<const float4*>(part_o + pb * kVDim) + threadIdx.x);
+        acc[0] = fmaf(ws, v.x, acc[0]);
+        acc[1] = fmaf(ws, v.y, acc[1]);
+        acc[2] = fmaf(ws, v.z, acc[2]);
+        acc[3] = fmaf(ws, v.w, acc[3]);
+      }
     }
   }
   const float inv = Z > 0.f ? 1.f / Z : 0.f;
@@ -631,20 +742,18 @@ cudaError_t latent_tensor_map(CUtensorMap* map, const uint8_t* cache, int64_t nu
 }
 
 template <int HG>
-cudaError_t launch_smla_group(const MlaArgs& a, const MlaLayout& L, cudaStream_t st) {
-  using S = Mla2Smem<HG>;
+cudaError_t launch_smla(const MlaArgs& a, const MlaLayout& L, int G, cudaStream_t st) {
+  using S = MlaSmem<HG>;
   alignas(64) CUtensorMap map;
-  cudaError_t me = latent_tensor_map(&map, a.latent_cache, a.num_pages);
-  if (me != cudaSuccess) return me;
-  cudaError_t e = cudaFuncSetAttribute(smla2_kernel<HG>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, S::alloc);
+  cudaError_t e = latent_tensor_map(&map, a.latent_cache, a.num_pages);
   if (e != cudaSuccess) return e;
-  dim3 grid(L.nsplit, a.R, a.H / HG);
-  smla2_kernel<HG><<<grid, kThreads2, S::alloc, st>>>(
-      map, a.scratch + L.q8, reinterpret_cast<const float*>(a.scratch + L.qc), a.H,
-      a.num_pages, a.latent_scale, a.block_table, a.B, a.max_pages, a.row_req, a.row_len, a.idx, a.k,
-      mla_tiles_per_split(a.R, a.k), L.nsplit, reinterpret_cast<float*>(a.scratch + L.part_o),
-      reinterpret_cast<float*>(a.scratch + L.part_lse), a.status);
+  e = cudaFuncSetAttribute(smla_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::alloc);
+  if (e != cudaSuccess) return e;
+  smla_kernel<HG><<<G, kThreads, S::alloc, st>>>(
+      map, a.scratch + L.q8, reinterpret_cast<const float*>(a.scratch + L.qc), a.H, a.num_pages,
+      a.latent_scale, a.block_table, a.B, a.max_pages, a.row_req, a.row_len, a.idx, a.k, a.R,
+      reinterpret_cast<float*>(a.scratch + L.part_o), reinterpret_cast<float*>(a.scratch + L.part_lse),
+      static_cast<__nv_bfloat16*>(a.out), a.lse, a.status);
   return cudaGetLastError();
 }
 
@@ -653,18 +762,21 @@ cudaError_t launch_smla_group(const MlaArgs& a, const MlaLayout& L, cudaStream_t
 cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t st) {
   if (a.R == 0) return cudaSuccess;
   const MlaLayout L(a.R, a.H, a.k);
-  const int warps = a.R * a.H;
-  mla_qprep_kernel<<<(warps + 7) / 8, 256, 0, st>>>(
-      static_cast<const __nv_bfloat16*>(a.q), a.R, a.H, a.softmax_scale, a.latent_scale,
-      a.scratch + L.q8, reinterpret_cast<float*>(a.scratch + L.qc));
-  cudaError_t e;
-  if (a.H == 16) e = launch_smla_group<16>(a, L, st);
-  else if (a.H == 32) e = launch_smla_group<32>(a, L, st);
-  else e = launch_smla_group<64>(a, L, st);
-  if (e != cudaSuccess) return e;
+  const MlaWork w(a.R, a.H, a.k);
+  if (w.G > 0) {
+    const int warps = a.R * a.H;
+    mla_qprep_kernel<<<(warps + 7) / 8, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(a.q), a.R, a.H, a.softmax_scale, a.latent_scale,
+        a.scratch + L.q8, reinterpret_cast<float*>(a.scratch + L.qc));
+    cudaError_t e;
+    if (a.H == 16) e = launch_smla<16>(a, L, w.G, st);
+    else if (a.H == 32) e = launch_smla<32>(a, L, w.G, st);
+    else e = launch_smla<64>(a, L, w.G, st);
+    if (e != cudaSuccess) return e;
+  }
   mla_combine_kernel<<<a.R * a.H, 128, 0, st>>>(reinterpret_cast<const float*>(a.scratch + L.part_o),
                                                 reinterpret_cast<const float*>(a.scratch + L.part_lse),
-                                                a.H, L.nsplit, static_cast<__nv_bfloat16*>(a.out),
+                                                a.R, a.H, a.k, static_cast<__nv_bfloat16*>(a.out),
                                                 a.lse);
   return cudaGetLastError();
 }

@@ -35,6 +35,14 @@ SMALL = [
 ]
 
 
+# Many short units: CTA ranges hold whole units (written straight out) as well
+# as cut ones (merged by the combine), for one and for two head groups.
+MLA_WIDE = [
+    inputs.Workload("many_rows_h16", [300, 1000, 257] * 20, [7] * 60, H=16, k=256, seed=5),
+    inputs.Workload("many_units_h128", [700, 260] * 10, [5] * 20, H=128, k=256, seed=6),
+]
+
+
 def _sub(host, rows):
     """Host inputs restricted to the given rows (caches and block table unchanged)."""
     h = dict(host)
@@ -127,7 +135,7 @@ def test_topk_long_row_split_over_chunks(dsa, oracle_mod):
 
 
 # --------------------------------------------------------------- sparse MLA
-@pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
+@pytest.mark.parametrize("wl", SMALL + MLA_WIDE, ids=[w.name for w in SMALL + MLA_WIDE])
 def test_sparse_mla_matches_oracle(dsa, oracle_mod, wl):
     inp = inputs.make_inputs(wl, device=DEV)
     host = inputs.to_numpy(inp)
