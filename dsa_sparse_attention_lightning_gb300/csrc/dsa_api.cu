@@ -2,9 +2,44 @@
 // argument validation, workspace carving and the launch sequence of each
 // entry point.  No allocation, no host synchronisation (except the explicit
 // status read), no global mutable state.
+#include <cudaTypedefs.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "dsa_common.cuh"
+
+namespace dsa {
+
+cudaError_t encode_tensor_map_u8(CUtensorMap* map, int rank, const void* base, const uint64_t* dims,
+                                 const uint64_t* strides, const uint32_t* box) {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  if (!enc) return cudaErrorNotSupported;
+  if (rank < 1 || rank > 5) return cudaErrorInvalidValue;
+  cuuint64_t d[5], st[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) st[i] = strides[i];
+  }
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base),
+                         d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace dsa
 
 using namespace dsa;
 

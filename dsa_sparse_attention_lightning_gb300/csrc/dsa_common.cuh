@@ -3,6 +3,7 @@
 // oracle.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -143,5 +144,12 @@ struct MlaArgs {
   uint32_t* status;
 };
 cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t st);
+
+// Tiled TMA descriptor over a byte tensor of the given rank: dims[0] is the
+// contiguous extent, strides[i] the byte stride of dim i + 1, box the tile
+// copied per load; 128-byte swizzle, out-of-range elements read as zero.
+// The driver entry point is looked up once per process.
+cudaError_t encode_tensor_map_u8(CUtensorMap* map, int rank, const void* base, const uint64_t* dims,
+                                 const uint64_t* strides, const uint32_t* box);
 
 }  // namespace dsa

@@ -12,24 +12,29 @@
 //    up to 4 rows; the group's keys are read from HBM once for all its rows,
 //    as the pages' MI350X scorer does for verification rows ("Reducing
 //    indexer overhead on AMD MI350X").
-//  * Per 128-token tile the contraction is a real GEMM,
-//      D[token, (row, head)] = K8[token, 0:128] . Q[(row, head), 0:128]^T,
-//    M = 128 tokens, N = 32 x rows, K = 128: one tcgen05.mma kind::f16 chain
-//    with the accumulator in tensor memory.  Keys are widened E4M3 -> f16 in
-//    shared memory (exact: E4M3 is a subset of f16); the bf16 query is
-//    rescaled per (row, head) by a power of two into f16 range (exact for all
-//    but values 2^-22 below the head's absmax) and the inverse power of two is
-//    folded into the head weight.  Accumulation is f32.
-//  * Each TMEM lane holds one token's (row, head) logits, so the ReLU-weighted
-//    head sum is a per-thread loop: no shuffles.
-//  * Persistent CTAs, one per SM, each taking a contiguous run of (group, tile)
-//    work items; warp roles: 0 MMA issuer and TMEM owner, 1-2 loaders, 3-10
-//    converters, 11-14 epilogue (TMEM -> scores).
-//  * The loaders stream the keys HBM -> shared staging with 16-byte cp.async
-//    copies, kStages tiles ahead (64 KB in flight per SM; many small copies
-//    sustain more bandwidth here than page-sized bulk copies issued by one
-//    thread); the converters widen them to f16 and store the swizzled
-//    tensor-core operand.
+//  * Per 128-token tile the contraction is one GEMM on the FP8 tensor cores,
+//      D[token, (row, head)] = [K8 | K8][token, 0:256] . [Qhi | Qlo][(row, head), 0:256]^T,
+//    M = 128 tokens, N = 32 x rows, K = 2 x 128, kind::f8f6f4 with f32
+//    accumulators in tensor memory: the two query terms are two halves of
+//    the contraction against the same key operand, so the tensor core adds
+//    them.  The keys are the A operand exactly as they sit in the cache: TMA
+//    moves a page's 64 x 128-byte key block straight into the
+//    128-byte-swizzled K-major layout, no conversion.
+//  * A bf16 query is split into two E4M3 terms per (row, head): s = q * 2^a
+//    with a power of two putting the head's absmax in [128, 256), hi =
+//    E4M3(s), lo = E4M3(s - hi); 2^-a is folded into the head weight.  The
+//    split is exact for every |s| >= 1/4 (all but query elements below about
+//    1/500 of the head's absmax, where lo keeps a 2^-9 grid).  An E4M3 query
+//    is its own hi term (lo = 0) and its scale is folded into the weight.
+//  * Each TMEM lane holds one token's (row, head) logits, so the
+//    ReLU-weighted head sum is a per-thread loop: no shuffles.
+//  * Persistent CTAs, one per SM, each taking a contiguous run of (group,
+//    tile) work items; warp roles: 0 MMA issuer and TMEM owner, 1-4 TMA
+//    producers (keys, key scales, group queries; page ids looked up 32 tiles
+//    ahead; tile i is loaded by producer i % 4 -- TMA loads issued from one
+//    thread complete at about half the HBM rate, so each SM runs several
+//    streams), 5-12 epilogue (TMEM -> scores; warp w takes TMEM lane
+//    quarter w % 4, i.e. 32 tokens, of two of the group's rows).
 #include <limits.h>
 #include <math.h>
 
@@ -42,42 +47,40 @@ namespace {
 using namespace ptx;
 
 constexpr int kTileTok = 128;
-constexpr int kAtomBytes = kTileTok * 128;              // 128 rows x 128 B (64 f16 of K)
-constexpr int kABytes = 2 * kAtomBytes;                 // K = 128 f16 = two atoms
-constexpr int kABufs = 3;                               // f16 key tiles in flight to the MMA
 constexpr int kMaxGroupRows = 4;
-constexpr int kLoadWarps = 2;                           // warps 1-2
-constexpr int kLoadThreads = 32 * kLoadWarps;
-constexpr int kConvThreads = 256;                       // warps 3-10
-constexpr int kChunks = kTileTok * 8 / kConvThreads;    // 16-byte key chunks per thread per tile
-constexpr int kStages = 4;                              // tiles of keys in flight per SM
-constexpr int kEpiWarp0 = 1 + kLoadWarps + kConvThreads / 32;   // warps 11-14
-constexpr int kThreads = (kEpiWarp0 + 4) * 32;
-constexpr int kDBufs = 4;                               // TMEM accumulators of 128 columns
-constexpr uint32_t kTmemCols = 128 * kDBufs;
+constexpr int kQAtom = kMaxGroupRows * kIdxHeads * kIdxDim;  // 128 rows x 128 B: one query term
+constexpr int kQBytes = 2 * kQAtom;                     // one group's query operand (hi, lo)
+constexpr int kQBufs = 2;
+constexpr int kStages = 8;                              // key tiles in flight per SM
+constexpr int kKeyTileBytes = kTileTok * kIdxDim;       // 2 pages x 64 x 128 B
+constexpr int kPageKeyBytes = kPage * kIdxDim;          // 8192
+constexpr int kPageBytes = kPage * (kIdxDim + 4);       // 8448: keys, then 64 f32 scales
+constexpr int kProdWarps = 4;                           // warps 1-4: one TMA stream per warp
+constexpr int kEpiWarp0 = 1 + kProdWarps;               // warps 5-12
+constexpr int kEpiWarps = 8;
+constexpr int kEpiRows = kMaxGroupRows * 4 / kEpiWarps;  // group rows per epilogue warp
+static_assert(kStages % kProdWarps == 0, "a stage always belongs to the same producer");
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+constexpr int kDBufs = 4;
+constexpr int kDCols = kMaxGroupRows * kIdxHeads;       // 128 f32 columns per accumulator
+constexpr uint32_t kTmemCols = kDCols * kDBufs;
 
 // shared-memory map (offsets from a 1024-byte aligned base)
-constexpr int kOffA = 0;                                           // [kABufs] f16 key tiles
-constexpr int kOffB = kABufs * kABytes;                            // up to 128 x 128 f16 query
-constexpr int kOffW = kOffB + kABytes;                             // [4 warps][4 rows][32] f32
-constexpr int kOffLen = kOffW + 4 * kMaxGroupRows * kIdxHeads * 4;  // [4 warps][4 rows]
-constexpr int kRing = 8;                                           // scale ring slots
-static_assert(kRing >= kABufs + kDBufs, "a scale slot is reused only after its epilogue finished");
-constexpr int kOffScale = kOffLen + 4 * kMaxGroupRows * 4;          // [kRing][128] f32
-constexpr int kOffValid = kOffScale + kRing * kTileTok * 4;         // [kRing] page-valid bits
-constexpr int kOffStage = (kOffValid + kRing * 4 + 1023) / 1024 * 1024;  // [kStages] staging
-constexpr int kStageKeyBytes = kTileTok * kIdxDim;                 // E4M3 keys, then 128 f32
-constexpr int kStageBytes = kStageKeyBytes + kTileTok * 4 + 16;    // scales, then 2 page ids
-constexpr int kOffBar = kOffStage + kStages * kStageBytes;
-constexpr int kNumBars = 2 * kABufs + 2 * kDBufs + 2 + kRing + 2 * kStages;
+constexpr int kOffQ = 0;                                            // [kQBufs] query operands
+constexpr int kOffKeys = kOffQ + kQBufs * kQBytes;                  // [kStages] key tiles
+constexpr int kOffScale = kOffKeys + kStages * kKeyTileBytes;       // [kStages][128] f32
+constexpr int kOffPv = kOffScale + kStages * kTileTok * 4;          // [kStages] page-valid bits
+constexpr int kOffW = kOffPv + kStages * 4;                         // [kEpiWarps][kEpiRows][32] f32
+constexpr int kOffBar = kOffW + kEpiWarps * kEpiRows * kIdxHeads * 4;
+constexpr int kNumBars = 2 * kStages + 2 * kDBufs + 2 * kQBufs + 1;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffTmem + 16;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 
 // group = {first row, rows, request, max row length}
 struct ScanWs {
-  __half* qh;      // [R][32][128] f16 query, rescaled per (row, head)
-  float* weff;     // [R][32] head weight times the inverse rescale
+  uint8_t* q8;     // [2 terms][R][32 heads][128] E4M3 query terms
+  float* weff;     // [R][32] head weight times the inverse rescale (and query scale)
   int4* groups;    // [R]
   int* gstart;     // [R + 1] first tile of each group
   int* meta;       // {groups, tiles}
@@ -86,7 +89,7 @@ struct ScanWs {
 ScanWs scan_ws(uint8_t* base, int R) {
   ScanWs w;
   size_t o = 0;
-  w.qh = reinterpret_cast<__half*>(base + o);  o = align_up(o + (size_t)R * kIdxHeads * kIdxDim * 2);
+  w.q8 = base + o;                              o = align_up(o + (size_t)2 * R * kIdxHeads * kIdxDim);
   w.weff = reinterpret_cast<float*>(base + o); o = align_up(o + (size_t)R * kIdxHeads * 4);
   w.groups = reinterpret_cast<int4*>(base + o); o = align_up(o + (size_t)R * 16);
   w.gstart = reinterpret_cast<int*>(base + o);  o = align_up(o + (size_t)(R + 1) * 4);
@@ -96,8 +99,8 @@ ScanWs scan_ws(uint8_t* base, int R) {
 
 // ---------------------------------------------------------------------------
 // Prep, one launch of R + 1 CTAs of 1024 threads.
-//  * CTA r < R: warp h converts head h of row r's query to f16 (power-of-two
-//    rescale per head, folded into the head weight).
+//  * CTA r < R: warp h splits head h of row r's query into its two E4M3
+//    terms (power-of-two rescale per head, folded into the head weight).
 //  * CTA R: groups the rows.  A run is a maximal block of adjacent valid rows
 //    of one request; each run is cut into groups of up to 4 rows from its
 //    start.  Block-wide scans over chunks of 1024 rows give every row its run
@@ -193,43 +196,44 @@ scan_prep_kernel(const void* __restrict__ q_idx, int q_dtype, const float* __res
     }
     return;
   }
-  // query conversion: warp h handles head h of row r, lane l dims [4l, 4l + 4)
+  // query split: warp h handles head h of row r, lane l dims [4l, 4l + 4)
   const int r = blockIdx.x;
   const int h = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t off = ((size_t)r * kIdxHeads + h) * kIdxDim + lane * 4;
-  float x[4];
-  if (q_dtype == DSA_E4M3) {
-    const uint32_t v = *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(q_idx) + off);
-    const float2 a = e4m3x2_to_float2((uint16_t)(v & 0xFFFF));
-    const float2 b = e4m3x2_to_float2((uint16_t)(v >> 16));
-    x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y;       // |x| <= 448: exact in f16
+  uint8_t* hi_dst = ws.q8 + ((size_t)r * kIdxHeads + h) * kIdxDim + lane * 4;
+  uint8_t* lo_dst = hi_dst + (size_t)R * kIdxHeads * kIdxDim;
+  float wv = w[(size_t)r * kIdxHeads + h];
+  if (q_dtype == DSA_E4M3) {                        // already one E4M3 term
+    *reinterpret_cast<uint32_t*>(hi_dst) =
+        *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(q_idx) + off);
+    *reinterpret_cast<uint32_t*>(lo_dst) = 0u;
+    wv *= q_scale[(size_t)r * kIdxHeads + h];
   } else {
     const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(q_idx) + off);
+    float x[4];
     x[0] = __uint_as_float(v.x << 16);
     x[1] = __uint_as_float(v.x & 0xFFFF0000u);
     x[2] = __uint_as_float(v.y << 16);
     x[3] = __uint_as_float(v.y & 0xFFFF0000u);
-  }
-  float wv = w[(size_t)r * kIdxHeads + h];
-  if (q_dtype == DSA_E4M3) {
-    wv *= q_scale[(size_t)r * kIdxHeads + h];
-  } else {
     float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    if (amax > 0.f) {
-      const int e = ilogbf(amax);                 // amax in [2^e, 2^(e+1))
+    int a = 0;
+    if (amax > 0.f) a = 7 - ilogbf(amax);          // absmax into [128, 256)
+    uint32_t hw = 0, lw = 0;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) x[i] = ldexpf(x[i], 7 - e);   // absmax into [128, 256)
-      wv = ldexpf(wv, e - 7);
+    for (int i = 0; i < 4; ++i) {
+      const float sx = ldexpf(x[i], a);             // exact: a power of two
+      const uint8_t h8 = (uint8_t)__nv_cvt_float_to_fp8(sx, __NV_SATFINITE, __NV_E4M3);
+      const float rr = sx - e4m3_to_float(h8);      // exact: both on a common grid
+      const uint8_t l8 = (uint8_t)__nv_cvt_float_to_fp8(rr, __NV_SATFINITE, __NV_E4M3);
+      hw |= (uint32_t)h8 << (8 * i);
+      lw |= (uint32_t)l8 << (8 * i);
     }
+    *reinterpret_cast<uint32_t*>(hi_dst) = hw;
+    *reinterpret_cast<uint32_t*>(lo_dst) = lw;
+    wv = ldexpf(wv, -a);
   }
-  __half2 h01 = __floats2half2_rn(x[0], x[1]);
-  __half2 h23 = __floats2half2_rn(x[2], x[3]);
-  uint2 packed;
-  packed.x = *reinterpret_cast<uint32_t*>(&h01);
-  packed.y = *reinterpret_cast<uint32_t*>(&h23);
-  *reinterpret_cast<uint2*>(ws.qh + off) = packed;
   if (lane == 0) ws.weff[(size_t)r * kIdxHeads + h] = wv;
 }
 
@@ -257,6 +261,21 @@ struct TileCursor {
     load();
     t = tile - gs;
   }
+  // n tiles forward (crossing group boundaries; at most one load per group crossed)
+  __device__ void advance(int n) {
+    while (n > 0 && g < ngroups) {
+      const int left = (ge - gs) - t - 1;
+      if (n <= left) {
+        t += n;
+        return;
+      }
+      n -= left + 1;
+      ++g;
+      t = 0;
+      while (g < ngroups && gstart[g] == gstart[g + 1]) ++g;
+      if (g < ngroups) load();
+    }
+  }
   __device__ void next() {
     if (g >= ngroups) return;
     ++t;
@@ -276,72 +295,83 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// ---- cp.async (global -> shared) with mbarrier completion -----------------
-// A release-arrive on an mbarrier makes the arriving thread wait for its own
-// outstanding copies and loads.  So the threads that fetch keys (loaders) never
-// release-arrive: cp.async.mbarrier.arrive.noinc makes the barrier track the
-// completion of the loader's copies without the loader waiting, and the
-// converters, which release-arrive towards the MMA, have nothing in flight.
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
+// ---- TMA: tensor-map tile loads completing on an mbarrier -------------------
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
 }
 
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src)
-               : "memory");
-}
-
-// Arrive on `bar` once all cp.async copies issued so far by this thread landed.
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
 }
 
 __device__ __forceinline__ bool page_ok(int p, int64_t num_pages) { return p >= 0 && p < num_pages; }
 
-// 15 warps: one scheduler holds 4 of them, so 128 registers per thread is the cap.
+// Physical pages of a tile's two 64-token halves (-1: past the group's tokens).
+// Loads use clamped offsets so that no select waits on them.
+struct TilePages {
+  int p0, p1;
+  bool need0, need1;
+};
+
+__device__ __forceinline__ TilePages tile_pages(const TileCursor& c, const int32_t* block_table,
+                                                int max_pages) {
+  TilePages t;
+  const int lp0 = c.t * (kTileTok / kPage);
+  const int npg = (c.G.w + kPage - 1) / kPage;
+  t.need0 = lp0 < npg;
+  t.need1 = lp0 + 1 < npg;
+  const size_t base = (size_t)c.G.z * max_pages;
+  t.p0 = __ldg(block_table + base + (t.need0 ? lp0 : 0));
+  t.p1 = __ldg(block_table + base + (t.need1 ? lp0 + 1 : 0));
+  return t;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-scan_tc_kernel(const uint8_t* __restrict__ key_cache, int64_t num_pages,
-               const int32_t* __restrict__ block_table, int max_pages,
-               const int32_t* __restrict__ row_len, float* __restrict__ scores, int64_t ld,
-               ScanWs ws, uint32_t* status) {
+scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__ CUtensorMap q_map,
+            const uint8_t* __restrict__ key_cache, int64_t num_pages,
+            const int32_t* __restrict__ block_table, int max_pages,
+            const int32_t* __restrict__ row_len, float* __restrict__ scores, int64_t ld,
+            int n_rows, ScanWs ws, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* a_full = bars;                          // [kABufs]
-  uint64_t* a_empty = bars + kABufs;                // [kABufs]
-  uint64_t* d_full = bars + 2 * kABufs;             // [kDBufs]
+  uint64_t* full = bars;                            // [kStages] keys + scales landed
+  uint64_t* empty = bars + kStages;                 // [kStages] MMA and epilogue done with a stage
+  uint64_t* d_full = bars + 2 * kStages;            // [kDBufs]
   uint64_t* d_empty = d_full + kDBufs;              // [kDBufs]
-  uint64_t* b_full = d_full + 2 * kDBufs;
-  uint64_t* b_empty = b_full + 1;
-  uint64_t* sc_full = b_full + 2;                   // [kRing]
-  uint64_t* st_full = sc_full + kRing;              // [kStages]
-  uint64_t* st_empty = st_full + kStages;           // [kStages]
+  uint64_t* q_full = d_empty + kDBufs;              // [kQBufs]
+  uint64_t* q_empty = q_full + kQBufs;              // [kQBufs]
+  uint64_t* mma_done = q_empty + kQBufs;            // every issued MMA finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
-  float* w_s = reinterpret_cast<float*>(smem + kOffW);
-  int* len_s = reinterpret_cast<int*>(smem + kOffLen);
-  float* sc_ring = reinterpret_cast<float*>(smem + kOffScale);
-  uint32_t* valid_ring = reinterpret_cast<uint32_t*>(smem + kOffValid);
+  const float* scale_s = reinterpret_cast<const float*>(smem + kOffScale);
+  uint32_t* pv_s = reinterpret_cast<uint32_t*>(smem + kOffPv);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
-    for (int b = 0; b < kABufs; ++b) {
-      mbar_init(&a_full[b], kConvThreads / 32);
-      mbar_init(&a_empty[b], 1);
+    for (int x = 0; x < kStages; ++x) {
+      mbar_init(&full[x], 1);
+      mbar_init(&empty[x], 1 + kEpiWarps);          // the MMA commit and every epilogue warp
     }
     for (int b = 0; b < kDBufs; ++b) {
       mbar_init(&d_full[b], 1);
-      mbar_init(&d_empty[b], 4);
+      mbar_init(&d_empty[b], kEpiWarps);
     }
-    mbar_init(b_full, kConvThreads / 32);
-    mbar_init(b_empty, 1);
-    for (int x = 0; x < kRing; ++x) mbar_init(&sc_full[x], kConvThreads / 32);
-    for (int x = 0; x < kStages; ++x) {
-      mbar_init(&st_full[x], kLoadThreads);      // one cp.async-tracked arrival per loader
-      mbar_init(&st_empty[x], kConvThreads / 32);
+    for (int b = 0; b < kQBufs; ++b) {
+      mbar_init(&q_full[b], 1);
+      mbar_init(&q_empty[b], 1);
     }
+    mbar_init(mma_done, 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -368,217 +398,178 @@ scan_tc_kernel(const uint8_t* __restrict__ key_cache, int64_t num_pages,
     // ---------------- MMA issuer (lane 0 issues; the warp walks the same list)
     int cur_group = -1, gi = -1;
     uint32_t idesc = 0;
-    int nrows = 1;
     for (int i = 0; i < ntiles; ++i) {
       if (cur.g != cur_group) {
         cur_group = cur.g;
         ++gi;
-        nrows = cur.G.y;
-        idesc = idesc_f16_f32(kTileTok, 32 * nrows);
-        if (!warp_wait(b_full, (uint32_t)gi & 1, status)) break;
+        idesc = idesc_e4m3_f32(kTileTok, kIdxHeads * cur.G.y, false, false);
+        if (!warp_wait(&q_full[gi % kQBufs], (uint32_t)(gi / kQBufs) & 1, status)) break;
       }
-      const int ab = i % kABufs;
-      const int db = i % kDBufs;
-      if (!warp_wait(&a_full[ab], (uint32_t)(i / kABufs) & 1, status)) break;
+      const int s = i % kStages, db = i % kDBufs;
+      if (!warp_wait(&full[s], (uint32_t)(i / kStages) & 1, status)) break;
       if (!warp_wait(&d_empty[db], ((uint32_t)(i / kDBufs) & 1) ^ 1, status)) break;
       tc_fence_after();
       TileCursor nxt = cur;
       if (i + 1 < ntiles) nxt.next();
       if (lane == 0) {
-        const uint32_t a_addr = smem_u32(smem + kOffA + ab * kABytes);
-        const uint32_t b_addr = smem_u32(smem + kOffB);
-        const uint32_t b_atom = (uint32_t)(32 * nrows) * 128;
-        const uint32_t d_tmem = tmem_base + (uint32_t)db * 128;
+        const uint32_t a_addr = smem_u32(smem + kOffKeys + s * kKeyTileBytes);
+        const uint32_t b_addr = smem_u32(smem + kOffQ + (gi % kQBufs) * kQBytes);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(db * kDCols);
 #pragma unroll
-        for (int j = 0; j < kIdxDim / 16; ++j) {
-          const uint64_t ad = desc_kmajor_sw128(a_addr + (j >> 2) * kAtomBytes + (j & 3) * 32);
-          const uint64_t bd = desc_kmajor_sw128(b_addr + (j >> 2) * b_atom + (j & 3) * 32);
-          mma_f16_ss(d_tmem, ad, bd, idesc, j > 0 ? 1u : 0u);
-        }
-        mma_commit(&a_empty[ab]);
+        for (int j = 0; j < 2 * kIdxDim / 32; ++j)    // K = 2 x 128 bytes in steps of 32
+          mma_e4m3_ss(d_tmem, desc_kmajor_sw128(a_addr + (j & 3) * 32),
+                      desc_kmajor_sw128(b_addr + (j >> 2) * kQAtom + (j & 3) * 32), idesc,
+                      j > 0 ? 1u : 0u);
+        mma_commit(&empty[s]);
         mma_commit(&d_full[db]);
-        if (i + 1 == ntiles || nxt.g != cur.g) mma_commit(b_empty);
+        if (i + 1 == ntiles || nxt.g != cur.g) mma_commit(&q_empty[gi % kQBufs]);
       }
       __syncwarp();
       cur = nxt;
     }
-  } else if (ntiles > 0 && warp >= 1 && warp < 1 + kLoadWarps) {
-    // ---------------- loaders: keys, scales and page ids of tile i -> staging slot
-    // i % kStages with cp.async.  Lane j looks up the pages of tile i0 + j, so a
-    // batch of 32 tiles costs one block-table round trip.
-    const int lt = tid - 32;                         // 0 .. kLoadThreads-1
-    bool ok = true;
-    for (int i0 = 0; i0 < ntiles && ok; i0 += 32) {
-      int pg0 = -1, pg1 = -1, two = 0, bt_off = 0;
-      if (i0 + lane < ntiles) {
-        TileCursor c2 = cur;
-        c2.seek(t_begin + i0 + lane);
-        const int tok0 = c2.t * kTileTok;
-        bt_off = c2.G.z * max_pages + tok0 / kPage;
-        two = tok0 + kPage < c2.G.w;
-        pg0 = __ldg(block_table + bt_off);
-        if (two) pg1 = __ldg(block_table + bt_off + 1);
-      }
-      const int nb = min(32, ntiles - i0);
-      for (int j = 0; j < nb; ++j) {
-        const int i = i0 + j;
-        const int slot = i % kStages;
-        const int q0 = __shfl_sync(0xffffffffu, pg0, j);
-        const int q1 = __shfl_sync(0xffffffffu, pg1, j);
-        const int qtwo = __shfl_sync(0xffffffffu, two, j);
-        const int qoff = __shfl_sync(0xffffffffu, bt_off, j);
-        if (!warp_wait(&st_empty[slot], ((uint32_t)(i / kStages) & 1) ^ 1, status)) { ok = false; break; }
-        const bool v0 = page_ok(q0, num_pages);
-        const bool v1 = qtwo && page_ok(q1, num_pages);
-        if (lt == 0 && (!v0 || (qtwo && !v1))) raise_dev(status, DSA_DEV_BAD_PAGE);
-        uint8_t* stg = smem + kOffStage + slot * kStageBytes;
-#pragma unroll
-        for (int it = 0; it < kTileTok * 8 / kLoadThreads; ++it) {
-          const int id = it * kLoadThreads + lt;
-          const int r = id >> 3, c = id & 7;
-          const bool second = r >= kPage;
-          const int page = second ? q1 : q0;
-          if (second ? v1 : v0)
-            cp_async16(stg + r * kIdxDim + c * 16,
-                       key_cache + (size_t)page * kKeyPageBytes + (r & 63) * kIdxDim + c * 16);
-        }
-        float* ssc = reinterpret_cast<float*>(stg + kStageKeyBytes);
-#pragma unroll
-        for (int x = lt; x < kTileTok; x += kLoadThreads) {
-          const bool second = x >= kPage;
-          if (second ? v1 : v0)
-            cp_async4(ssc + x, key_cache + (size_t)(second ? q1 : q0) * kKeyPageBytes +
-                                   kKeyScaleOffset + (x & 63) * 4);
-        }
-        if (lt == 0) {
-          int* spid = reinterpret_cast<int*>(stg + kStageKeyBytes + kTileTok * 4);
-          cp_async4(spid, block_table + qoff);
-          if (qtwo) cp_async4(spid + 1, block_table + qoff + 1);
-        }
-        cp_async_arrive(&st_full[slot]);
-      }
+    if (lane == 0) {                                  // tensor memory is freed only after this
+      mma_commit(mma_done);
+      mbar_wait(mma_done, 0, status);
     }
-  } else if (ntiles > 0 && warp >= 1 + kLoadWarps && warp < kEpiWarp0) {
-    // ---------------- converters: staging slot -> f16 A tile (K-major, 128B swizzle)
-    // + the tile's scales and page-valid bits for the epilogue
-    const int ct = tid - 32 * (1 + kLoadWarps);
+    __syncwarp();
+  } else if (ntiles > 0 && warp >= 1 && warp <= kProdWarps) {
+    // ---------------- TMA producers: warp 1 + p loads the tiles i with
+    // i % kProdWarps == p.  Page ids are looked up a batch of 32 tiles ahead:
+    // lane j holds the pages of tile (batch start + j).
+    const int pw = warp - 1;
+    auto fetch = [&](const TileCursor& b0, int i0) {
+      TilePages tp{0, 0, false, false};
+      if (i0 + lane < ntiles) {
+        TileCursor cj = b0;
+        cj.advance(lane);
+        tp = tile_pages(cj, block_table, max_pages);
+      }
+      return tp;
+    };
+    TileCursor bc = cur;                              // start of the current batch
+    TilePages cb = fetch(bc, 0);
+    TileCursor bn = bc;
+    TilePages nb{0, 0, false, false};
+    if (ntiles > 32) {
+      bn.advance(32);
+      nb = fetch(bn, 32);
+    }
     int cur_group = -1, gi = -1;
-    for (int i = 0; i < ntiles; ++i) {
-      if (cur.g != cur_group) {
+    bool ok = true;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      const int j = i & 31;
+      if (j == 0 && i > 0) {                          // next batch; fetch the one after it
+        cb = nb;
+        bc = bn;
+        if (i + 32 < ntiles) {
+          bn.advance(32);
+          nb = fetch(bn, i + 32);
+        }
+      }
+      const int p0 = __shfl_sync(0xffffffffu, cb.p0, j);
+      const int p1 = __shfl_sync(0xffffffffu, cb.p1, j);
+      const bool need0 = __shfl_sync(0xffffffffu, cb.need0 ? 1 : 0, j) != 0;
+      const bool need1 = __shfl_sync(0xffffffffu, cb.need1 ? 1 : 0, j) != 0;
+      if (cur.g != cur_group) {                       // the group's query operand
         cur_group = cur.g;
         ++gi;
-        if (gi > 0 && !warp_wait(b_empty, (uint32_t)(gi - 1) & 1, status)) break;
-        const int N = 32 * cur.G.y;
-        const uint4* src =
-            reinterpret_cast<const uint4*>(ws.qh + (size_t)cur.G.x * kIdxHeads * kIdxDim);
-        uint8_t* bsm = smem + kOffB;
-        for (int id = ct; id < N * 16; id += kConvThreads) {
-          const int n = id >> 4, c = id & 15;
-          const uint4 v = src[id];
-          *reinterpret_cast<uint4*>(bsm + (c >> 3) * (N * 128) + n * 128 + (((c & 7) ^ (n & 7)) << 4)) = v;
+        if (i % kProdWarps != pw) {                   // loaded by the owner of this tile
+          cur.next();
+          continue;
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_full);
+        if (!warp_wait(&q_empty[gi % kQBufs], ((uint32_t)(gi / kQBufs) & 1) ^ 1, status)) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&q_full[gi % kQBufs], kQBytes);
+          uint8_t* qd = smem + kOffQ + (gi % kQBufs) * kQBytes;
+          tma_load_2d(qd, &q_map, 0, cur.G.x * kIdxHeads, &q_full[gi % kQBufs]);
+          tma_load_2d(qd + kQAtom, &q_map, 0, (n_rows + cur.G.x) * kIdxHeads, &q_full[gi % kQBufs]);
+        }
       }
-      const int slot = i % kStages;
-      const int ab = i % kABufs;
-      if (!warp_wait(&st_full[slot], (uint32_t)(i / kStages) & 1, status)) break;
-      if (!warp_wait(&a_empty[ab], ((uint32_t)(i / kABufs) & 1) ^ 1, status)) break;
-      const uint8_t* stg = smem + kOffStage + slot * kStageBytes;
-      const int* spid = reinterpret_cast<const int*>(stg + kStageKeyBytes + kTileTok * 4);
-      const bool two = cur.t * kTileTok + kPage < cur.G.w;
-      const uint32_t vb = (page_ok(spid[0], num_pages) ? 1u : 0u) |
-                          ((two && page_ok(spid[1], num_pages)) ? 2u : 0u);
-      // scales: ring slot i % kRing is free: the MMA of tile i - kABufs has
-      // completed (a_empty above), and it had waited for the epilogue of tile
-      // i - kABufs - kDBufs to drain, which is at least kRing tiles back.
-      const int rs = i % kRing;
-      if (ct < kTileTok)
-        sc_ring[rs * kTileTok + ct] =
-            ((vb >> (ct >> 6)) & 1u) ? reinterpret_cast<const float*>(stg + kStageKeyBytes)[ct] : 0.f;
-      if (ct == 0) valid_ring[rs] = vb;
+      if (i % kProdWarps != pw) {
+        cur.next();
+        continue;
+      }
+      const int s = i % kStages;
+      if (!warp_wait(&empty[s], ((uint32_t)(i / kStages) & 1) ^ 1, status)) break;
+      if (lane == 0) {
+        const bool v0 = need0 && page_ok(p0, num_pages);
+        const bool v1 = need1 && page_ok(p1, num_pages);
+        if ((need0 && !v0) || (need1 && !v1)) raise_dev(status, DSA_DEV_BAD_PAGE);
+        pv_s[s] = (v0 ? 1u : 0u) | (v1 ? 2u : 0u);
+        uint8_t* kd = smem + kOffKeys + s * kKeyTileBytes;
+        uint8_t* sd = smem + kOffScale + s * kTileTok * 4;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)((v0 ? 1 : 0) + (v1 ? 1 : 0)) *
+                                            (uint32_t)(kPageKeyBytes + kPage * 4));
+        if (v0) {
+          tma_load_3d(kd, &key_map, 0, 0, p0, &full[s]);
+          bulk_g2s(sd, key_cache + (size_t)p0 * kPageBytes + kPageKeyBytes, kPage * 4, &full[s]);
+        }
+        if (v1) {
+          tma_load_3d(kd + kPageKeyBytes, &key_map, 0, 0, p1, &full[s]);
+          bulk_g2s(sd + kPage * 4, key_cache + (size_t)p1 * kPageBytes + kPageKeyBytes,
+                   kPage * 4, &full[s]);
+        }
+      }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sc_full[rs]);
-      uint8_t* a = smem + kOffA + ab * kABytes;
-#pragma unroll
-      for (int it = 0; it < kChunks; ++it) {
-        const int r = it * (kConvThreads / 8) + (ct >> 3), c = ct & 7;
-        const uint4 raw = *reinterpret_cast<const uint4*>(stg + r * kIdxDim + c * 16);
-        uint4 lo, hi;
-        cvt_e4m3x4_f16x4(raw.x, lo.x, lo.y);
-        cvt_e4m3x4_f16x4(raw.y, lo.z, lo.w);
-        cvt_e4m3x4_f16x4(raw.z, hi.x, hi.y);
-        cvt_e4m3x4_f16x4(raw.w, hi.z, hi.w);
-        uint8_t* row = a + (c >> 2) * kAtomBytes + r * 128;
-        const int j0 = 2 * (c & 3);
-        uint4* plo = reinterpret_cast<uint4*>(row + ((j0 ^ (r & 7)) << 4));
-        uint4* phi = reinterpret_cast<uint4*>(row + (((j0 + 1) ^ (r & 7)) << 4));
-        if (c < 4) { *plo = lo; *phi = hi; } else { *phi = hi; *plo = lo; }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();                                // the warp's writes are ordered before
-      if (lane == 0) {                             // lane 0's release-arrivals
-        mbar_arrive(&a_full[ab]);
-        mbar_arrive(&st_empty[slot]);
-      }
       cur.next();
     }
+    // no copy may still be landing in shared memory when the CTA exits
+    for (int i = ntiles > kStages ? ntiles - kStages : 0; i < ntiles; ++i)
+      if (i % kProdWarps == pw) warp_wait(&full[i % kStages], (uint32_t)(i / kStages) & 1, status);
   } else if (ntiles > 0 && warp >= kEpiWarp0) {
-    // ---------------- epilogue: TMEM -> ReLU-weighted head sum -> scores
-    const int quarter = warp & 3;                 // TMEM lanes this warp may read
-    float* wq = w_s + (warp - kEpiWarp0) * kMaxGroupRows * kIdxHeads;   // this warp's copy
-    int* lq = len_s + (warp - kEpiWarp0) * kMaxGroupRows;
+    // ---------------- epilogue: token (32 x quarter + lane) of the tile, rows
+    // kEpiRows * ((w - kEpiWarp0) / 4) + [0, kEpiRows) of the group
+    const int quarter = warp & 3;
+    const int r0 = ((warp - kEpiWarp0) >> 2) * kEpiRows;
+    const int tok_in = quarter * 32 + lane;
+    float* w_s = reinterpret_cast<float*>(smem + kOffW) + (warp - kEpiWarp0) * kEpiRows * kIdxHeads;
     int cur_group = -1;
+    int len[kEpiRows];
     for (int i = 0; i < ntiles; ++i) {
-      const int4 G = cur.G;
-      if (cur.g != cur_group) {
+      const int s = i % kStages, db = i % kDBufs;
+      if (cur.g != cur_group) {                       // this warp's rows of the new group
         cur_group = cur.g;
-        __syncwarp();
-        for (int x = lane; x < G.y * kIdxHeads; x += 32) wq[x] = ws.weff[(size_t)G.x * kIdxHeads + x];
-        if (lane < G.y) lq[lane] = row_len[G.x + lane];
+#pragma unroll
+        for (int rr = 0; rr < kEpiRows; ++rr) {
+          const bool has = r0 + rr < cur.G.y;
+          len[rr] = has ? row_len[cur.G.x + r0 + rr] : 0;
+          w_s[rr * kIdxHeads + lane] = has ? ws.weff[(size_t)(cur.G.x + r0 + rr) * kIdxHeads + lane] : 0.f;
+        }
         __syncwarp();
       }
-      const int b = i % kDBufs;
-      const int slot = i % kRing;
-      if (!warp_wait(&sc_full[slot], (uint32_t)(i / kRing) & 1, status)) break;
-      if (!warp_wait(&d_full[b], (uint32_t)(i / kDBufs) & 1, status)) break;
+      if (!warp_wait(&d_full[db], (uint32_t)(i / kDBufs) & 1, status)) break;
+      if (!warp_wait(&full[s], (uint32_t)(i / kStages) & 1, status)) break;   // scales landed
       tc_fence_after();
-      const int tt = quarter * 32 + lane;             // token within the tile
-      const int tok = cur.t * kTileTok + tt;
-      const float ks = sc_ring[slot * kTileTok + tt];
-      const bool valid = tok < G.w && ((valid_ring[slot] >> (tt >> 6)) & 1u);
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)b * 128;
+      const bool page_valid = (pv_s[s] >> (tok_in >> 6)) & 1u;
+      const float ks = scale_s[s * kTileTok + tok_in];
+      const int tok = cur.t * kTileTok + tok_in;
 #pragma unroll
-      for (int p = 0; p < kMaxGroupRows; p += 2) {
-        if (p < G.y) {
-          uint32_t d[2][32];
-          tmem_ld_32x32b_x32(taddr + (uint32_t)p * 32, d[0]);
-          if (p + 1 < G.y) tmem_ld_32x32b_x32(taddr + (uint32_t)(p + 1) * 32, d[1]);
+      for (int rr = 0; rr < kEpiRows; ++rr) {
+        const int r = r0 + rr;
+        if (r < cur.G.y) {
+          uint32_t xv[32];
+          const uint32_t ta = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                              (uint32_t)(db * kDCols + r * kIdxHeads);
+          tmem_ld_32x32b_x32(ta, xv);
           tmem_wait_ld();
-          if (p + 2 >= G.y) {                       // accumulator drained into registers
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&d_empty[b]);
-          }
+          const float4* wr = reinterpret_cast<const float4*>(w_s + rr * kIdxHeads);
+          float acc = 0.f;
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            const int nr = p + q;
-            if (nr < G.y) {
-              const float4* wr = reinterpret_cast<const float4*>(wq + nr * kIdxHeads);
-              float acc = 0.f;
+          for (int h4 = 0; h4 < kIdxHeads / 4; ++h4) {
+            const float4 wv = wr[h4];
+            const float w4[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-              for (int h4 = 0; h4 < 8; ++h4) {
-                const float4 wv = wr[h4];
-                acc = fmaf(wv.x, fmaxf(__uint_as_float(d[q][4 * h4 + 0]), 0.f), acc);
-                acc = fmaf(wv.y, fmaxf(__uint_as_float(d[q][4 * h4 + 1]), 0.f), acc);
-                acc = fmaf(wv.z, fmaxf(__uint_as_float(d[q][4 * h4 + 2]), 0.f), acc);
-                acc = fmaf(wv.w, fmaxf(__uint_as_float(d[q][4 * h4 + 3]), 0.f), acc);
-              }
-              if (valid && tok < lq[nr]) scores[(size_t)(G.x + nr) * ld + tok] = acc * ks;
-            }
+            for (int u = 0; u < 4; ++u)
+              acc = fmaf(w4[u], fmaxf(__uint_as_float(xv[4 * h4 + u]), 0.f), acc);
           }
+          if (page_valid && tok < len[rr]) scores[(size_t)(cur.G.x + r) * ld + tok] = acc * ks;
         }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&d_empty[db]);
+        mbar_arrive(&empty[s]);
       }
       cur.next();
     }
@@ -596,14 +587,14 @@ scan_tc_kernel(const uint8_t* __restrict__ key_cache, int64_t num_pages,
 }  // namespace
 
 size_t scan_scratch_bytes(int R) {
-  return align_up((size_t)R * kIdxHeads * kIdxDim * 2) + align_up((size_t)R * kIdxHeads * 4) +
+  return align_up((size_t)2 * R * kIdxHeads * kIdxDim) + align_up((size_t)R * kIdxHeads * 4) +
          align_up((size_t)R * 16) + align_up((size_t)(R + 1) * 4) + align_up(16);
 }
 
 cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st) {
   if (a.R == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  cudaError_t e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemAlloc);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   e = cudaGetDevice(&dev);
@@ -611,11 +602,27 @@ cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st) {
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   ScanWs ws = scan_ws(a.scratch, a.R);
+  // keys: [page][64 tokens][128 B] inside pages of 8448 bytes; a box is one
+  // page's key block.  Queries: [2 terms x R x 32 rows][128 B]; a box is 128
+  // rows (one term of a group of up to 4 rows; rows past the group are never
+  // multiplied).
+  alignas(64) CUtensorMap kmap, qmap;
+  const uint64_t kdims[3] = {(uint64_t)kIdxDim, (uint64_t)kPage,
+                             (uint64_t)(a.num_pages > 0 ? a.num_pages : 1)};
+  const uint64_t kstr[2] = {(uint64_t)kIdxDim, (uint64_t)kPageBytes};
+  const uint32_t kbox[3] = {(uint32_t)kIdxDim, (uint32_t)kPage, 1};
+  e = encode_tensor_map_u8(&kmap, 3, a.key_cache, kdims, kstr, kbox);
+  if (e != cudaSuccess) return e;
+  const uint64_t qdims[2] = {(uint64_t)kIdxDim, (uint64_t)2 * a.R * kIdxHeads};
+  const uint64_t qstr[1] = {(uint64_t)kIdxDim};
+  const uint32_t qbox[2] = {(uint32_t)kIdxDim, (uint32_t)(kMaxGroupRows * kIdxHeads)};
+  e = encode_tensor_map_u8(&qmap, 2, ws.q8, qdims, qstr, qbox);
+  if (e != cudaSuccess) return e;
   scan_prep_kernel<<<a.R + 1, kPrepThreads, 0, st>>>(a.q_idx, a.q_dtype, a.q_scale, a.w, a.row_req,
                                              a.row_len, a.R, a.B, a.max_pages, ws, a.status);
-  scan_tc_kernel<<<sms, kThreads, kSmemAlloc, st>>>(a.key_cache, a.num_pages, a.block_table,
-                                                     a.max_pages, a.row_len, a.scores, a.ld, ws,
-                                                     a.status);
+  scan_kernel<<<sms, kThreads, kSmemAlloc, st>>>(kmap, qmap, a.key_cache, a.num_pages,
+                                                 a.block_table, a.max_pages, a.row_len, a.scores,
+                                                 a.ld, a.R, ws, a.status);
   return cudaGetLastError();
 }
 

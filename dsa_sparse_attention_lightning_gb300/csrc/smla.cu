@@ -44,11 +44,8 @@
 //     tile read as an MN-major operand, so V is never copied.
 // Accumulators (S and O^T) live in tensor memory; an MMA warp pipelines S of
 // tile i + 1 against the softmax and P.V of tile i through mbarriers.
-#include <cuda.h>
-#include <cudaTypedefs.h>
+#include <limits.h>
 #include <math.h>
-
-#include <mutex>
 
 #include "dsa_common.cuh"
 #include "sm100_ptx.cuh"
@@ -707,38 +704,17 @@ mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ p
   if (lse && threadIdx.x == 0) lse[(size_t)r * H + h] = Z > 0.f ? M + logf(Z) : -INFINITY;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // The latent cache as a 2-D tensor of 576-byte rows (one per token slot); a box
 // is 128 bytes of one row, stored with the 128-byte swizzle.
 cudaError_t latent_tensor_map(CUtensorMap* map, const uint8_t* cache, int64_t num_pages) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return cudaErrorNotSupported;
   // Row coordinates are signed 32-bit.  With no pages every lookup is rejected
   // before a coordinate is formed, so a one-page map is never dereferenced.
   if (num_pages * kPage > INT32_MAX) return cudaErrorInvalidValue;
   const int64_t rows = (num_pages > 0 ? num_pages : 1) * kPage;
-  const cuuint64_t dims[2] = {(cuuint64_t)kLatDim, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)kLatDim};
-  const cuuint32_t box[2] = {128, 1};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(cache), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  const uint64_t dims[2] = {(uint64_t)kLatDim, (uint64_t)rows};
+  const uint64_t strides[1] = {(uint64_t)kLatDim};
+  const uint32_t box[2] = {128, 1};
+  return encode_tensor_map_u8(map, 2, cache, dims, strides, box);
 }
 
 template <int HG>
