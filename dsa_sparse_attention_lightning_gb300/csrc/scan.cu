@@ -31,10 +31,13 @@
 //  * Persistent CTAs, one per SM, each taking a contiguous run of (group,
 //    tile) work items; warp roles: 0 MMA issuer and TMEM owner, 1-4 TMA
 //    producers (keys, key scales, group queries; page ids looked up 32 tiles
-//    ahead; tile i is loaded by producer i % 4 -- TMA loads issued from one
-//    thread complete at about half the HBM rate, so each SM runs several
-//    streams), 5-12 epilogue (TMEM -> scores; warp w takes TMEM lane
-//    quarter w % 4, i.e. 32 tokens, of two of the group's rows).
+//    ahead; tile i is loaded by producer i % 2 -- TMA loads issued from one
+//    thread complete at about half the HBM rate, so each SM runs two
+//    streams), 3-18 epilogue in two groups of eight that take alternate
+//    tiles (TMEM -> scores; a warp takes TMEM lane quarter w % 4, i.e. 32
+//    tokens, of two of the group's rows).  A key stage is released by the
+//    MMA's completion alone; the key scales live in their own ring, held
+//    until the epilogue has used them.
 #include <limits.h>
 #include <math.h>
 
@@ -50,29 +53,36 @@ constexpr int kTileTok = 128;
 constexpr int kMaxGroupRows = 4;
 constexpr int kQAtom = kMaxGroupRows * kIdxHeads * kIdxDim;  // 128 rows x 128 B: one query term
 constexpr int kQBytes = 2 * kQAtom;                     // one group's query operand (hi, lo)
-constexpr int kQBufs = 2;
-constexpr int kStages = 8;                              // key tiles in flight per SM
+constexpr int kQBufs = 1;
+constexpr int kStages = 10;                             // key tiles in flight per SM
 constexpr int kKeyTileBytes = kTileTok * kIdxDim;       // 2 pages x 64 x 128 B
 constexpr int kPageKeyBytes = kPage * kIdxDim;          // 8192
 constexpr int kPageBytes = kPage * (kIdxDim + 4);       // 8448: keys, then 64 f32 scales
-constexpr int kProdWarps = 4;                           // warps 1-4: one TMA stream per warp
-constexpr int kEpiWarp0 = 1 + kProdWarps;               // warps 5-12
-constexpr int kEpiWarps = 8;
-constexpr int kEpiRows = kMaxGroupRows * 4 / kEpiWarps;  // group rows per epilogue warp
+constexpr int kScRing = 16;                             // key-scale slots (outlive their key stage)
+constexpr int kProdWarps = 2;                           // warps 1-2: one TMA stream per warp
+constexpr int kEpiWarp0 = 1 + kProdWarps;               // warps 3-18
+constexpr int kEpiGroups = 2;                           // epilogue group g takes tiles i % 2 == g
+constexpr int kEpiWarpsPerGroup = 8;
+constexpr int kEpiWarps = kEpiGroups * kEpiWarpsPerGroup;
+constexpr int kEpiRows = kMaxGroupRows * 4 / kEpiWarpsPerGroup;  // group rows per epilogue warp
 static_assert(kStages % kProdWarps == 0, "a stage always belongs to the same producer");
+static_assert(kScRing % kProdWarps == 0 && kScRing % kEpiGroups == 0, "fixed slot owners");
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
 constexpr int kDBufs = 4;
+static_assert(kDBufs % kEpiGroups == 0, "a TMEM accumulator always belongs to the same group");
 constexpr int kDCols = kMaxGroupRows * kIdxHeads;       // 128 f32 columns per accumulator
 constexpr uint32_t kTmemCols = kDCols * kDBufs;
 
 // shared-memory map (offsets from a 1024-byte aligned base)
 constexpr int kOffQ = 0;                                            // [kQBufs] query operands
 constexpr int kOffKeys = kOffQ + kQBufs * kQBytes;                  // [kStages] key tiles
-constexpr int kOffScale = kOffKeys + kStages * kKeyTileBytes;       // [kStages][128] f32
-constexpr int kOffPv = kOffScale + kStages * kTileTok * 4;          // [kStages] page-valid bits
-constexpr int kOffW = kOffPv + kStages * 4;                         // [kEpiWarps][kEpiRows][32] f32
-constexpr int kOffBar = kOffW + kEpiWarps * kEpiRows * kIdxHeads * 4;
-constexpr int kNumBars = 2 * kStages + 2 * kDBufs + 2 * kQBufs + 1;
+constexpr int kOffScale = kOffKeys + kStages * kKeyTileBytes;       // [kScRing][128] f32
+constexpr int kOffPv = kOffScale + kScRing * kTileTok * 4;          // [kScRing] page-valid bits
+constexpr int kOffW = (kOffPv + kScRing * 4 + 15) / 16 * 16;       // [kEpiWarps][kEpiRows][32] f32
+constexpr int kOffBar = (kOffW + kEpiWarps * kEpiRows * kIdxHeads * 4 + 7) / 8 * 8;
+static_assert(kOffKeys % 1024 == 0 && kKeyTileBytes % 1024 == 0, "swizzled TMA tiles need 1024-byte alignment");
+static_assert(kOffScale % 16 == 0 && kOffW % 16 == 0 && kOffBar % 8 == 0, "vector and mbarrier alignment");
+constexpr int kNumBars = 2 * kStages + 2 * kScRing + 2 * kDBufs + 2 * kQBufs + 1;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffTmem + 16;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
@@ -346,9 +356,11 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* full = bars;                            // [kStages] keys + scales landed
-  uint64_t* empty = bars + kStages;                 // [kStages] MMA and epilogue done with a stage
-  uint64_t* d_full = bars + 2 * kStages;            // [kDBufs]
+  uint64_t* full = bars;                            // [kStages] keys landed
+  uint64_t* empty = bars + kStages;                 // [kStages] MMA done with a key stage
+  uint64_t* sc_full = bars + 2 * kStages;           // [kScRing] scales landed
+  uint64_t* sc_empty = sc_full + kScRing;           // [kScRing] epilogue done with them
+  uint64_t* d_full = sc_empty + kScRing;            // [kDBufs]
   uint64_t* d_empty = d_full + kDBufs;              // [kDBufs]
   uint64_t* q_full = d_empty + kDBufs;              // [kQBufs]
   uint64_t* q_empty = q_full + kQBufs;              // [kQBufs]
@@ -361,11 +373,15 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
   if (tid == 0) {
     for (int x = 0; x < kStages; ++x) {
       mbar_init(&full[x], 1);
-      mbar_init(&empty[x], 1 + kEpiWarps);          // the MMA commit and every epilogue warp
+      mbar_init(&empty[x], 1);                      // the MMA commit
+    }
+    for (int x = 0; x < kScRing; ++x) {
+      mbar_init(&sc_full[x], 1);
+      mbar_init(&sc_empty[x], kEpiWarpsPerGroup);
     }
     for (int b = 0; b < kDBufs; ++b) {
       mbar_init(&d_full[b], 1);
-      mbar_init(&d_empty[b], kEpiWarps);
+      mbar_init(&d_empty[b], kEpiWarpsPerGroup);
     }
     for (int b = 0; b < kQBufs; ++b) {
       mbar_init(&q_full[b], 1);
@@ -395,40 +411,46 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
   if (ntiles > 0) cur.seek(t_begin);
 
   if (ntiles > 0 && warp == 0) {
-    // ---------------- MMA issuer (lane 0 issues; the warp walks the same list)
-    int cur_group = -1, gi = -1;
-    uint32_t idesc = 0;
-    for (int i = 0; i < ntiles; ++i) {
-      if (cur.g != cur_group) {
-        cur_group = cur.g;
-        ++gi;
-        idesc = idesc_e4m3_f32(kTileTok, kIdxHeads * cur.G.y, false, false);
-        if (!warp_wait(&q_full[gi % kQBufs], (uint32_t)(gi / kQBufs) & 1, status)) break;
-      }
-      const int s = i % kStages, db = i % kDBufs;
-      if (!warp_wait(&full[s], (uint32_t)(i / kStages) & 1, status)) break;
-      if (!warp_wait(&d_empty[db], ((uint32_t)(i / kDBufs) & 1) ^ 1, status)) break;
-      tc_fence_after();
-      TileCursor nxt = cur;
-      if (i + 1 < ntiles) nxt.next();
-      if (lane == 0) {
-        const uint32_t a_addr = smem_u32(smem + kOffKeys + s * kKeyTileBytes);
-        const uint32_t b_addr = smem_u32(smem + kOffQ + (gi % kQBufs) * kQBytes);
+    // ---------------- MMA issuer: lane 0 alone walks the tiles and issues
+    if (lane == 0) {
+      int cur_group = -1, gi = -1, left = 0;          // tiles left in the current group
+      uint32_t idesc = 0;
+      uint64_t b_desc = 0;
+      const uint64_t a_desc_base = desc_kmajor_sw128(smem_u32(smem + kOffKeys));
+      int s = 0;                                      // key stage of tile i
+      uint32_t s_phase = 0;
+      bool ok = true;
+      for (int i = 0; i < ntiles && ok; ++i) {
+        if (cur.g != cur_group) {
+          cur_group = cur.g;
+          ++gi;
+          left = (cur.ge - cur.gs) - cur.t;
+          idesc = idesc_e4m3_f32(kTileTok, kIdxHeads * cur.G.y, false, false);
+          b_desc = desc_kmajor_sw128(smem_u32(smem + kOffQ + (gi % kQBufs) * kQBytes));
+          if (!mbar_wait(&q_full[gi % kQBufs], (uint32_t)(gi / kQBufs) & 1, status)) break;
+        }
+        const int db = i % kDBufs;
+        if (!mbar_wait(&full[s], s_phase, status)) break;
+        if (!mbar_wait(&d_empty[db], ((uint32_t)(i / kDBufs) & 1) ^ 1, status)) break;
+        tc_fence_after();
+        const uint64_t a_desc = a_desc_base + (uint64_t)((s * kKeyTileBytes) >> 4);
         const uint32_t d_tmem = tmem_base + (uint32_t)(db * kDCols);
 #pragma unroll
         for (int j = 0; j < 2 * kIdxDim / 32; ++j)    // K = 2 x 128 bytes in steps of 32
-          mma_e4m3_ss(d_tmem, desc_kmajor_sw128(a_addr + (j & 3) * 32),
-                      desc_kmajor_sw128(b_addr + (j >> 2) * kQAtom + (j & 3) * 32), idesc,
+          mma_e4m3_ss(d_tmem, a_desc + (uint64_t)((j & 3) * 2),
+                      b_desc + (uint64_t)(((j >> 2) * kQAtom + (j & 3) * 32) >> 4), idesc,
                       j > 0 ? 1u : 0u);
         mma_commit(&empty[s]);
         mma_commit(&d_full[db]);
-        if (i + 1 == ntiles || nxt.g != cur.g) mma_commit(&q_empty[gi % kQBufs]);
+        --left;
+        if (i + 1 == ntiles || left == 0) mma_commit(&q_empty[gi % kQBufs]);
+        if (++s == kStages) {
+          s = 0;
+          s_phase ^= 1u;
+        }
+        if (left == 0 && i + 1 < ntiles) cur.advance(cur.ge - cur.gs - cur.t);   // next group
       }
-      __syncwarp();
-      cur = nxt;
-    }
-    if (lane == 0) {                                  // tensor memory is freed only after this
-      mma_commit(mma_done);
+      mma_commit(mma_done);                           // tensor memory is freed only after this
       mbar_wait(mma_done, 0, status);
     }
     __syncwarp();
@@ -489,25 +511,27 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
         cur.next();
         continue;
       }
-      const int s = i % kStages;
+      const int s = i % kStages, x = i % kScRing;
       if (!warp_wait(&empty[s], ((uint32_t)(i / kStages) & 1) ^ 1, status)) break;
+      if (!warp_wait(&sc_empty[x], ((uint32_t)(i / kScRing) & 1) ^ 1, status)) break;
       if (lane == 0) {
         const bool v0 = need0 && page_ok(p0, num_pages);
         const bool v1 = need1 && page_ok(p1, num_pages);
         if ((need0 && !v0) || (need1 && !v1)) raise_dev(status, DSA_DEV_BAD_PAGE);
-        pv_s[s] = (v0 ? 1u : 0u) | (v1 ? 2u : 0u);
+        pv_s[x] = (v0 ? 1u : 0u) | (v1 ? 2u : 0u);
         uint8_t* kd = smem + kOffKeys + s * kKeyTileBytes;
-        uint8_t* sd = smem + kOffScale + s * kTileTok * 4;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)((v0 ? 1 : 0) + (v1 ? 1 : 0)) *
-                                            (uint32_t)(kPageKeyBytes + kPage * 4));
+        uint8_t* sd = smem + kOffScale + x * kTileTok * 4;
+        const uint32_t nv = (v0 ? 1u : 0u) + (v1 ? 1u : 0u);
+        mbar_arrive_expect_tx(&full[s], nv * kPageKeyBytes);
+        mbar_arrive_expect_tx(&sc_full[x], nv * kPage * 4);
         if (v0) {
           tma_load_3d(kd, &key_map, 0, 0, p0, &full[s]);
-          bulk_g2s(sd, key_cache + (size_t)p0 * kPageBytes + kPageKeyBytes, kPage * 4, &full[s]);
+          bulk_g2s(sd, key_cache + (size_t)p0 * kPageBytes + kPageKeyBytes, kPage * 4, &sc_full[x]);
         }
         if (v1) {
           tma_load_3d(kd + kPageKeyBytes, &key_map, 0, 0, p1, &full[s]);
           bulk_g2s(sd + kPage * 4, key_cache + (size_t)p1 * kPageBytes + kPageKeyBytes,
-                   kPage * 4, &full[s]);
+                   kPage * 4, &sc_full[x]);
         }
       }
       __syncwarp();
@@ -516,17 +540,23 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
     // no copy may still be landing in shared memory when the CTA exits
     for (int i = ntiles > kStages ? ntiles - kStages : 0; i < ntiles; ++i)
       if (i % kProdWarps == pw) warp_wait(&full[i % kStages], (uint32_t)(i / kStages) & 1, status);
+    for (int i = ntiles > kScRing ? ntiles - kScRing : 0; i < ntiles; ++i)
+      if (i % kProdWarps == pw) warp_wait(&sc_full[i % kScRing], (uint32_t)(i / kScRing) & 1, status);
   } else if (ntiles > 0 && warp >= kEpiWarp0) {
-    // ---------------- epilogue: token (32 x quarter + lane) of the tile, rows
-    // kEpiRows * ((w - kEpiWarp0) / 4) + [0, kEpiRows) of the group
+    // ---------------- epilogue: group eg takes the tiles i % 2 == eg; in it,
+    // warp e takes token (32 x quarter + lane) of the tile and rows
+    // kEpiRows * (e / 4) + [0, kEpiRows) of the group
+    const int eg = (warp - kEpiWarp0) / kEpiWarpsPerGroup;
+    const int e = (warp - kEpiWarp0) % kEpiWarpsPerGroup;
     const int quarter = warp & 3;
-    const int r0 = ((warp - kEpiWarp0) >> 2) * kEpiRows;
+    const int r0 = (e >> 2) * kEpiRows;
     const int tok_in = quarter * 32 + lane;
     float* w_s = reinterpret_cast<float*>(smem + kOffW) + (warp - kEpiWarp0) * kEpiRows * kIdxHeads;
     int cur_group = -1;
     int len[kEpiRows];
-    for (int i = 0; i < ntiles; ++i) {
-      const int s = i % kStages, db = i % kDBufs;
+    if (eg > 0) cur.advance(eg);
+    for (int i = eg; i < ntiles; i += kEpiGroups) {
+      const int x = i % kScRing, db = i % kDBufs;
       if (cur.g != cur_group) {                       // this warp's rows of the new group
         cur_group = cur.g;
 #pragma unroll
@@ -538,10 +568,10 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
         __syncwarp();
       }
       if (!warp_wait(&d_full[db], (uint32_t)(i / kDBufs) & 1, status)) break;
-      if (!warp_wait(&full[s], (uint32_t)(i / kStages) & 1, status)) break;   // scales landed
+      if (!warp_wait(&sc_full[x], (uint32_t)(i / kScRing) & 1, status)) break;
       tc_fence_after();
-      const bool page_valid = (pv_s[s] >> (tok_in >> 6)) & 1u;
-      const float ks = scale_s[s * kTileTok + tok_in];
+      const bool page_valid = (pv_s[x] >> (tok_in >> 6)) & 1u;
+      const float ks = scale_s[x * kTileTok + tok_in];
       const int tok = cur.t * kTileTok + tok_in;
 #pragma unroll
       for (int rr = 0; rr < kEpiRows; ++rr) {
@@ -569,9 +599,9 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&d_empty[db]);
-        mbar_arrive(&empty[s]);
+        mbar_arrive(&sc_empty[x]);
       }
-      cur.next();
+      cur.advance(kEpiGroups);
     }
   }
 
