@@ -35,7 +35,9 @@ from dsa_sparse_attention_lightning_gb300 import inputs, traffic  # noqa: E402
 
 METRIC = "DSA decode-step µs/layer and achieved HBM GB/s vs 8 TB/s roofline, 1 GB300"
 L2_FLUSH_BYTES = 256 << 20
-KERNELS_PER_STEP = 6   # scan 1, top-k 3 (hist, collect, finalize), MLA 2 (split, combine)
+# scan 2 (query split + grouping, scan), top-k 3 (histogram, collect, finalize),
+# sparse MLA 3 (query split, attention, combine of cut units)
+KERNELS_PER_STEP = 8
 
 
 def _peaks():
@@ -292,7 +294,8 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "us_per_layer_step": round(ms_per_step * 1e3, 2),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32 (tensor cores), f32 softmax and selection",
         "data": "synthetic",
         "config": {"workload": wl.name, "requests": wl.B, "rows": R, "context": wl.ctx[0],
                    "heads": H, "topk": wl.k, "algorithmic_bytes_per_step": bytes_step,
