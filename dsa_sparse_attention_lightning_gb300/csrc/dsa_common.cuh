@@ -33,18 +33,22 @@ constexpr int kTopkBins3 = 1024;               // third digit: bits 9..0
 
 inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a; }
 
-// Byte offsets of the top-k scratch inside a workspace region.
+// Byte offsets of the top-k scratch inside a workspace region: per row a
+// candidate threshold, a candidate count (zeroed by a memset before every
+// selection), where each 4096-score chunk put its candidates, and room for
+// kTopkCandCap (key, position) candidates.
+constexpr int kTopkCandCap = 8192;
 struct TopkLayout {
-  size_t hist, thr, seg_count, items, bytes;
+  size_t tau, cnt, runs, items, bytes;
   int nchunks;
   TopkLayout(int R, int64_t max_len) {
     nchunks = (int)((max_len + kTopkChunk - 1) / kTopkChunk);
     if (nchunks < 1) nchunks = 1;
     size_t o = 0;
-    hist = o;      o = align_up(o + (size_t)R * kTopkBins1 * 4);
-    thr = o;       o = align_up(o + (size_t)R * 8);
-    seg_count = o; o = align_up(o + (size_t)R * nchunks * 4);
-    items = o;     o = align_up(o + (size_t)R * nchunks * kTopkChunk * 8);
+    tau = o;       o = align_up(o + (size_t)R * 4);
+    cnt = o;       o = align_up(o + (size_t)R * 4);
+    runs = o;      o = align_up(o + (size_t)R * nchunks * 8);     // per chunk: (offset, count)
+    items = o;     o = align_up(o + (size_t)R * kTopkCandCap * 8);
     bytes = o;
   }
 };

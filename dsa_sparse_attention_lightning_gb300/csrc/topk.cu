@@ -2,30 +2,40 @@
 //
 // Keeps the min(k, len) highest-scoring positions of each row, ties to the
 // lower position (TokenSpeed post on Kimi K3.1 Pro, step 3 "Select": a radix
-// top-k keeps the 2,048 highest-scoring positions for each query).  Like the
-// pages' multi-workgroup design ("Reducing indexer overhead on AMD MI350X":
-// each row is spread over many workgroups that share a histogram of score
-// prefixes), one long row is spread over many CTAs:
+// top-k keeps the 2,048 highest-scoring positions for each query).  Scores are
+// compared as order-preserving uint32 keys.  Three launches:
 //
-//   1. hist     (row x 4096-score chunk CTAs): histogram of the top 11 bits of
-//               the order-preserving uint32 key of every score.
-//   2. collect  (row x chunk CTAs): every CTA finds the threshold digit D1 (the
-//               digit holding the k-th best key) from the shared histogram and
-//               copies, in position order, the (key, position) pairs whose
-//               digit is >= D1 into the chunk's own segment.
-//   3. finalize (one CTA per row): two more radix digits over the collected
-//               candidates give the exact k-th key T and how many keys equal
-//               to T are needed; an ordered pass over the segments emits every
-//               key > T and the first `need` keys == T, so ties go to the
-//               lower position and idx comes out in ascending order.
+//   1. sample   (one CTA per row): a fixed sample of the row (every sb-th
+//               block of 32 scores, sb >= 16, at most 16384 scores) gives a
+//               threshold tau low enough that the row should hold about
+//               1.5 k + 32 sb keys >= tau: the key of the sample's rank-rho
+//               element, rounded down to its 22-bit prefix (two radix digits
+//               over the sample).
+//   2. collect  (row x 4096-score chunk CTAs): every key >= tau is appended,
+//               with its position, to the row's candidate list (one global
+//               reservation per CTA, so each chunk's candidates form one run in
+//               position order; the run's place is recorded); the count is
+//               kept even past capacity.
+//   3. finalize (one CTA per row): if the row holds at least k and at most
+//               kTopkCandCap candidates, every one of the k best keys is a
+//               candidate (count(key >= tau) >= k means tau <= the k-th key),
+//               so an exact radix select over the candidates in shared memory
+//               gives the k-th key T and how many keys equal to T to keep (the
+//               lowest positions).  The kept candidates are written in
+//               position order by ranking them within their chunk's run and
+//               the runs in chunk order (scans, no sort).  Otherwise the same
+//               exact select runs over the whole row in position order.
+// The threshold only decides how much work the exact select does, never its
+// result: the result is the exact top-k for any sample.
 #include "dsa_common.cuh"
 
 namespace dsa {
 namespace {
 
-constexpr int kHistThreads = 512;
+constexpr int kSampleThreads = 1024;
 constexpr int kCollectThreads = 256;
 constexpr int kFinalThreads = 1024;
+constexpr int kSampleStride = 16;              // one 32-score block in 16
 
 // Inclusive block scan of one uint32 per thread (NT threads).
 template <int NT>
@@ -88,43 +98,82 @@ __device__ __forceinline__ bool row_ok(int len, int64_t max_len) {
   return len >= 0 && (int64_t)len <= max_len;
 }
 
-// ---- 1. histogram of the top digit ---------------------------------------
-__global__ void __launch_bounds__(kHistThreads)
-topk_hist_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
-                 int64_t max_len, int k, uint32_t* __restrict__ hist) {
-  const int r = blockIdx.y;
-  const int len = row_len[r];
-  if (!row_ok(len, max_len) || len <= k) return;
-  const int64_t s0 = (int64_t)blockIdx.x * kTopkChunk;
-  if (s0 >= len) return;
-  const int64_t s1 = min((int64_t)len, s0 + kTopkChunk);
-  __shared__ uint32_t h[kTopkBins1];
-  for (int i = threadIdx.x; i < kTopkBins1; i += kHistThreads) h[i] = 0;
-  __syncthreads();
-  const float* row = scores + (size_t)r * ld;
-  for (int64_t s = s0 + threadIdx.x * 4; s < s1; s += kHistThreads * 4) {
-    if (s + 4 <= s1) {
-      const float4 v = __ldg(reinterpret_cast<const float4*>(row + s));
-      atomicAdd(&h[ordered_key(v.x) >> 21], 1u);
-      atomicAdd(&h[ordered_key(v.y) >> 21], 1u);
-      atomicAdd(&h[ordered_key(v.z) >> 21], 1u);
-      atomicAdd(&h[ordered_key(v.w) >> 21], 1u);
-    } else {
-      for (int64_t t = s; t < s1; ++t) atomicAdd(&h[ordered_key(row[t]) >> 21], 1u);
-    }
-  }
-  __syncthreads();
-  uint32_t* gh = hist + (size_t)r * kTopkBins1;
-  for (int i = threadIdx.x; i < kTopkBins1; i += kHistThreads)
-    if (h[i]) atomicAdd(&gh[i], h[i]);
+// Shared-memory histogram add; lanes that fall in the same bin add once.
+// All 32 lanes of the warp call it.
+__device__ __forceinline__ void hist_add(uint32_t* h, uint32_t bin, bool valid) {
+  const unsigned m = __match_any_sync(0xffffffffu, valid ? bin : 0xFFFFFFFFu);
+  if (valid && (threadIdx.x & 31) == __ffs(m) - 1) atomicAdd(&h[bin], (uint32_t)__popc(m));
 }
 
-// ---- 2. ordered collection of digit >= D1 ------------------------------------
+// ---- 1. threshold from a fixed sample ----------------------------------------
+// Every sb-th block of 32 scores, sb >= 16 chosen so that the sample holds at
+// most kSampleBlocks blocks.
+constexpr int kSampleBlocks = 512;
+
+__device__ __forceinline__ int64_t sample_stride(int len) {
+  const int64_t blocks = ((int64_t)len + 31) / 32;
+  const int64_t sb = (blocks + kSampleBlocks - 1) / kSampleBlocks;
+  return sb < kSampleStride ? kSampleStride : sb;
+}
+
+__global__ void __launch_bounds__(kSampleThreads)
+topk_sample_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
+                   int64_t max_len, int k, uint32_t* __restrict__ tau) {
+  const int r = blockIdx.x;
+  const int len = row_len[r];
+  if (!row_ok(len, max_len) || len <= k) return;
+  __shared__ uint32_t h[kTopkBins1];
+  __shared__ uint32_t warp_sums[32];
+  __shared__ int s_d;
+  __shared__ uint32_t s_above, s_n;
+  const float* row = scores + (size_t)r * ld;
+  const int64_t sb = sample_stride(len);
+  const int64_t ns = ((((int64_t)len + 31) / 32 + sb - 1) / sb) * 32;   // upper bound (ragged end)
+  auto sample_pos = [&](int64_t e) { return (e / 32) * 32 * sb + (e % 32); };
+  // rank rho in the sample ~ 1.5 k / sb + 32 (about 1.5 k + 32 sb candidates in the row)
+  const uint32_t rho = (uint32_t)((3 * (int64_t)k + 2 * sb - 1) / (2 * sb)) + 32;
+  for (int i = threadIdx.x; i < kTopkBins1; i += kSampleThreads) h[i] = 0;
+  if (threadIdx.x == 0) s_n = 0;
+  __syncthreads();
+  uint32_t n_local = 0;
+  for (int64_t b = 0; b < ns; b += kSampleThreads) {              // uniform trip count
+    const int64_t e = b + threadIdx.x;
+    const int64_t pos = sample_pos(e);
+    const bool v = e < ns && pos < len;
+    const uint32_t key = v ? ordered_key(row[pos]) : 0u;
+    n_local += v ? 1u : 0u;
+    hist_add(h, key >> 21, v);
+  }
+  atomicAdd(&s_n, n_local);
+  __syncthreads();
+  if (s_n < rho) {                             // short sample: take every key
+    if (threadIdx.x == 0) tau[r] = 0u;
+    return;
+  }
+  find_threshold<kTopkBins1, kSampleThreads>(h, rho, warp_sums, &s_d, &s_above);
+  const uint32_t d1 = (uint32_t)s_d;
+  const uint32_t need = rho - s_above;
+  __syncthreads();
+  for (int i = threadIdx.x; i < kTopkBins1; i += kSampleThreads) h[i] = 0;
+  __syncthreads();
+  for (int64_t b = 0; b < ns; b += kSampleThreads) {
+    const int64_t e = b + threadIdx.x;
+    const int64_t pos = sample_pos(e);
+    const bool v = e < ns && pos < len;
+    const uint32_t key = v ? ordered_key(row[pos]) : 0u;
+    hist_add(h, (key >> 10) & 0x7FF, v && (key >> 21) == d1);
+  }
+  __syncthreads();
+  find_threshold<kTopkBins2, kSampleThreads>(h, need, warp_sums, &s_d, &s_above);
+  if (threadIdx.x == 0) tau[r] = (d1 << 21) | ((uint32_t)s_d << 10);
+}
+
+// ---- 2. candidates: every key >= tau -------------------------------------------
 __global__ void __launch_bounds__(kCollectThreads)
 topk_collect_kernel(const float* __restrict__ scores, int64_t ld,
                     const int32_t* __restrict__ row_len, int64_t max_len, int k,
-                    const uint32_t* __restrict__ hist, uint2* __restrict__ thr,
-                    uint32_t* __restrict__ seg_count, uint2* __restrict__ items, int nchunks) {
+                    const uint32_t* __restrict__ tau, uint32_t* __restrict__ cnt,
+                    uint2* __restrict__ runs, int nchunks, uint2* __restrict__ items) {
   const int r = blockIdx.y;
   const int c = blockIdx.x;
   const int len = row_len[r];
@@ -132,24 +181,15 @@ topk_collect_kernel(const float* __restrict__ scores, int64_t ld,
   const int64_t s0 = (int64_t)c * kTopkChunk;
   if (s0 >= len) return;
   const int64_t s1 = min((int64_t)len, s0 + kTopkChunk);
-
-  __shared__ uint32_t h[kTopkBins1];
   __shared__ uint32_t warp_sums[32];
-  __shared__ int s_d;
-  __shared__ uint32_t s_above;
-  for (int i = threadIdx.x; i < kTopkBins1; i += kCollectThreads)
-    h[i] = hist[(size_t)r * kTopkBins1 + i];
-  __syncthreads();
-  find_threshold<kTopkBins1, kCollectThreads>(h, (uint32_t)k, warp_sums, &s_d, &s_above);
-  const uint32_t d1 = (uint32_t)s_d;
-  if (c == 0 && threadIdx.x == 0) thr[r] = make_uint2(d1, s_above);
+  __shared__ uint32_t s_base;
+  const uint32_t t = tau[r];
 
-  // each thread owns 16 consecutive positions: keeps the chunk's order
+  // each thread owns 16 consecutive positions
   constexpr int PER = kTopkChunk / kCollectThreads;
   const float* row = scores + (size_t)r * ld;
   const int64_t base = s0 + (int64_t)threadIdx.x * PER;
   uint32_t keys[PER];
-  uint32_t cnt = 0;
 #pragma unroll
   for (int i = 0; i < PER; i += 4) {
     float4 v;
@@ -166,40 +206,125 @@ topk_collect_kernel(const float* __restrict__ scores, int64_t ld,
     keys[i + 2] = ordered_key(v.z);
     keys[i + 3] = ordered_key(v.w);
   }
+  uint32_t n = 0;
 #pragma unroll
-  for (int i = 0; i < PER; ++i) cnt += (base + i < s1 && (keys[i] >> 21) >= d1) ? 1u : 0u;
-  const uint32_t incl = block_inclusive_scan<kCollectThreads>(cnt, warp_sums);
-  uint32_t pos = incl - cnt;
-  uint2* seg = items + ((size_t)r * nchunks + c) * kTopkChunk;
+  for (int i = 0; i < PER; ++i) n += (base + i < s1 && keys[i] >= t) ? 1u : 0u;
+  const uint32_t incl = block_inclusive_scan<kCollectThreads>(n, warp_sums);
+  if (threadIdx.x == kCollectThreads - 1) {
+    s_base = incl ? atomicAdd(&cnt[r], incl) : 0u;
+    runs[(size_t)r * nchunks + c] = make_uint2(s_base, incl);   // this chunk's run in the list
+  }
+  __syncthreads();
+  uint32_t pos = s_base + incl - n;
+  uint2* seg = items + (size_t)r * kTopkCandCap;
 #pragma unroll
   for (int i = 0; i < PER; ++i)
-    if (base + i < s1 && (keys[i] >> 21) >= d1) seg[pos++] = make_uint2(keys[i], (uint32_t)(base + i));
-  if (threadIdx.x == kCollectThreads - 1) seg_count[(size_t)r * nchunks + c] = incl;
+    if (base + i < s1 && keys[i] >= t) {
+      if (pos < (uint32_t)kTopkCandCap) seg[pos] = make_uint2(keys[i], (uint32_t)(base + i));
+      ++pos;
+    }
 }
 
-// ---- 3. exact threshold and ordered emission (one CTA per row) -------------
-__device__ __forceinline__ uint2 item_at(const uint2* seg_base, const uint32_t* prefix, int nch,
-                                         uint32_t i) {
-  // chunk c holds flattened items [prefix[c], prefix[c+1])
-  int lo = 0, hi = nch;  // find last c with prefix[c] <= i
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= i) lo = mid; else hi = mid;
+// ---- 3. exact select ----------------------------------------------------------
+struct SelectSmem {
+  uint32_t h[kTopkBins1];
+  uint32_t warp_sums[32];
+  int d;
+  uint32_t above, acc[2];
+};
+
+// k-th key T of `total` keys key_at(i) and how many keys equal to T to keep:
+// three radix digits of 11, 11 and 10 bits.  n_eq = keys equal to T.
+template <typename KeyAt>
+__device__ void kth_key(KeyAt key_at, uint32_t total, int k, SelectSmem& S, uint32_t& T,
+                        uint32_t& need_eq, uint32_t& n_eq) {
+  uint32_t need = (uint32_t)k;
+  uint32_t prefix = 0;                         // key bits fixed so far
+  int shift = 32;
+  for (int dgt = 0; dgt < 3; ++dgt) {
+    const int w = dgt < 2 ? 11 : 10;
+    shift -= w;
+    for (int i = threadIdx.x; i < kTopkBins1; i += kFinalThreads) S.h[i] = 0;
+    __syncthreads();
+    const int pshift = shift + w;              // bits above this digit
+    for (uint32_t b = 0; b < total; b += kFinalThreads) {
+      const uint32_t i = b + threadIdx.x;
+      const uint32_t key = i < total ? key_at(i) : 0u;
+      const bool v = i < total && (dgt == 0 || (key >> pshift) == prefix);
+      hist_add(S.h, (key >> shift) & ((1u << w) - 1u), v);
+    }
+    __syncthreads();
+    if (w == 11) find_threshold<kTopkBins1, kFinalThreads>(S.h, need, S.warp_sums, &S.d, &S.above);
+    else find_threshold<kTopkBins3, kFinalThreads>(S.h, need, S.warp_sums, &S.d, &S.above);
+    prefix = (prefix << w) | (uint32_t)S.d;
+    need -= S.above;
   }
-  return seg_base[(size_t)lo * kTopkChunk + (i - prefix[lo])];
+  T = prefix;
+  need_eq = need;
+  n_eq = S.h[S.d];
+  __syncthreads();
 }
+
+// Exclusive scan of PER flags per thread (consecutive elements) into ex[];
+// returns the total.  All threads call it.
+template <int PER>
+__device__ __forceinline__ uint32_t scan_flags(const uint8_t (&f)[PER], uint16_t* ex, uint32_t n,
+                                               SelectSmem& S) {
+  uint32_t local = 0;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) local += f[u];
+  const uint32_t incl = block_inclusive_scan<kFinalThreads>(local, S.warp_sums);
+  uint32_t run = incl - local;
+  const uint32_t i0 = threadIdx.x * PER;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    if (i0 + u <= n) ex[i0 + u] = (uint16_t)run;   // ex[n] = total (run end lookups)
+    run += f[u];
+  }
+  if (threadIdx.x == kFinalThreads - 1) S.acc[0] = incl;
+  __syncthreads();
+  const uint32_t total = S.acc[0];
+  if (threadIdx.x == 0) ex[n] = (uint16_t)total;
+  __syncthreads();
+  return total;
+}
+
+// Exclusive scan over chunks (in chunk order) of the counts cnt_of(c) -> base[c].
+template <typename CntOf>
+__device__ __forceinline__ void scan_chunks(CntOf cnt_of, int nch, uint32_t* base, SelectSmem& S) {
+  uint32_t carry = 0;
+  for (int c0 = 0; c0 < nch; c0 += kFinalThreads) {
+    const int c = c0 + threadIdx.x;
+    const uint32_t v = c < nch ? cnt_of(c) : 0u;
+    const uint32_t incl = block_inclusive_scan<kFinalThreads>(v, S.warp_sums);
+    if (c < nch) base[c] = carry + incl - v;
+    if (threadIdx.x == kFinalThreads - 1) S.acc[1] = incl;
+    __syncthreads();
+    carry += S.acc[1];
+    __syncthreads();
+  }
+}
+
+constexpr int kCandPer = kTopkCandCap / kFinalThreads;     // candidates per thread
+constexpr int kMaxRunChunks = 4096;                       // chunk table held in shared memory
+
+struct CandSmem {
+  uint2 cand[kTopkCandCap];
+  uint16_t ex_tie[kTopkCandCap + kFinalThreads];
+  uint16_t ex_sel[kTopkCandCap + kFinalThreads];
+  uint32_t base_tie[kMaxRunChunks];
+  uint32_t base_sel[kMaxRunChunks];
+};
 
 __global__ void __launch_bounds__(kFinalThreads)
-topk_finalize_kernel(const int32_t* __restrict__ row_len, int64_t max_len, int k,
-                     const uint2* __restrict__ thr, const uint32_t* __restrict__ seg_count,
-                     const uint2* __restrict__ items, int nchunks, int32_t* __restrict__ idx,
+topk_finalize_kernel(const float* __restrict__ scores, int64_t ld,
+                     const int32_t* __restrict__ row_len, int64_t max_len, int k,
+                     const uint32_t* __restrict__ cnt, const uint2* __restrict__ runs,
+                     int nchunks, const uint2* __restrict__ items, int32_t* __restrict__ idx,
                      uint32_t* status) {
-  extern __shared__ uint32_t prefix[];  // nchunks + 1
-  __shared__ uint32_t h[kTopkBins2];
-  __shared__ uint32_t warp_sums[32];
-  __shared__ int s_d;
-  __shared__ uint32_t s_above;
-  __shared__ uint32_t s_total;
+  extern __shared__ __align__(16) uint8_t fin_smem[];
+  SelectSmem& S = *reinterpret_cast<SelectSmem*>(fin_smem);
+  CandSmem& C = *reinterpret_cast<CandSmem*>(fin_smem + (sizeof(SelectSmem) + 15) / 16 * 16);
   const int r = blockIdx.x;
   const int len = row_len[r];
   int32_t* out = idx + (size_t)r * k;
@@ -212,73 +337,77 @@ topk_finalize_kernel(const int32_t* __restrict__ row_len, int64_t max_len, int k
     for (int j = threadIdx.x; j < k; j += kFinalThreads) out[j] = j < len ? j : -1;
     return;
   }
+  const uint32_t n = cnt[r];
   const int nch = (int)((len + kTopkChunk - 1) / kTopkChunk);
-  const uint2* seg_base = items + (size_t)r * nchunks * kTopkChunk;
-  if (threadIdx.x == 0) {
-    uint32_t acc = 0;
-    for (int c = 0; c < nch; ++c) {
-      prefix[c] = acc;
-      acc += seg_count[(size_t)r * nchunks + c];
-    }
-    prefix[nch] = acc;
-    s_total = acc;
-  }
-  __syncthreads();
-  const uint32_t total = s_total;
-  const uint2 t1 = thr[r];
-  const uint32_t d1 = t1.x;
-  uint32_t need = (uint32_t)k - t1.y;  // keys with digit == d1 still needed (>= 1)
-
-  // second digit among digit-1 == d1
-  for (int i = threadIdx.x; i < kTopkBins2; i += kFinalThreads) h[i] = 0;
-  __syncthreads();
-  for (uint32_t i = threadIdx.x; i < total; i += kFinalThreads) {
-    const uint2 it = item_at(seg_base, prefix, nch, i);
-    if ((it.x >> 21) == d1) atomicAdd(&h[(it.x >> 10) & 0x7FF], 1u);
-  }
-  __syncthreads();
-  find_threshold<kTopkBins2, kFinalThreads>(h, need, warp_sums, &s_d, &s_above);
-  const uint32_t d2 = (uint32_t)s_d;
-  need -= s_above;
-  const uint32_t hi22 = (d1 << 11) | d2;
-
-  // third digit among the top 22 bits == (d1, d2)
-  for (int i = threadIdx.x; i < kTopkBins2; i += kFinalThreads) h[i] = 0;
-  __syncthreads();
-  for (uint32_t i = threadIdx.x; i < total; i += kFinalThreads) {
-    const uint2 it = item_at(seg_base, prefix, nch, i);
-    if ((it.x >> 10) == hi22) atomicAdd(&h[it.x & 0x3FF], 1u);
-  }
-  __syncthreads();
-  find_threshold<kTopkBins3, kFinalThreads>(h, need, warp_sums, &s_d, &s_above);
-  const uint32_t T = (hi22 << 10) | (uint32_t)s_d;
-  const uint32_t need_eq = need - s_above;  // keys equal to T to take, lowest positions first
-
-  // ordered emission
-  uint32_t out_count = 0, eq_seen = 0;
-  for (uint32_t b = 0; b < total; b += kFinalThreads) {
-    const uint32_t i = b + threadIdx.x;
-    uint2 it = make_uint2(0u, 0u);
-    if (i < total) it = item_at(seg_base, prefix, nch, i);
-    const uint32_t is_eq = (i < total && it.x == T) ? 1u : 0u;
-    const uint32_t eq_incl = block_inclusive_scan<kFinalThreads>(is_eq, warp_sums);
-    const uint32_t take_eq = is_eq && (eq_seen + eq_incl - 1u) < need_eq;
-    const uint32_t sel = (i < total && it.x > T) || take_eq ? 1u : 0u;
-    const uint32_t sel_incl = block_inclusive_scan<kFinalThreads>(sel, warp_sums);
-    const uint32_t pos = out_count + sel_incl - 1u;
-    if (sel && pos < (uint32_t)k) out[pos] = (int32_t)it.y;
-    // totals of this batch: the last thread's inclusive values
-    __shared__ uint32_t s_batch[2];
-    if (threadIdx.x == kFinalThreads - 1) {
-      s_batch[0] = sel_incl;
-      s_batch[1] = eq_incl;
-    }
+  uint32_t T, need_eq, n_eq;
+  if (n >= (uint32_t)k && n <= (uint32_t)kTopkCandCap && nch <= kMaxRunChunks) {
+    // ---- candidates in shared memory, ranked by position through their runs
+    const uint2* src = items + (size_t)r * kTopkCandCap;
+    for (uint32_t i = threadIdx.x; i < n; i += kFinalThreads) C.cand[i] = src[i];
     __syncthreads();
-    out_count += s_batch[0];
-    eq_seen += s_batch[1];
-    __syncthreads();
+    kth_key([&](uint32_t i) { return C.cand[i].x; }, n, k, S, T, need_eq, n_eq);
+    const uint2* rr = runs + (size_t)r * nchunks;
+    const uint32_t i0 = threadIdx.x * kCandPer;
+    uint8_t f[kCandPer];
+    // ties: rank by position = ties in earlier chunks + ties earlier in the run
+#pragma unroll
+    for (int u = 0; u < kCandPer; ++u) f[u] = (i0 + u < n && C.cand[i0 + u].x == T) ? 1 : 0;
+    scan_flags(f, C.ex_tie, n, S);
+    scan_chunks([&](int c) { const uint2 q = rr[c]; return (uint32_t)(C.ex_tie[q.x + q.y] - C.ex_tie[q.x]); },
+                nch, C.base_tie, S);
+    // kept: key > T, or a tie of rank < need_eq
+#pragma unroll
+    for (int u = 0; u < kCandPer; ++u) {
+      const uint32_t i = i0 + u;
+      uint8_t keep = 0;
+      if (i < n) {
+        const uint2 v = C.cand[i];
+        if (v.x > T) {
+          keep = 1;
+        } else if (v.x == T) {
+          const uint2 q = rr[v.y / kTopkChunk];
+          keep = (C.base_tie[v.y / kTopkChunk] + C.ex_tie[i] - C.ex_tie[q.x]) < need_eq ? 1 : 0;
+        }
+      }
+      f[u] = keep;
+    }
+    scan_flags(f, C.ex_sel, n, S);
+    scan_chunks([&](int c) { const uint2 q = rr[c]; return (uint32_t)(C.ex_sel[q.x + q.y] - C.ex_sel[q.x]); },
+                nch, C.base_sel, S);
+#pragma unroll
+    for (int u = 0; u < kCandPer; ++u) {
+      if (!f[u]) continue;
+      const uint2 v = C.cand[i0 + u];
+      const int c = (int)(v.y / kTopkChunk);
+      const uint32_t o = C.base_sel[c] + C.ex_sel[i0 + u] - C.ex_sel[rr[c].x];
+      if (o < (uint32_t)k) out[o] = (int32_t)v.y;
+    }
+    (void)n_eq;
+  } else {
+    // ---- the whole row, in position order
+    const float* row = scores + (size_t)r * ld;
+    kth_key([&](uint32_t i) { return ordered_key(row[i]); }, (uint32_t)len, k, S, T, need_eq, n_eq);
+    uint32_t out_count = 0, eq_seen = 0;
+    for (uint32_t b = 0; b < (uint32_t)len; b += kFinalThreads) {
+      const uint32_t i = b + threadIdx.x;
+      const uint32_t key = i < (uint32_t)len ? ordered_key(row[i]) : 0u;
+      const uint32_t is_eq = (i < (uint32_t)len && key == T) ? 1u : 0u;
+      const uint32_t eq_incl = block_inclusive_scan<kFinalThreads>(is_eq, S.warp_sums);
+      const bool take_eq = is_eq && (eq_seen + eq_incl - 1u) < need_eq;
+      const uint32_t sel = ((i < (uint32_t)len && key > T) || take_eq) ? 1u : 0u;
+      const uint32_t sel_incl = block_inclusive_scan<kFinalThreads>(sel, S.warp_sums);
+      const uint32_t pos = out_count + sel_incl - 1u;
+      if (sel && pos < (uint32_t)k) out[pos] = (int32_t)i;
+      if (threadIdx.x == kFinalThreads - 1) {
+        S.acc[0] = sel_incl;
+        S.acc[1] = eq_incl;
+      }
+      __syncthreads();
+      out_count += S.acc[0];
+      eq_seen += S.acc[1];
+      __syncthreads();
+    }
   }
-  for (int j = (int)out_count + threadIdx.x; j < k; j += kFinalThreads) out[j] = -1;
 }
 
 }  // namespace
@@ -286,25 +415,23 @@ topk_finalize_kernel(const int32_t* __restrict__ row_len, int64_t max_len, int k
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
   if (a.R == 0) return cudaSuccess;
   const TopkLayout L(a.R, a.max_len);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(a.scratch + L.hist);
-  uint2* thr = reinterpret_cast<uint2*>(a.scratch + L.thr);
-  uint32_t* seg_count = reinterpret_cast<uint32_t*>(a.scratch + L.seg_count);
+  uint32_t* tau = reinterpret_cast<uint32_t*>(a.scratch + L.tau);
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(a.scratch + L.cnt);
+  uint2* runs = reinterpret_cast<uint2*>(a.scratch + L.runs);
   uint2* items = reinterpret_cast<uint2*>(a.scratch + L.items);
-  cudaError_t e = cudaMemsetAsync(hist, 0, (size_t)a.R * kTopkBins1 * 4, st);
+  cudaError_t e = cudaMemsetAsync(cnt, 0, (size_t)a.R * 4, st);
   if (e != cudaSuccess) return e;
+  topk_sample_kernel<<<a.R, kSampleThreads, 0, st>>>(a.scores, a.ld, a.row_len, a.max_len, a.k,
+                                                     tau);
   dim3 grid(L.nchunks, a.R);
-  topk_hist_kernel<<<grid, kHistThreads, 0, st>>>(a.scores, a.ld, a.row_len, a.max_len, a.k, hist);
   topk_collect_kernel<<<grid, kCollectThreads, 0, st>>>(a.scores, a.ld, a.row_len, a.max_len,
-                                                        a.k, hist, thr, seg_count, items,
-                                                        L.nchunks);
-  const size_t smem = (size_t)(L.nchunks + 1) * 4;
-  if (smem > 48 * 1024) {
-    e = cudaFuncSetAttribute(topk_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-  }
-  topk_finalize_kernel<<<a.R, kFinalThreads, smem, st>>>(a.row_len, a.max_len, a.k, thr,
-                                                         seg_count, items, L.nchunks, a.idx,
+                                                        a.k, tau, cnt, runs, L.nchunks, items);
+  const size_t smem = (sizeof(SelectSmem) + 15) / 16 * 16 + sizeof(CandSmem);
+  e = cudaFuncSetAttribute(topk_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem);
+  if (e != cudaSuccess) return e;
+  topk_finalize_kernel<<<a.R, kFinalThreads, smem, st>>>(a.scores, a.ld, a.row_len, a.max_len,
+                                                         a.k, cnt, runs, L.nchunks, items, a.idx,
                                                          a.status);
   return cudaGetLastError();
 }

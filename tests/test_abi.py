@@ -46,8 +46,10 @@ def test_version_and_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    assert lib.dsa_topk_workspace_size(4, 1000, 64) >= 256 + 4 * 2048 * 4
-    assert lib.dsa_topk_workspace_size(8, 1 << 20, 2048) > lib.dsa_topk_workspace_size(8, 1 << 10, 2048)
+    # per row: a threshold, a count and room for 8192 (key, position) candidates,
+    # whatever the row length (longer rows fall back to a pass over the scores)
+    assert lib.dsa_topk_workspace_size(4, 1000, 64) >= 4 * 8192 * 8
+    assert lib.dsa_topk_workspace_size(8, 1 << 20, 2048) == lib.dsa_topk_workspace_size(8, 1 << 10, 2048)
     assert lib.dsa_sparse_mla_workspace_size(64, 64, 2048) >= 64 * 64 * 512 * 4
     assert lib.dsa_decode_step_workspace_size(16, 64, 512, 64, 2048) >= \
         lib.dsa_topk_workspace_size(64, 512 * 64, 2048)

@@ -126,6 +126,25 @@ def test_topk_ties_signs_and_edges(dsa, oracle_mod):
     _topk_bitexact(dsa, oracle_mod, s[:2], [0, 5], 16)
 
 
+def test_topk_rows_built_against_the_sample(dsa, oracle_mod):
+    """The selection is exact whatever a fixed sample of the row suggests: rows
+    whose best scores sit only outside, or only inside, the sampled blocks
+    (every 16th block of 32 scores), so the candidate threshold is far too low
+    (candidates overflow) or too high (fewer than k candidates)."""
+    rng = np.random.default_rng(2)
+    L = 40000
+    pos = np.arange(L)
+    in_sample = (pos // 32) % 16 == 0
+    hidden = rng.standard_normal(L).astype(np.float32)
+    hidden[~in_sample] += 10.0                           # best scores never sampled
+    only = rng.standard_normal(L).astype(np.float32)
+    only[in_sample] += 10.0                              # 2528 sampled highs, then noise
+    short = rng.standard_normal(L).astype(np.float32)
+    short[in_sample & (pos < 16384)] += 10.0             # 1024 sampled highs < k
+    s = np.stack([hidden, only, short])
+    _topk_bitexact(dsa, oracle_mod, s, [L, L, 16384], 2048)
+
+
 def test_topk_long_row_split_over_chunks(dsa, oracle_mod):
     rng = np.random.default_rng(1)
     L = 1 << 20
