@@ -663,45 +663,87 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
   }
 }
 
-// One CTA per (row, head) of a unit cut by CTA ranges: merge its partials by
-// log-sum-exp.  Units held whole by one CTA were written by the main kernel.
-__global__ void __launch_bounds__(128)
+// Merge of the partials of units cut by CTA ranges, by log-sum-exp.  A CTA
+// takes kCombHeads heads of one unit (128 threads per head, 4 dims each): the
+// partial lse values of all its splits are loaded at once into shared memory,
+// then every thread accumulates its dims over the splits with independent
+// loads.  Units held whole by one CTA were written by the main kernel; with no
+// slots at all (k = 0) the outputs are zero and lse = -inf.
+constexpr int kCombHeads = 4;
+constexpr int kCombMaxSplits = 2 * kMlaGrid;
+
+__global__ void __launch_bounds__(128 * kCombHeads)
 mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int R,
                    int H, int k, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-  const int r = blockIdx.x / H, h = blockIdx.x % H;
+  __shared__ float s_w[kCombHeads][kCombMaxSplits];  // weights e^{lse_s - M} / Z
+  __shared__ int s_slot[kCombMaxSplits];
+  __shared__ float s_lse[kCombHeads];
+  const int hq = threadIdx.x >> 7, t = threadIdx.x & 127;
+  const int h = blockIdx.x % (H / kCombHeads) * kCombHeads + hq;
+  const int r = blockIdx.x / (H / kCombHeads);
   const int HG = mla_heads_per_cta(H);
-  const int u = r * (H / HG) + h / HG, hl = h % HG;
+  const int u = r * (H / HG) + h / HG;               // the block's heads share a unit
+  const int hl = h % HG;
   const MlaWork w(R, H, k);
-  float M = -INFINITY;
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  float Z = 0.f;
+  int c0 = 0, c1 = -1;
   if (w.T > 0) {
-    const int c0 = w.cta_of((int64_t)u * w.NT), c1 = w.cta_of((int64_t)(u + 1) * w.NT - 1);
-    if (c0 == c1) return;
-    auto slot = [&](int c) { return 2 * c + (w.begin(c) / w.NT == u ? 0 : 1); };
-    for (int c = c0; c <= c1; ++c) M = fmaxf(M, part_lse[(size_t)slot(c) * HG + hl]);
-    if (M != -INFINITY) {
-      for (int c = c0; c <= c1; ++c) {
-        const size_t pb = (size_t)slot(c) * HG + hl;
-        const float ls = part_lse[pb];
-        if (ls == -INFINITY) continue;
-        const float ws = __expf(ls - M);
-        Z += ws;
-        const float4 v = __ldg(reinterpret_cast<const float4*>(part_o + pb * kVDim) + threadIdx.x);
-        acc[0] = fmaf(ws, v.x, acc[0]);
-        acc[1] = fmaf(ws, v.y, acc[1]);
-        acc[2] = fmaf(ws, v.z, acc[2]);
-        acc[3] = fmaf(ws, v.w, acc[3]);
-      }
+    c0 = w.cta_of((int64_t)u * w.NT);
+    c1 = w.cta_of((int64_t)(u + 1) * w.NT - 1);
+    if (c0 == c1) return;                           // written by the main kernel
+  }
+  const int ns = c1 - c0 + 1;                       // 0 when there are no slots
+  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
+    const int c = c0 + i;
+    s_slot[i] = 2 * c + (w.begin(c) / w.NT == u ? 0 : 1);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < ns * kCombHeads; i += blockDim.x) {
+    const int hh = i / ns, sp = i % ns;
+    s_w[hh][sp] = part_lse[(size_t)s_slot[sp] * HG + (hl - hq + hh)];
+  }
+  __syncthreads();
+  if (t == 0) {                                     // one thread per head: max, sum, weights
+    float M = -INFINITY;
+    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, s_w[hq][sp]);
+    float Z = 0.f;
+    for (int sp = 0; sp < ns; ++sp) {
+      const float e = (M == -INFINITY || s_w[hq][sp] == -INFINITY) ? 0.f : __expf(s_w[hq][sp] - M);
+      s_w[hq][sp] = e;
+      Z += e;
+    }
+    const float inv = Z > 0.f ? 1.f / Z : 0.f;
+    for (int sp = 0; sp < ns; ++sp) s_w[hq][sp] *= inv;
+    s_lse[hq] = Z > 0.f ? M + logf(Z) : -INFINITY;
+  }
+  __syncthreads();
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  int sp = 0;
+  for (; sp + 4 <= ns; sp += 4) {                   // four independent loads in flight
+    float4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      v[j] = __ldg(reinterpret_cast<const float4*>(part_o + ((size_t)s_slot[sp + j] * HG + hl) * kVDim) + t);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float ws = s_w[hq][sp + j];
+      acc.x = fmaf(ws, v[j].x, acc.x);
+      acc.y = fmaf(ws, v[j].y, acc.y);
+      acc.z = fmaf(ws, v[j].z, acc.z);
+      acc.w = fmaf(ws, v[j].w, acc.w);
     }
   }
-  const float inv = Z > 0.f ? 1.f / Z : 0.f;
-  __nv_bfloat16* dst = out + ((size_t)r * H + h) * kVDim + threadIdx.x * 4;
-  dst[0] = __float2bfloat16_rn(acc[0] * inv);
-  dst[1] = __float2bfloat16_rn(acc[1] * inv);
-  dst[2] = __float2bfloat16_rn(acc[2] * inv);
-  dst[3] = __float2bfloat16_rn(acc[3] * inv);
-  if (lse && threadIdx.x == 0) lse[(size_t)r * H + h] = Z > 0.f ? M + logf(Z) : -INFINITY;
+  for (; sp < ns; ++sp) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(part_o + ((size_t)s_slot[sp] * HG + hl) * kVDim) + t);
+    const float ws = s_w[hq][sp];
+    acc.x = fmaf(ws, v.x, acc.x);
+    acc.y = fmaf(ws, v.y, acc.y);
+    acc.z = fmaf(ws, v.z, acc.z);
+    acc.w = fmaf(ws, v.w, acc.w);
+  }
+  __nv_bfloat16* dst = out + ((size_t)r * H + h) * kVDim + t * 4;
+  reinterpret_cast<__nv_bfloat162*>(dst)[0] = __floats2bfloat162_rn(acc.x, acc.y);
+  reinterpret_cast<__nv_bfloat162*>(dst)[1] = __floats2bfloat162_rn(acc.z, acc.w);
+  if (lse && t == 0) lse[(size_t)r * H + h] = s_lse[hq];
 }
 
 // The latent cache as a 2-D tensor of 576-byte rows (one per token slot); a box
@@ -750,7 +792,7 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t st) {
     else e = launch_smla<64>(a, L, w.G, st);
     if (e != cudaSuccess) return e;
   }
-  mla_combine_kernel<<<a.R * a.H, 128, 0, st>>>(reinterpret_cast<const float*>(a.scratch + L.part_o),
+  mla_combine_kernel<<<a.R * a.H / kCombHeads, 128 * kCombHeads, 0, st>>>(reinterpret_cast<const float*>(a.scratch + L.part_o),
                                                 reinterpret_cast<const float*>(a.scratch + L.part_lse),
                                                 a.R, a.H, a.k, static_cast<__nv_bfloat16*>(a.out),
                                                 a.lse);
