@@ -35,9 +35,19 @@ from dsa_sparse_attention_lightning_gb300 import inputs, traffic  # noqa: E402
 
 METRIC = "DSA decode-step µs/layer and achieved HBM GB/s vs 8 TB/s roofline, 1 GB300"
 L2_FLUSH_BYTES = 256 << 20
-# scan 2 (query split + grouping, scan), top-k 3 (histogram, collect, finalize),
+# scan 2 (query split + grouping, scan), top-k 3 (sample, collect, finalize),
 # sparse MLA 3 (query split, attention, combine of cut units)
 KERNELS_PER_STEP = 8
+
+# DRAM bytes (read + write) per call of a stage, summed over its kernels, from
+# the ncu launch list in profiles/decode_step_launches_16x4_ctx32768.md (taken
+# on the current kernels; cold cache, so the combine's L2-resident partials
+# count as DRAM reads).  Stages and workloads not captured report null.
+NCU_STAGE_TRAFFIC = {
+    ("decode_16x4_ctx32768_h64", "indexer_scan"): 71.59e6,
+    ("decode_16x4_ctx32768_h64", "topk"): 10.82e6,
+    ("decode_16x4_ctx32768_h64", "sparse_mla"): 118.44e6,
+}
 
 
 def _peaks():
@@ -253,7 +263,8 @@ def run_gpu(args):
     achieved = dom_bytes / (stage_ms[dominant] * 1e-3) / 1e9
     roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1),
                 "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
-                "frac": round(achieved / hbm_peak, 4), "traffic": None,
+                "frac": round(achieved / hbm_peak, 4),
+                "traffic": NCU_STAGE_TRAFFIC.get((wl.name, dominant)),
                 "stage_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
                 "step_frac_of_8TBs": round(bytes_step / (ms_per_step * 1e-3) / 8e12, 4),
                 "step_frac_of_measured": round(bytes_step / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
