@@ -44,9 +44,9 @@ KERNELS_PER_STEP = 8
 # on the current kernels; cold cache, so the combine's L2-resident partials
 # count as DRAM reads).  Stages and workloads not captured report null.
 NCU_STAGE_TRAFFIC = {
-    ("decode_16x4_ctx32768_h64", "indexer_scan"): 71.59e6,
+    ("decode_16x4_ctx32768_h64", "indexer_scan"): 70.40e6,
     ("decode_16x4_ctx32768_h64", "topk"): 10.82e6,
-    ("decode_16x4_ctx32768_h64", "sparse_mla"): 118.44e6,
+    ("decode_16x4_ctx32768_h64", "sparse_mla"): 115.44e6,
 }
 
 
