@@ -50,6 +50,8 @@ SIGNATURES = [
     ("dsa_decode_step", I32, [P, I32, P, P, P, P, I64, F32, P, I32, I32, P, P, I32, P, I32, F32,
                               I32, P, P, P, P, SZ, P]),
     ("dsa_check_device_status", I32, [P, P, P]),
+    ("dsa_selftest_workspace_size", SZ, []),
+    ("dsa_selftest_bounded_wait", I32, [I32, P, SZ, P]),
 ]
 
 _lock = threading.Lock()
@@ -265,3 +267,22 @@ def check_device_status(workspace: torch.Tensor) -> int:
     if st not in (DSA_OK, DSA_ERR_DEVICE_CHECK):
         _check("dsa_check_device_status", st)
     return int(bits.value)
+
+
+def selftest_workspace_size() -> int:
+    return int(load().dsa_selftest_workspace_size())
+
+
+def selftest_bounded_wait(wait_us: int, workspace: torch.Tensor) -> None:
+    """Enqueue the library's bounded-wait self-test on the current stream.
+
+    One CTA waits ``wait_us`` microseconds on a barrier nothing arrives on,
+    raises the timeout bit in ``workspace``'s status word, drains its bulk copy
+    of ``workspace[256:512]`` into ``workspace[512:768]`` and frees its tensor
+    memory.  Read the result with :func:`check_device_status`.
+    """
+    _need(workspace, "workspace", torch.uint8)
+    if workspace.device.type != "cuda":
+        raise ValueError("workspace must be CUDA device memory")
+    _check("dsa_selftest_bounded_wait", load().dsa_selftest_bounded_wait(
+        int(wait_us), _ptr(workspace), workspace.numel(), _stream(workspace.device)))

@@ -273,6 +273,21 @@ int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const 
   return to_status(launch_sparse_mla(ma, st));
 }
 
+size_t dsa_selftest_workspace_size(void) { return selftest_workspace_bytes(); }
+
+int dsa_selftest_bounded_wait(int wait_us, void* workspace, size_t ws_bytes, void* stream) {
+  if (wait_us < 1 || wait_us > 1000000) return DSA_ERR_INVALID_ARG;
+  int s = check_workspace(workspace, ws_bytes, selftest_workspace_bytes());
+  if (s) return s;
+  int dev = 0, khz = 0;
+  if ((s = to_status(cudaGetDevice(&dev)))) return s;
+  if ((s = to_status(cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev)))) return s;
+  cudaStream_t st = as_stream(stream);
+  if ((s = clear_status(workspace, st))) return s;
+  const long long cycles = (long long)wait_us * (khz > 0 ? khz : 2000000) / 1000;
+  return to_status(launch_selftest_wait(workspace, cycles, st));
+}
+
 int dsa_check_device_status(const void* workspace, void* stream, uint32_t* bits) {
   if (!workspace) return DSA_ERR_WORKSPACE;
   uint32_t v = 0;

@@ -149,6 +149,12 @@ struct MlaArgs {
 };
 cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t st);
 
+// Library self-test: one CTA whose bounded wait on a barrier that nothing
+// arrives on runs out after `limit_cycles` SM cycles (workspace layout in
+// selftest.cu, selftest_workspace_bytes() bytes).
+cudaError_t launch_selftest_wait(void* workspace, long long limit_cycles, cudaStream_t st);
+size_t selftest_workspace_bytes();
+
 // Tiled TMA descriptor over a byte tensor of the given rank: dims[0] is the
 // contiguous extent, strides[i] the byte stride of dim i + 1, box the tile
 // copied per load; 128-byte swizzle, out-of-range elements read as zero.

@@ -224,6 +224,28 @@ int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const 
  * DSA_ERR_DEVICE_CHECK when one is, DSA_ERR_CUDA when the copy fails. */
 int dsa_check_device_status(const void* workspace, void* stream, uint32_t* bits);
 
+/* ------------------------------------------------------------------------
+ * dsa_selftest_bounded_wait -- library self-test of failure detection.
+ *
+ * The pipeline kernels bound every wait on an mbarrier (about 2 s); when one
+ * runs out the kernel raises DSA_DEV_TIMEOUT, waits for the copies it issued,
+ * frees its tensor memory and returns, leaving the stream and the context
+ * usable.  This call takes that path on purpose: it launches one CTA that
+ * holds 32 TMEM columns, has a 256-byte bulk copy in flight and waits on an
+ * mbarrier that nothing arrives on, with a limit of `wait_us` microseconds
+ * (1..1000000, converted with the device's peak SM clock).  Once the stream
+ * has run it, dsa_check_device_status reports DSA_DEV_TIMEOUT, and bytes
+ * [512,768) of the workspace hold a copy of bytes [256,512) (the bulk copy,
+ * drained after the failed wait).
+ *  workspace >= dsa_selftest_workspace_size() bytes, 256-byte aligned:
+ *             [0,256) status word, [256,512) copy source (any contents,
+ *             caller-owned), [512,768) the kernel's copy of it.
+ * Returns DSA_OK once enqueued; DSA_ERR_INVALID_ARG (wait_us out of range),
+ * DSA_ERR_WORKSPACE, DSA_ERR_CUDA.
+ * ------------------------------------------------------------------------ */
+size_t dsa_selftest_workspace_size(void);
+int dsa_selftest_bounded_wait(int wait_us, void* workspace, size_t ws_bytes, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

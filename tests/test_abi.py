@@ -95,6 +95,15 @@ def test_mla_and_step_reject_bad_shapes(lib):
                                  100, FAKE, 1 << 20, None) == 1   # ld < max_pages * 64
 
 
+def test_selftest_rejects_bad_arguments(lib):
+    need = lib.dsa_selftest_workspace_size()
+    assert need >= 768
+    assert lib.dsa_selftest_bounded_wait(0, FAKE, need, None) == 1          # wait_us < 1
+    assert lib.dsa_selftest_bounded_wait(2_000_000, FAKE, need, None) == 1  # > 1 s
+    assert lib.dsa_selftest_bounded_wait(100, None, need, None) == 3
+    assert lib.dsa_selftest_bounded_wait(100, FAKE, need - 1, None) == 3
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     from dsa_sparse_attention_lightning_gb300 import _lib
     monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -255,6 +255,37 @@ def test_device_checks_flag_bad_values(dsa):
     assert dsa.check_device_status(ws) == 0
 
 
+def test_bounded_wait_runs_out_and_context_stays_usable(dsa):
+    """A wait that nothing satisfies ends in the timeout bit, not a hang: the
+    self-test CTA gives up after its 2 ms limit, drains the bulk copy it had in
+    flight, frees its tensor memory and returns; later launches on the same
+    context run normally."""
+    import time
+    ws = torch.zeros(dsa.selftest_workspace_size(), dtype=torch.uint8, device=DEV)
+    pattern = ((torch.arange(256, device=DEV) * 7 + 3) % 251).to(torch.uint8)
+    ws[256:512] = pattern
+    for _ in range(2):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dsa.selftest_bounded_wait(2000, ws)
+        bits = dsa.check_device_status(ws)
+        dt = time.perf_counter() - t0
+        assert bits == 0x8
+        assert torch.equal(ws[512:768], pattern)
+        assert 1.5e-3 <= dt < 1.0
+        ws[512:768] = 0
+    wl = inputs.Workload("after_timeout", [900], [2], H=16, k=64, seed=14)
+    inp = inputs.make_inputs(wl, device=DEV)
+    wss = torch.empty(dsa.decode_step_workspace_size(1, 2, wl.max_pages, 16, 64),
+                      dtype=torch.uint8, device=DEV)
+    out, lse = dsa.dsa_decode_step(inp["q_idx"], inp["w"], inp["key_cache"], inp["latent_cache"],
+                                   inp["latent_scale"], inp["block_table"], inp["row_req"],
+                                   inp["row_len"], inp["q"], softmax_scale=inp["softmax_scale"],
+                                   k=64, workspace=wss)
+    assert dsa.check_device_status(wss) == 0
+    assert torch.isfinite(out.float()).all() and torch.isfinite(lse).all()
+
+
 # ----------------------------------------------- full benchmark sizes, sampled
 FULL = [1, 2, 3]
 
