@@ -29,15 +29,15 @@
 //  * Each TMEM lane holds one token's (row, head) logits, so the
 //    ReLU-weighted head sum is a per-thread loop: no shuffles.
 //  * Persistent CTAs, one per SM, each taking a contiguous run of (group,
-//    tile) work items; warp roles: 0 MMA issuer and TMEM owner, 1-4 TMA
-//    producers (keys, key scales, group queries; page ids looked up 32 tiles
-//    ahead; tile i is loaded by producer i % 2 -- TMA loads issued from one
-//    thread complete at about half the HBM rate, so each SM runs two
-//    streams), 3-18 epilogue in two groups of eight that take alternate
-//    tiles (TMEM -> scores; a warp takes TMEM lane quarter w % 4, i.e. 32
-//    tokens, of two of the group's rows).  A key stage is released by the
-//    MMA's completion alone; the key scales live in their own ring, held
-//    until the epilogue has used them.
+//    tile) work items; warp roles: 0-1 MMA issuers (tile i by warp i % 2;
+//    warp 0 owns TMEM), 2-3 TMA producers (keys, key scales, group queries;
+//    page ids looked up 32 tiles ahead; tile i is loaded by producer i % 2
+//    -- TMA loads issued from one thread complete at about half the HBM
+//    rate, so each SM runs two streams), 4-19 epilogue in two groups of
+//    eight that take alternate tiles (TMEM -> scores; a warp takes TMEM
+//    lane quarter w % 4, i.e. 32 tokens, of two of the group's rows).  A key
+//    stage is released by the MMA's completion alone; the key scales live in
+//    their own ring, held until the epilogue has used them.
 #include <limits.h>
 #include <math.h>
 
@@ -59,17 +59,20 @@ constexpr int kKeyTileBytes = kTileTok * kIdxDim;       // 2 pages x 64 x 128 B
 constexpr int kPageKeyBytes = kPage * kIdxDim;          // 8192
 constexpr int kPageBytes = kPage * (kIdxDim + 4);       // 8448: keys, then 64 f32 scales
 constexpr int kScRing = 16;                             // key-scale slots (outlive their key stage)
-constexpr int kProdWarps = 2;                           // warps 1-2: one TMA stream per warp
-constexpr int kEpiWarp0 = 1 + kProdWarps;               // warps 3-18
+constexpr int kMmaWarps = 2;                            // warps 0-1: lane 0 issues tiles i % 2 == warp
+constexpr int kProdWarps = 2;                           // warps 2-3: one TMA stream per warp
+constexpr int kEpiWarp0 = kMmaWarps + kProdWarps;       // warps 4-19
 constexpr int kEpiGroups = 2;                           // epilogue group g takes tiles i % 2 == g
 constexpr int kEpiWarpsPerGroup = 8;
 constexpr int kEpiWarps = kEpiGroups * kEpiWarpsPerGroup;
 constexpr int kEpiRows = kMaxGroupRows * 4 / kEpiWarpsPerGroup;  // group rows per epilogue warp
 static_assert(kStages % kProdWarps == 0, "a stage always belongs to the same producer");
+static_assert(kStages % kMmaWarps == 0, "a stage is always released by the same MMA issuer");
 static_assert(kScRing % kProdWarps == 0 && kScRing % kEpiGroups == 0, "fixed slot owners");
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
 constexpr int kDBufs = 4;
 static_assert(kDBufs % kEpiGroups == 0, "a TMEM accumulator always belongs to the same group");
+static_assert(kDBufs % kMmaWarps == 0 && kEpiGroups == kMmaWarps, "one epilogue group per MMA issuer");
 constexpr int kDCols = kMaxGroupRows * kIdxHeads;       // 128 f32 columns per accumulator
 constexpr uint32_t kTmemCols = kDCols * kDBufs;
 
@@ -82,7 +85,7 @@ constexpr int kOffW = (kOffPv + kScRing * 4 + 15) / 16 * 16;       // [kEpiWarps
 constexpr int kOffBar = (kOffW + kEpiWarps * kEpiRows * kIdxHeads * 4 + 7) / 8 * 8;
 static_assert(kOffKeys % 1024 == 0 && kKeyTileBytes % 1024 == 0, "swizzled TMA tiles need 1024-byte alignment");
 static_assert(kOffScale % 16 == 0 && kOffW % 16 == 0 && kOffBar % 8 == 0, "vector and mbarrier alignment");
-constexpr int kNumBars = 2 * kStages + 2 * kScRing + 2 * kDBufs + 2 * kQBufs + 1;
+constexpr int kNumBars = 2 * kStages + 2 * kScRing + 2 * kDBufs + 2 * kQBufs + kMmaWarps;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffTmem + 16;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
@@ -364,7 +367,7 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
   uint64_t* d_empty = d_full + kDBufs;              // [kDBufs]
   uint64_t* q_full = d_empty + kDBufs;              // [kQBufs]
   uint64_t* q_empty = q_full + kQBufs;              // [kQBufs]
-  uint64_t* mma_done = q_empty + kQBufs;            // every issued MMA finished
+  uint64_t* mma_done = q_empty + kQBufs;            // [kMmaWarps] every MMA of an issuer finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
   const float* scale_s = reinterpret_cast<const float*>(smem + kOffScale);
   uint32_t* pv_s = reinterpret_cast<uint32_t*>(smem + kOffPv);
@@ -385,9 +388,9 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
     }
     for (int b = 0; b < kQBufs; ++b) {
       mbar_init(&q_full[b], 1);
-      mbar_init(&q_empty[b], 1);
+      mbar_init(&q_empty[b], kMmaWarps);            // one release per MMA issuer
     }
-    mbar_init(mma_done, 1);
+    for (int m = 0; m < kMmaWarps; ++m) mbar_init(&mma_done[m], 1);
     fence_mbar_init();
   }
   if (warp == 0) {
@@ -410,55 +413,68 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
   cur.ngroups = ngroups;
   if (ntiles > 0) cur.seek(t_begin);
 
-  if (ntiles > 0 && warp == 0) {
-    // ---------------- MMA issuer: lane 0 alone walks the tiles and issues
+  if (ntiles > 0 && warp < kMmaWarps) {
+    // ---------------- MMA issuers: lane 0 of warp m issues the tiles i with
+    // i % kMmaWarps == m.  An issuing thread is held at every tcgen05.mma
+    // until the tensor core takes it, and its barrier waits and commits cost
+    // about as much again per tile; with two issuers one thread's
+    // bookkeeping overlaps the other's MMAs.  Both walk every tile to follow
+    // the group, stage and accumulator sequence.
     if (lane == 0) {
+      const int m = warp;
       int cur_group = -1, gi = -1, left = 0;          // tiles left in the current group
+      bool issued_in_group = false;
       uint32_t idesc = 0;
       uint64_t b_desc = 0;
       const uint64_t a_desc_base = desc_kmajor_sw128(smem_u32(smem + kOffKeys));
       int s = 0;                                      // key stage of tile i
       uint32_t s_phase = 0;
-      bool ok = true;
-      for (int i = 0; i < ntiles && ok; ++i) {
+      for (int i = 0; i < ntiles; ++i) {
         if (cur.g != cur_group) {
           cur_group = cur.g;
           ++gi;
           left = (cur.ge - cur.gs) - cur.t;
+          issued_in_group = false;
           idesc = idesc_e4m3_f32(kTileTok, kIdxHeads * cur.G.y, false, false);
           b_desc = desc_kmajor_sw128(smem_u32(smem + kOffQ + (gi % kQBufs) * kQBytes));
           if (!mbar_wait(&q_full[gi % kQBufs], (uint32_t)(gi / kQBufs) & 1, status)) break;
         }
-        const int db = i % kDBufs;
-        if (!mbar_wait(&full[s], s_phase, status)) break;
-        if (!mbar_wait(&d_empty[db], ((uint32_t)(i / kDBufs) & 1) ^ 1, status)) break;
-        tc_fence_after();
-        const uint64_t a_desc = a_desc_base + (uint64_t)((s * kKeyTileBytes) >> 4);
-        const uint32_t d_tmem = tmem_base + (uint32_t)(db * kDCols);
+        if (i % kMmaWarps == m) {
+          const int db = i % kDBufs;
+          if (!mbar_wait(&full[s], s_phase, status)) break;
+          if (!mbar_wait(&d_empty[db], ((uint32_t)(i / kDBufs) & 1) ^ 1, status)) break;
+          tc_fence_after();
+          const uint64_t a_desc = a_desc_base + (uint64_t)((s * kKeyTileBytes) >> 4);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(db * kDCols);
 #pragma unroll
-        for (int j = 0; j < 2 * kIdxDim / 32; ++j)    // K = 2 x 128 bytes in steps of 32
-          mma_e4m3_ss(d_tmem, a_desc + (uint64_t)((j & 3) * 2),
-                      b_desc + (uint64_t)(((j >> 2) * kQAtom + (j & 3) * 32) >> 4), idesc,
-                      j > 0 ? 1u : 0u);
-        mma_commit(&empty[s]);
-        mma_commit(&d_full[db]);
+          for (int j = 0; j < 2 * kIdxDim / 32; ++j)  // K = 2 x 128 bytes in steps of 32
+            mma_e4m3_ss(d_tmem, a_desc + (uint64_t)((j & 3) * 2),
+                        b_desc + (uint64_t)(((j >> 2) * kQAtom + (j & 3) * 32) >> 4), idesc,
+                        j > 0 ? 1u : 0u);
+          mma_commit(&empty[s]);
+          mma_commit(&d_full[db]);
+          issued_in_group = true;
+        }
         --left;
-        if (i + 1 == ntiles || left == 0) mma_commit(&q_empty[gi % kQBufs]);
+        if (i + 1 == ntiles || left == 0) {           // the group's query operand is released
+          if (issued_in_group) mma_commit(&q_empty[gi % kQBufs]);
+          else mbar_arrive(&q_empty[gi % kQBufs]);
+        }
         if (++s == kStages) {
           s = 0;
           s_phase ^= 1u;
         }
         if (left == 0 && i + 1 < ntiles) cur.advance(cur.ge - cur.gs - cur.t);   // next group
       }
-      mma_commit(mma_done);                           // tensor memory is freed only after this
-      mbar_wait(mma_done, 0, status);
+      mma_commit(&mma_done[m]);                       // tensor memory is freed only after this
+      mbar_wait(&mma_done[m], 0, status);
     }
     __syncwarp();
-  } else if (ntiles > 0 && warp >= 1 && warp <= kProdWarps) {
-    // ---------------- TMA producers: warp 1 + p loads the tiles i with
+  } else if (ntiles > 0 && warp >= kMmaWarps && warp < kEpiWarp0) {
+    // ---------------- TMA producers: warp kMmaWarps + p loads the tiles i with
     // i % kProdWarps == p.  Page ids are looked up a batch of 32 tiles ahead:
     // lane j holds the pages of tile (batch start + j).
-    const int pw = warp - 1;
+    const int pw = warp - kMmaWarps;
     auto fetch = [&](const TileCursor& b0, int i0) {
       TilePages tp{0, 0, false, false};
       if (i0 + lane < ntiles) {
