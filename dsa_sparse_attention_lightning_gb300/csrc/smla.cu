@@ -135,16 +135,19 @@ mla_qprep_kernel(const __nv_bfloat16* __restrict__ q, int R, int H, float softma
 }
 
 // ---------------------------------------------------------------------------
-// Warp roles (512 threads): warp 0 issues the MMAs and owns tensor memory;
-// warps 1-7 gather latent rows with TMA (double-buffered; 160 gather4 loads per
-// tile spread one per lane, since one warp's loads issue one lane at a time);
-// warps 8-15 run the softmax and the epilogues: warp w reads TMEM lane quarter
-// (w & 3) and token half (w - 8) / 4 of S.
+// Warp roles (512 threads): warp 0 issues the score MMAs and owns tensor
+// memory, warp 1 issues the P.V MMAs (a thread is held at every tcgen05.mma
+// until the tensor core takes it, so two issuers keep S of one tile and P.V of
+// the previous one both fed); warps 2-7 gather latent rows with TMA
+// (double-buffered; 160 gather4 loads per tile spread one per lane, since one
+// warp's loads issue one lane at a time); warps 8-15 run the softmax and the
+// epilogues: warp w reads TMEM lane quarter (w & 3) and token half (w - 8) / 4
+// of S.
 constexpr int kThreads = 512;
-constexpr int kGatherLanes = 23;                       // 7 x 23 >= 160 loads per tile
+constexpr int kGatherWarp0 = 2;
+constexpr int kGatherLanes = 27;                       // 6 x 27 >= 160 loads per tile
 constexpr int kSmWarp0 = 8;                            // first softmax warp
 constexpr int kSmThreads = 256;
-constexpr uint32_t kPollNs = 128;                      // MMA warp's suspend limit per probe
 constexpr int kTileBytes = kLatAtoms * kAtom;          // one latent buffer
 constexpr uint32_t kQCol = 0;                          // A operand: Q (dims 0..511), 128 cols
 constexpr uint32_t kSCol = 128;                        // S: [(head, term)] x [128 tokens]
@@ -159,8 +162,8 @@ struct MlaSmem {
   static constexpr int red = corr + 64 * 4;                          // [2 halves][64] f32
   static constexpr int lsum = red + 2 * 64 * 4;                      // [2 halves][64] f32
   static constexpr int flag = lsum + 2 * 64 * 4;                     // [2] int
-  static constexpr int bar = (flag + 8 + 7) / 8 * 8;                 // 9 mbarriers
-  static constexpr int tmem = bar + 9 * 8;
+  static constexpr int bar = (flag + 8 + 7) / 8 * 8;                 // 10 mbarriers
+  static constexpr int tmem = bar + 10 * 8;
   static constexpr int bytes = tmem + 16;
   static constexpr int alloc = bytes + 1024;
 };
@@ -235,7 +238,7 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
   uint64_t* s_empty = bars + 5;       // S read (and Q in place) for the next score MMA
   uint64_t* p_full = bars + 6;        // P in shared memory, O rescaled
   uint64_t* p_empty = bars + 7;       // P.V finished (O complete up to this tile)
-  uint64_t* mma_done = bars + 8;      // every issued MMA finished
+  uint64_t* mma_done = bars + 8;      // [2] every MMA of an issuer finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem);
 
   const int groups = H / HG;
@@ -257,7 +260,8 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
     mbar_init(s_empty, 8);
     mbar_init(p_full, 8);
     mbar_init(p_empty, 1);
-    mbar_init(mma_done, 1);
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
     fence_mbar_init();
     flag_s[0] = 0;
     flag_s[1] = 0;
@@ -274,9 +278,9 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
   const uint32_t idesc_s = idesc_e4m3_f32(kMlaTile, kMlaTile, false, false);
   const uint32_t idesc_o = idesc_e4m3_f32(kMlaTile, HG, true, false);
 
-  if (warp == 0) {
-    // ================= MMA issuer: S(i) once tile i has landed and S(i - 1)
-    // has been read; O(i) once P(i) is in place -- whichever is ready first
+  if (warp < kGatherWarp0) {
+    // ================= MMA issuers: warp 0 issues S(i) once tile i has landed
+    // and S(i - 1) has been read; warp 1 issues O(i) once P(i) is in place
     auto issue_s = [&](int i) {
       const uint32_t lb = smem_u32(lat + (i & 1) * kTileBytes);
 #pragma unroll
@@ -308,42 +312,29 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
       mma_commit(&lat_empty[i & 1]);
     };
     if (lane == 0 && n > 0) {
-      int si = 0, oi = 0;
-      TileIt ot = it0;                                // tile of the next O
-      long long t_last = clock64();
-      while (oi < n) {
-        bool prog = false;
-        // probes sleep in hardware (a busy poll would steal the shared-memory
-        // pipe from the softmax warps)
-        if (si < n && si <= oi + 1 &&
-            mbar_try_wait_ns(&lat_full[si & 1], (uint32_t)(si >> 1) & 1, kPollNs) &&
-            mbar_try_wait_ns(s_empty, (uint32_t)si & 1, kPollNs)) {
+      if (warp == 0) {
+        for (int si = 0; si < n; ++si) {
+          if (!mbar_wait(&lat_full[si & 1], (uint32_t)(si >> 1) & 1, status)) break;
+          if (!mbar_wait(s_empty, (uint32_t)si & 1, status)) break;
           tc_fence_after();
           issue_s(si);
-          ++si;
-          prog = true;
         }
-        if (oi < si && mbar_try_wait_ns(p_full, (uint32_t)oi & 1, kPollNs)) {
+      } else {
+        TileIt ot = it0;                              // tile of the next O
+        for (int oi = 0; oi < n; ++oi) {
+          if (!mbar_wait(p_full, (uint32_t)oi & 1, status)) break;
           tc_fence_after();
           issue_o(oi, ot.first());
           ot.next(NT);
-          ++oi;
-          prog = true;
-        }
-        if (prog) {
-          t_last = clock64();
-        } else if (clock64() - t_last > kWaitCycles) {
-          raise_dev(status, DSA_DEV_TIMEOUT);
-          break;
         }
       }
-      mma_commit(mma_done);                           // tensor memory is freed only after this
-      mbar_wait(mma_done, 0, status);
+      mma_commit(&mma_done[warp]);                    // tensor memory is freed only after this
+      mbar_wait(&mma_done[warp], 0, status);
     }
     __syncwarp();
   } else if (warp < kSmWarp0) {
     // ================= TMA gather: lane op = (group g of 4 tile rows, box a of 5)
-    const int op = (warp - 1) * kGatherLanes + lane;
+    const int op = (warp - kGatherWarp0) * kGatherLanes + lane;
     const bool op_ok = lane < kGatherLanes && op < 32 * kLatAtoms;
     const int g = op & 31, a = op >> 5;
     int y[4] = {-1, -1, -1, -1};
@@ -383,7 +374,7 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
       if (!wwait(&lat_empty[b], ((uint32_t)(i >> 1) & 1) ^ 1, status)) break;
       // complete_tx of other warps may land before this arrive: the phase
       // cannot complete until the single arrival has come
-      if (warp == 1 && lane == 0) mbar_arrive_expect_tx(&lat_full[b], kTileBytes);
+      if (warp == kGatherWarp0 && lane == 0) mbar_arrive_expect_tx(&lat_full[b], kTileBytes);
       if (op_ok) {
         tma_gather4(lat + b * kTileBytes + a * kAtom + g * 512, &lat_map, a * 128, y[0], y[1],
                     y[2], y[3], &lat_full[b]);
@@ -391,7 +382,7 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
       }
     }
     // no copy may still be landing in shared memory when the CTA exits
-    if (warp == 1 && n > 0) {
+    if (warp == kGatherWarp0 && n > 0) {
       const int last = n - 1;
       wwait(&lat_full[last & 1], (uint32_t)(last >> 1) & 1, status);
       if (n > 1) wwait(&lat_full[(last - 1) & 1], (uint32_t)((last - 1) >> 1) & 1, status);

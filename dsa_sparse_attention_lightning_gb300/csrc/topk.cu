@@ -98,11 +98,18 @@ __device__ __forceinline__ bool row_ok(int len, int64_t max_len) {
   return len >= 0 && (int64_t)len <= max_len;
 }
 
-// Shared-memory histogram add; lanes that fall in the same bin add once.
-// All 32 lanes of the warp call it.
+// Shared-memory histogram add; all 32 lanes of the warp call it.  The keys of
+// a row crowd into a few high-order bins, so the lanes that share the first
+// valid lane's bin add once through it (two ballots and a shuffle, cheaper
+// than a full match), and the others add one each.
 __device__ __forceinline__ void hist_add(uint32_t* h, uint32_t bin, bool valid) {
-  const unsigned m = __match_any_sync(0xffffffffu, valid ? bin : 0xFFFFFFFFu);
-  if (valid && (threadIdx.x & 31) == __ffs(m) - 1) atomicAdd(&h[bin], (uint32_t)__popc(m));
+  const unsigned vm = __ballot_sync(0xffffffffu, valid);
+  if (vm == 0u) return;
+  const int leader = __ffs(vm) - 1;
+  const uint32_t lb = __shfl_sync(0xffffffffu, bin, leader);
+  const unsigned same = __ballot_sync(0xffffffffu, valid && bin == lb);
+  if ((int)(threadIdx.x & 31) == leader) atomicAdd(&h[lb], (uint32_t)__popc(same));
+  else if (valid && bin != lb) atomicAdd(&h[bin], 1u);
 }
 
 // ---- 1. threshold from a fixed sample ----------------------------------------
@@ -349,12 +356,15 @@ topk_finalize_kernel(const float* __restrict__ scores, int64_t ld,
     const uint2* rr = runs + (size_t)r * nchunks;
     const uint32_t i0 = threadIdx.x * kCandPer;
     uint8_t f[kCandPer];
-    // ties: rank by position = ties in earlier chunks + ties earlier in the run
+    const bool all_ties = need_eq == n_eq;           // every key equal to T is kept
+    if (!all_ties) {
+      // ties: rank by position = ties in earlier chunks + ties earlier in the run
 #pragma unroll
-    for (int u = 0; u < kCandPer; ++u) f[u] = (i0 + u < n && C.cand[i0 + u].x == T) ? 1 : 0;
-    scan_flags(f, C.ex_tie, n, S);
-    scan_chunks([&](int c) { const uint2 q = rr[c]; return (uint32_t)(C.ex_tie[q.x + q.y] - C.ex_tie[q.x]); },
-                nch, C.base_tie, S);
+      for (int u = 0; u < kCandPer; ++u) f[u] = (i0 + u < n && C.cand[i0 + u].x == T) ? 1 : 0;
+      scan_flags(f, C.ex_tie, n, S);
+      scan_chunks([&](int c) { const uint2 q = rr[c]; return (uint32_t)(C.ex_tie[q.x + q.y] - C.ex_tie[q.x]); },
+                  nch, C.base_tie, S);
+    }
     // kept: key > T, or a tie of rank < need_eq
 #pragma unroll
     for (int u = 0; u < kCandPer; ++u) {
@@ -362,7 +372,7 @@ topk_finalize_kernel(const float* __restrict__ scores, int64_t ld,
       uint8_t keep = 0;
       if (i < n) {
         const uint2 v = C.cand[i];
-        if (v.x > T) {
+        if (v.x > T || (all_ties && v.x == T)) {
           keep = 1;
         } else if (v.x == T) {
           const uint2 q = rr[v.y / kTopkChunk];
@@ -382,7 +392,6 @@ topk_finalize_kernel(const float* __restrict__ scores, int64_t ld,
       const uint32_t o = C.base_sel[c] + C.ex_sel[i0 + u] - C.ex_sel[rr[c].x];
       if (o < (uint32_t)k) out[o] = (int32_t)v.y;
     }
-    (void)n_eq;
   } else {
     // ---- the whole row, in position order
     const float* row = scores + (size_t)r * ld;
