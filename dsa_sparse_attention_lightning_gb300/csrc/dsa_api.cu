@@ -265,11 +265,11 @@ int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const 
               row_req, row_len, R, scores, ld, ws + L.scan, status};
   cudaError_t e = launch_indexer_scan(sa, st);
   if (e != cudaSuccess) return to_status(e);
-  TopkArgs ta{scores, ld, row_len, R, ld, k, idx, ws + L.topk, status};
+  TopkArgs ta{scores, ld, row_len, R, ld, k, idx, ws + L.topk, status, true};
   e = launch_topk(ta, st);
   if (e != cudaSuccess) return to_status(e);
   MlaArgs ma{q, H, softmax_scale, latent_cache, num_pages, latent_scale, block_table, B,
-             max_pages, row_req, row_len, idx, k, R, out, lse, ws + L.mla, status};
+             max_pages, row_req, row_len, idx, k, R, out, lse, ws + L.mla, status, true};
   return to_status(launch_sparse_mla(ma, st));
 }
 

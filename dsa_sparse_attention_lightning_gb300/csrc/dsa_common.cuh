@@ -93,6 +93,43 @@ struct MlaLayout {
   }
 };
 
+// ---- programmatic dependent launch ---------------------------------------
+// The kernels of one call run back to back on a stream.  Each but the first
+// is launched with programmatic stream serialization: it may be scheduled as
+// soon as every CTA of the kernel before it has called pdl_trigger(), so its
+// prologue (barrier set-up, tensor-memory allocation, descriptor prefetch)
+// overlaps that kernel's tail and the launch gap disappears.  Every CTA of
+// every kernel calls pdl_wait() -- which returns once the kernel before it
+// has completed and its writes are visible -- before it reads anything an
+// earlier kernel wrote, and before it exits, so that the completion of a
+// kernel still implies the completion of all kernels before it.  A kernel
+// that allocates tensor memory triggers only after its allocation: a
+// dependent CTA placed on the same SM then cannot take the columns first and
+// wait on a kernel that waits for them.  Launched without the attribute,
+// both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launches `kernel` on `st`; `chained` = may overlap the previous kernel on
+// the stream (it must follow the pdl_wait() rule above).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t st, bool chained, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = chained ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- device helpers ----------------------------------------------------
 __device__ __forceinline__ void raise_dev(uint32_t* status, uint32_t bit) {
   if (status) atomicOr(status, bit);
@@ -137,6 +174,7 @@ struct TopkArgs {
   const float* scores; int64_t ld; const int32_t* row_len; int R; int64_t max_len; int k;
   int32_t* idx; uint8_t* scratch;  // TopkLayout(R, max_len).bytes bytes
   uint32_t* status;
+  bool chained = false;   // the first kernel may overlap the previous one on the stream
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st);
 
@@ -146,6 +184,7 @@ struct MlaArgs {
   const int32_t* row_len; const int32_t* idx; int k; int R; void* out; float* lse;
   uint8_t* scratch;  // MlaLayout(R, H, k).bytes bytes
   uint32_t* status;
+  bool chained = false;   // the first kernel may overlap the previous one on the stream
 };
 cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t st);
 

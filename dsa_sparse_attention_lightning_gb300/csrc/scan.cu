@@ -160,6 +160,8 @@ scan_prep_kernel(const void* __restrict__ q_idx, int q_dtype, const float* __res
                  const float* __restrict__ w, const int32_t* __restrict__ row_req,
                  const int32_t* __restrict__ row_len, int R, int B, int max_pages, ScanWs ws,
                  uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   if (blockIdx.x == (unsigned)R) {
     __shared__ int warp_buf[32];
     __shared__ int s_carry[3];   // run start of the last row, groups so far, tiles so far
@@ -401,6 +403,8 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();                                    // after the tensor-memory allocation
+  pdl_wait();                                       // the prep kernel's groups and query terms
 
   const int ngroups = ws.meta[0];
   const int total = ws.meta[1];
@@ -666,9 +670,10 @@ cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   scan_prep_kernel<<<a.R + 1, kPrepThreads, 0, st>>>(a.q_idx, a.q_dtype, a.q_scale, a.w, a.row_req,
                                              a.row_len, a.R, a.B, a.max_pages, ws, a.status);
-  scan_kernel<<<sms, kThreads, kSmemAlloc, st>>>(kmap, qmap, a.key_cache, a.num_pages,
-                                                 a.block_table, a.max_pages, a.row_len, a.scores,
-                                                 a.ld, a.R, ws, a.status);
+  e = launch_kernel(scan_kernel, dim3(sms), dim3(kThreads), kSmemAlloc, st, true, kmap, qmap,
+                    a.key_cache, a.num_pages, a.block_table, a.max_pages, a.row_len, a.scores,
+                    a.ld, a.R, ws, a.status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

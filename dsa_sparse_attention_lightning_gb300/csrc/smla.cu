@@ -108,8 +108,14 @@ __device__ __forceinline__ uint8_t f32_to_e4m3(float x) {
 __global__ void __launch_bounds__(256)
 mla_qprep_kernel(const __nv_bfloat16* __restrict__ q, int R, int H, float softmax_scale,
                  float latent_scale, uint8_t* __restrict__ q8, float* __restrict__ qc) {
+  // reads only the caller's query: runs alongside the kernel before it, and
+  // completes after it (pdl_wait at the end)
+  pdl_trigger();
   const int w = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (w >= R * H) return;
+  if (w >= R * H) {
+    pdl_wait();
+    return;
+  }
   const __nv_bfloat16* src = q + (size_t)w * kLatDim;
   float x[kLatDim / 32];
   float amax = 0.f;
@@ -132,6 +138,7 @@ mla_qprep_kernel(const __nv_bfloat16* __restrict__ q, int R, int H, float softma
     lo[i * 32 + lane] = f32_to_e4m3(r * 32.f);
   }
   if (lane == 0) qc[w] = softmax_scale * latent_scale * kLog2e * ldexpf(1.f, -a);
+  pdl_wait();
 }
 
 // ---------------------------------------------------------------------------
@@ -274,6 +281,8 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_trigger();                                    // after the tensor-memory allocation
+  pdl_wait();                                       // query terms and selected indices
 
   const uint32_t idesc_s = idesc_e4m3_f32(kMlaTile, kMlaTile, false, false);
   const uint32_t idesc_o = idesc_e4m3_f32(kMlaTile, HG, true, false);
@@ -669,6 +678,8 @@ mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ p
   __shared__ float s_w[kCombHeads][kCombMaxSplits];  // weights e^{lse_s - M} / Z
   __shared__ int s_slot[kCombMaxSplits];
   __shared__ float s_lse[kCombHeads];
+  pdl_trigger();
+  pdl_wait();                                       // the partials
   const int hq = threadIdx.x >> 7, t = threadIdx.x & 127;
   const int h = blockIdx.x % (H / kCombHeads) * kCombHeads + hq;
   const int r = blockIdx.x / (H / kCombHeads);
@@ -758,11 +769,14 @@ cudaError_t launch_smla(const MlaArgs& a, const MlaLayout& L, int G, cudaStream_
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(smla_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::alloc);
   if (e != cudaSuccess) return e;
-  smla_kernel<HG><<<G, kThreads, S::alloc, st>>>(
-      map, a.scratch + L.q8, reinterpret_cast<const float*>(a.scratch + L.qc), a.H, a.num_pages,
-      a.latent_scale, a.block_table, a.B, a.max_pages, a.row_req, a.row_len, a.idx, a.k, a.R,
-      reinterpret_cast<float*>(a.scratch + L.part_o), reinterpret_cast<float*>(a.scratch + L.part_lse),
-      static_cast<__nv_bfloat16*>(a.out), a.lse, a.status);
+  e = launch_kernel(smla_kernel<HG>, dim3(G), dim3(kThreads), S::alloc, st, true, map,
+                    (const uint8_t*)(a.scratch + L.q8),
+                    reinterpret_cast<const float*>(a.scratch + L.qc), a.H, a.num_pages,
+                    a.latent_scale, a.block_table, a.B, a.max_pages, a.row_req, a.row_len, a.idx,
+                    a.k, a.R, reinterpret_cast<float*>(a.scratch + L.part_o),
+                    reinterpret_cast<float*>(a.scratch + L.part_lse),
+                    static_cast<__nv_bfloat16*>(a.out), a.lse, a.status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -774,19 +788,23 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t st) {
   const MlaWork w(a.R, a.H, a.k);
   if (w.G > 0) {
     const int warps = a.R * a.H;
-    mla_qprep_kernel<<<(warps + 7) / 8, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(a.q), a.R, a.H, a.softmax_scale, a.latent_scale,
-        a.scratch + L.q8, reinterpret_cast<float*>(a.scratch + L.qc));
-    cudaError_t e;
+    cudaError_t e = launch_kernel(mla_qprep_kernel, dim3((warps + 7) / 8), dim3(256), 0, st,
+                                  a.chained, static_cast<const __nv_bfloat16*>(a.q), a.R, a.H,
+                                  a.softmax_scale, a.latent_scale, a.scratch + L.q8,
+                                  reinterpret_cast<float*>(a.scratch + L.qc));
+    if (e != cudaSuccess) return e;
     if (a.H == 16) e = launch_smla<16>(a, L, w.G, st);
     else if (a.H == 32) e = launch_smla<32>(a, L, w.G, st);
     else e = launch_smla<64>(a, L, w.G, st);
     if (e != cudaSuccess) return e;
   }
-  mla_combine_kernel<<<a.R * a.H / kCombHeads, 128 * kCombHeads, 0, st>>>(reinterpret_cast<const float*>(a.scratch + L.part_o),
-                                                reinterpret_cast<const float*>(a.scratch + L.part_lse),
-                                                a.R, a.H, a.k, static_cast<__nv_bfloat16*>(a.out),
-                                                a.lse);
+  // chained after the main kernel, or (no slots at all) after the caller's work
+  cudaError_t e = launch_kernel(mla_combine_kernel, dim3(a.R * a.H / kCombHeads),
+                                dim3(128 * kCombHeads), 0, st, w.G > 0 || a.chained,
+                                reinterpret_cast<const float*>(a.scratch + L.part_o),
+                                reinterpret_cast<const float*>(a.scratch + L.part_lse), a.R, a.H,
+                                a.k, static_cast<__nv_bfloat16*>(a.out), a.lse);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

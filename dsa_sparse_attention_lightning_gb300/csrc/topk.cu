@@ -125,8 +125,11 @@ __device__ __forceinline__ int64_t sample_stride(int len) {
 
 __global__ void __launch_bounds__(kSampleThreads)
 topk_sample_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
-                   int64_t max_len, int k, uint32_t* __restrict__ tau) {
+                   int64_t max_len, int k, uint32_t* __restrict__ tau, uint32_t* __restrict__ cnt) {
+  pdl_trigger();
+  pdl_wait();                                  // the scores
   const int r = blockIdx.x;
+  if (threadIdx.x == 0) cnt[r] = 0;            // the collect kernel's candidate count
   const int len = row_len[r];
   if (!row_ok(len, max_len) || len <= k) return;
   __shared__ uint32_t h[kTopkBins1];
@@ -181,6 +184,8 @@ topk_collect_kernel(const float* __restrict__ scores, int64_t ld,
                     const int32_t* __restrict__ row_len, int64_t max_len, int k,
                     const uint32_t* __restrict__ tau, uint32_t* __restrict__ cnt,
                     uint2* __restrict__ runs, int nchunks, uint2* __restrict__ items) {
+  pdl_trigger();
+  pdl_wait();                                  // tau and the zeroed counts
   const int r = blockIdx.y;
   const int c = blockIdx.x;
   const int len = row_len[r];
@@ -332,6 +337,8 @@ topk_finalize_kernel(const float* __restrict__ scores, int64_t ld,
   extern __shared__ __align__(16) uint8_t fin_smem[];
   SelectSmem& S = *reinterpret_cast<SelectSmem*>(fin_smem);
   CandSmem& C = *reinterpret_cast<CandSmem*>(fin_smem + (sizeof(SelectSmem) + 15) / 16 * 16);
+  pdl_trigger();
+  pdl_wait();                                  // the candidate lists
   const int r = blockIdx.x;
   const int len = row_len[r];
   int32_t* out = idx + (size_t)r * k;
@@ -428,20 +435,21 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
   uint32_t* cnt = reinterpret_cast<uint32_t*>(a.scratch + L.cnt);
   uint2* runs = reinterpret_cast<uint2*>(a.scratch + L.runs);
   uint2* items = reinterpret_cast<uint2*>(a.scratch + L.items);
-  cudaError_t e = cudaMemsetAsync(cnt, 0, (size_t)a.R * 4, st);
-  if (e != cudaSuccess) return e;
-  topk_sample_kernel<<<a.R, kSampleThreads, 0, st>>>(a.scores, a.ld, a.row_len, a.max_len, a.k,
-                                                     tau);
-  dim3 grid(L.nchunks, a.R);
-  topk_collect_kernel<<<grid, kCollectThreads, 0, st>>>(a.scores, a.ld, a.row_len, a.max_len,
-                                                        a.k, tau, cnt, runs, L.nchunks, items);
   const size_t smem = (sizeof(SelectSmem) + 15) / 16 * 16 + sizeof(CandSmem);
-  e = cudaFuncSetAttribute(topk_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(topk_finalize_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  topk_finalize_kernel<<<a.R, kFinalThreads, smem, st>>>(a.scores, a.ld, a.row_len, a.max_len,
-                                                         a.k, cnt, runs, L.nchunks, items, a.idx,
-                                                         a.status);
+  e = launch_kernel(topk_sample_kernel, dim3(a.R), dim3(kSampleThreads), 0, st, a.chained,
+                    a.scores, a.ld, a.row_len, a.max_len, a.k, tau, cnt);
+  if (e != cudaSuccess) return e;
+  e = launch_kernel(topk_collect_kernel, dim3(L.nchunks, a.R), dim3(kCollectThreads), 0, st, true,
+                    a.scores, a.ld, a.row_len, a.max_len, a.k, (const uint32_t*)tau, cnt, runs,
+                    L.nchunks, items);
+  if (e != cudaSuccess) return e;
+  e = launch_kernel(topk_finalize_kernel, dim3(a.R), dim3(kFinalThreads), smem, st, true,
+                    a.scores, a.ld, a.row_len, a.max_len, a.k, (const uint32_t*)cnt,
+                    (const uint2*)runs, L.nchunks, (const uint2*)items, a.idx, a.status);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
