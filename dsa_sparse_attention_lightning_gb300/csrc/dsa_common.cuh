@@ -55,12 +55,14 @@ struct TopkLayout {
 
 // Sparse MLA works on tiles of 128 selected slots.  A unit is one query row
 // and one group of up to 64 heads; unit u = row * groups + group has
-// NT = ceil(k / 128) tiles.  The U * NT tiles are cut into G = min(152, U * NT)
-// contiguous ranges of near-equal length, one per CTA (one CTA per SM of a
-// 152-SM part); the cut is a fixed function of (R, H, k) so that results do
-// not depend on the device.  A CTA's range covers whole units (written
-// straight to the output) and at most two cut units, whose partials it leaves
-// in slots 2c (its first unit) and 2c + 1 (its last) for the combine.
+// NT = ceil(k / 128) tiles.  With fewer units than SMs (U < 152), each unit is
+// cut into S = min(152 / U, NT) near-equal parts, one CTA each (G = U * S);
+// otherwise the U * NT tiles are cut into G = min(152, U * NT) contiguous
+// ranges of near-equal length.  The cut is a fixed function of (R, H, k) so
+// that results do not depend on the device.  A CTA's range covers whole units
+// (written straight to the output) and at most two cut units, whose partials
+// it leaves in slots 2c (its first unit) and 2c + 1 (its last) for the
+// combine.
 constexpr int kMlaTile = 128;
 constexpr int kMlaGrid = 152;
 
@@ -69,14 +71,31 @@ __host__ __device__ inline int mla_heads_per_cta(int H) { return H < 64 ? H : 64
 struct MlaWork {
   int64_t U, NT, T;
   int G;
+  int S;   // > 0: each unit is split over S CTAs of its own; 0: one contiguous split of all tiles
   __host__ __device__ MlaWork(int R, int H, int k) {
     U = (int64_t)R * (H / mla_heads_per_cta(H));
     NT = (k + kMlaTile - 1) / kMlaTile;
     T = U * NT;
-    G = (int)(T < kMlaGrid ? T : kMlaGrid);
+    if (U > 0 && U < kMlaGrid) {
+      // fewer units than SMs: S equal parts per unit, so that no CTA holds the
+      // end of one unit and the start of the next (two output epilogues)
+      const int64_t sp = kMlaGrid / U;
+      S = (int)(sp < NT ? sp : NT);
+      G = (int)(U * S);
+    } else {
+      S = 0;
+      G = (int)(T < kMlaGrid ? T : kMlaGrid);
+    }
   }
-  __host__ __device__ int64_t begin(int64_t c) const { return c * T / G; }   // first tile of CTA c
-  __host__ __device__ int cta_of(int64_t t) const { return (int)(((t + 1) * G - 1) / T); }
+  __host__ __device__ int64_t begin(int64_t c) const {   // first tile of CTA c
+    if (S == 0) return c * T / G;
+    return (c / S) * NT + (c % S) * NT / S;
+  }
+  __host__ __device__ int cta_of(int64_t t) const {
+    if (S == 0) return (int)(((t + 1) * G - 1) / T);
+    const int64_t u = t / NT, lt = t - u * NT;
+    return (int)(u * S + ((lt + 1) * S - 1) / NT);
+  }
 };
 
 struct MlaLayout {
