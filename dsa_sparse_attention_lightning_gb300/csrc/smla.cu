@@ -663,28 +663,30 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
   }
 }
 
-// Merge of the partials of units cut by CTA ranges, by log-sum-exp.  A CTA
-// takes kCombHeads heads of one unit (128 threads per head, 4 dims each): the
-// partial lse values of all its splits are loaded at once into shared memory,
-// then every thread accumulates its dims over the splits with independent
-// loads.  Units held whole by one CTA were written by the main kernel; with no
-// slots at all (k = 0) the outputs are zero and lse = -inf.
-constexpr int kCombHeads = 4;
-constexpr int kCombMaxSplits = 2 * kMlaGrid;
+// Merge of the partials of units cut by CTA ranges, by log-sum-exp.  One warp
+// per (row, head, 1/W of the 512 dims), kCombHeads heads per CTA and no
+// block-wide barrier: a lane takes the partials' lse values of splits lane,
+// lane + 32, ...; two warp reductions give the maximum M and
+// Z = sum_s e^{lse_s - M}; then every lane accumulates 16 / W dims over the
+// splits (16-byte loads, two splits in flight), the split's slot and weight
+// broadcast by a shuffle.  W > 1 spreads few rows over more SMs.  Units held
+// whole by one CTA were written by the main kernel; with no slots at all
+// (k = 0) the outputs are zero and lse = -inf.
+constexpr int kCombHeads = 16;
 
-__global__ void __launch_bounds__(128 * kCombHeads)
+template <int W>
+__global__ void __launch_bounds__(32 * kCombHeads)
 mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int R,
                    int H, int k, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
-  __shared__ float s_w[kCombHeads][kCombMaxSplits];  // weights e^{lse_s - M} / Z
-  __shared__ int s_slot[kCombMaxSplits];
-  __shared__ float s_lse[kCombHeads];
+  constexpr int NQ = 4 / W;                         // 16-byte chunks per lane per split
   pdl_trigger();
   pdl_wait();                                       // the partials
-  const int hq = threadIdx.x >> 7, t = threadIdx.x & 127;
+  const int hq = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q0 = (int)blockIdx.y * (128 / W);       // first 16-byte chunk of this CTA's dims
   const int h = blockIdx.x % (H / kCombHeads) * kCombHeads + hq;
   const int r = blockIdx.x / (H / kCombHeads);
   const int HG = mla_heads_per_cta(H);
-  const int u = r * (H / HG) + h / HG;               // the block's heads share a unit
+  const int u = r * (H / HG) + h / HG;
   const int hl = h % HG;
   const MlaWork w(R, H, k);
   int c0 = 0, c1 = -1;
@@ -694,58 +696,69 @@ mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ p
     if (c0 == c1) return;                           // written by the main kernel
   }
   const int ns = c1 - c0 + 1;                       // 0 when there are no slots
-  for (int i = threadIdx.x; i < ns; i += blockDim.x) {
-    const int c = c0 + i;
-    s_slot[i] = 2 * c + (w.begin(c) / w.NT == u ? 0 : 1);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < ns * kCombHeads; i += blockDim.x) {
-    const int hh = i / ns, sp = i % ns;
-    s_w[hh][sp] = part_lse[(size_t)s_slot[sp] * HG + (hl - hq + hh)];
-  }
-  __syncthreads();
-  if (t == 0) {                                     // one thread per head: max, sum, weights
-    float M = -INFINITY;
-    for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, s_w[hq][sp]);
-    float Z = 0.f;
-    for (int sp = 0; sp < ns; ++sp) {
-      const float e = (M == -INFINITY || s_w[hq][sp] == -INFINITY) ? 0.f : __expf(s_w[hq][sp] - M);
-      s_w[hq][sp] = e;
-      Z += e;
-    }
-    const float inv = Z > 0.f ? 1.f / Z : 0.f;
-    for (int sp = 0; sp < ns; ++sp) s_w[hq][sp] *= inv;
-    s_lse[hq] = Z > 0.f ? M + logf(Z) : -INFINITY;
-  }
-  __syncthreads();
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  int sp = 0;
-  for (; sp + 4 <= ns; sp += 4) {                   // four independent loads in flight
-    float4 v[4];
+  auto slot_of = [&](int sp) {
+    const int c = c0 + sp;
+    return 2 * c + (w.begin(c) / w.NT == u ? 0 : 1);
+  };
+  auto lse_of = [&](int sp) { return __ldg(part_lse + (size_t)slot_of(sp) * HG + hl); };
+  float M = -INFINITY;
+  for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, lse_of(sp));
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      v[j] = __ldg(reinterpret_cast<const float4*>(part_o + ((size_t)s_slot[sp + j] * HG + hl) * kVDim) + t);
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float Z = 0.f;
+  for (int sp = lane; sp < ns; sp += 32) {
+    const float l = lse_of(sp);
+    Z += (M == -INFINITY || l == -INFINITY) ? 0.f : __expf(l - M);
+  }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float ws = s_w[hq][sp + j];
-      acc.x = fmaf(ws, v[j].x, acc.x);
-      acc.y = fmaf(ws, v[j].y, acc.y);
-      acc.z = fmaf(ws, v[j].z, acc.z);
-      acc.w = fmaf(ws, v[j].w, acc.w);
+  for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+  const float inv = Z > 0.f ? 1.f / Z : 0.f;
+  float4 acc[NQ];
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto add = [&](float ws, const float4& v, float4& a) {
+    a.x = fmaf(ws, v.x, a.x);
+    a.y = fmaf(ws, v.y, a.y);
+    a.z = fmaf(ws, v.z, a.z);
+    a.w = fmaf(ws, v.w, a.w);
+  };
+  for (int sp0 = 0; sp0 < ns; sp0 += 32) {
+    int my_slot = 0;
+    float my_w = 0.f;
+    if (sp0 + lane < ns) {
+      my_slot = slot_of(sp0 + lane);
+      const float l = __ldg(part_lse + (size_t)my_slot * HG + hl);
+      my_w = (M == -INFINITY || l == -INFINITY) ? 0.f : __expf(l - M) * inv;
+    }
+    const int cnt = min(32, ns - sp0);
+    for (int j = 0; j < cnt; j += 2) {              // two splits in flight (the second may be empty)
+      const int sa = __shfl_sync(0xffffffffu, my_slot, j);
+      const float wa = __shfl_sync(0xffffffffu, my_w, j);
+      const int sb = __shfl_sync(0xffffffffu, my_slot, (j + 1) & 31);
+      const float wb = j + 1 < cnt ? __shfl_sync(0xffffffffu, my_w, (j + 1) & 31) : 0.f;
+      const float4* pa = reinterpret_cast<const float4*>(part_o + ((size_t)sa * HG + hl) * kVDim);
+      const float4* pb = reinterpret_cast<const float4*>(part_o + ((size_t)(j + 1 < cnt ? sb : sa) * HG + hl) * kVDim);
+      float4 va[NQ], vb[NQ];
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        va[q] = __ldg(pa + q0 + lane + 32 * q);
+        vb[q] = __ldg(pb + q0 + lane + 32 * q);
+      }
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) {
+        add(wa, va[q], acc[q]);
+        add(wb, vb[q], acc[q]);
+      }
     }
   }
-  for (; sp < ns; ++sp) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(part_o + ((size_t)s_slot[sp] * HG + hl) * kVDim) + t);
-    const float ws = s_w[hq][sp];
-    acc.x = fmaf(ws, v.x, acc.x);
-    acc.y = fmaf(ws, v.y, acc.y);
-    acc.z = fmaf(ws, v.z, acc.z);
-    acc.w = fmaf(ws, v.w, acc.w);
+  __nv_bfloat16* dst = out + ((size_t)r * H + h) * kVDim;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    __nv_bfloat162* d2 = reinterpret_cast<__nv_bfloat162*>(dst + (q0 + lane + 32 * q) * 4);
+    d2[0] = __floats2bfloat162_rn(acc[q].x, acc[q].y);
+    d2[1] = __floats2bfloat162_rn(acc[q].z, acc[q].w);
   }
-  __nv_bfloat16* dst = out + ((size_t)r * H + h) * kVDim + t * 4;
-  reinterpret_cast<__nv_bfloat162*>(dst)[0] = __floats2bfloat162_rn(acc.x, acc.y);
-  reinterpret_cast<__nv_bfloat162*>(dst)[1] = __floats2bfloat162_rn(acc.z, acc.w);
-  if (lse && t == 0) lse[(size_t)r * H + h] = s_lse[hq];
+  if (lse && lane == 0 && blockIdx.y == 0) lse[(size_t)r * H + h] = Z > 0.f ? M + logf(Z) : -INFINITY;
 }
 
 // The latent cache as a 2-D tensor of 576-byte rows (one per token slot); a box
@@ -799,8 +812,11 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   // chained after the main kernel, or (no slots at all) after the caller's work
-  cudaError_t e = launch_kernel(mla_combine_kernel, dim3(a.R * a.H / kCombHeads),
-                                dim3(128 * kCombHeads), 0, st, w.G > 0 || a.chained,
+  const int nblk = a.R * a.H / kCombHeads;
+  const int W = nblk >= kMlaGrid ? 1 : (2 * nblk >= kMlaGrid ? 2 : 4);
+  auto kern = W == 1 ? mla_combine_kernel<1> : (W == 2 ? mla_combine_kernel<2> : mla_combine_kernel<4>);
+  cudaError_t e = launch_kernel(kern, dim3(nblk, W), dim3(32 * kCombHeads), 0, st,
+                                w.G > 0 || a.chained,
                                 reinterpret_cast<const float*>(a.scratch + L.part_o),
                                 reinterpret_cast<const float*>(a.scratch + L.part_lse), a.R, a.H,
                                 a.k, static_cast<__nv_bfloat16*>(a.out), a.lse);
