@@ -25,7 +25,8 @@
 //    E4M3(s), lo = E4M3(s - hi); 2^-a is folded into the head weight.  The
 //    split is exact for every |s| >= 1/4 (all but query elements below about
 //    1/500 of the head's absmax, where lo keeps a 2^-9 grid).  An E4M3 query
-//    is its own hi term (lo = 0) and its scale is folded into the weight.
+//    is its own single term (K = 128: the lo half is neither loaded nor
+//    multiplied) and its scale is folded into the weight.
 //  * Each TMEM lane holds one token's (row, head) logits, so the
 //    ReLU-weighted head sum is a per-thread loop: no shuffles.
 //  * Persistent CTAs, one per SM, each taking a contiguous run of (group,
@@ -221,7 +222,6 @@ scan_prep_kernel(const void* __restrict__ q_idx, int q_dtype, const float* __res
   if (q_dtype == DSA_E4M3) {                        // already one E4M3 term
     *reinterpret_cast<uint32_t*>(hi_dst) =
         *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(q_idx) + off);
-    *reinterpret_cast<uint32_t*>(lo_dst) = 0u;
     wv *= q_scale[(size_t)r * kIdxHeads + h];
   } else {
     const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(q_idx) + off);
@@ -356,7 +356,7 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
             const uint8_t* __restrict__ key_cache, int64_t num_pages,
             const int32_t* __restrict__ block_table, int max_pages,
             const int32_t* __restrict__ row_len, float* __restrict__ scores, int64_t ld,
-            int n_rows, ScanWs ws, uint32_t* status) {
+            int n_rows, int q_terms, ScanWs ws, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -451,10 +451,12 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
           const uint64_t a_desc = a_desc_base + (uint64_t)((s * kKeyTileBytes) >> 4);
           const uint32_t d_tmem = tmem_base + (uint32_t)(db * kDCols);
 #pragma unroll
-          for (int j = 0; j < 2 * kIdxDim / 32; ++j)  // K = 2 x 128 bytes in steps of 32
+          for (int j = 0; j < 2 * kIdxDim / 32; ++j) {  // K = q_terms x 128 bytes in steps of 32
+            if (j >= q_terms * (kIdxDim / 32)) break;
             mma_e4m3_ss(d_tmem, a_desc + (uint64_t)((j & 3) * 2),
                         b_desc + (uint64_t)(((j >> 2) * kQAtom + (j & 3) * 32) >> 4), idesc,
                         j > 0 ? 1u : 0u);
+          }
           mma_commit(&empty[s]);
           mma_commit(&d_full[db]);
           issued_in_group = true;
@@ -521,10 +523,12 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
         }
         if (!warp_wait(&q_empty[gi % kQBufs], ((uint32_t)(gi / kQBufs) & 1) ^ 1, status)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&q_full[gi % kQBufs], kQBytes);
+          mbar_arrive_expect_tx(&q_full[gi % kQBufs], q_terms * kQAtom);
           uint8_t* qd = smem + kOffQ + (gi % kQBufs) * kQBytes;
           tma_load_2d(qd, &q_map, 0, cur.G.x * kIdxHeads, &q_full[gi % kQBufs]);
-          tma_load_2d(qd + kQAtom, &q_map, 0, (n_rows + cur.G.x) * kIdxHeads, &q_full[gi % kQBufs]);
+          if (q_terms == 2)
+            tma_load_2d(qd + kQAtom, &q_map, 0, (n_rows + cur.G.x) * kIdxHeads,
+                        &q_full[gi % kQBufs]);
         }
       }
       if (i % kProdWarps != pw) {
@@ -672,7 +676,7 @@ cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st) {
                                              a.row_len, a.R, a.B, a.max_pages, ws, a.status);
   e = launch_kernel(scan_kernel, dim3(sms), dim3(kThreads), kSmemAlloc, st, true, kmap, qmap,
                     a.key_cache, a.num_pages, a.block_table, a.max_pages, a.row_len, a.scores,
-                    a.ld, a.R, ws, a.status);
+                    a.ld, a.R, a.q_dtype == DSA_E4M3 ? 1 : 2, ws, a.status);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -123,6 +123,56 @@ __device__ __forceinline__ int64_t sample_stride(int len) {
   return sb < kSampleStride ? kSampleStride : sb;
 }
 
+// Candidate threshold of a row from its fixed sample: the key of the
+// sample's rank-rho element rounded down to its 22-bit prefix (0: take every
+// key, when the sample holds fewer than rho keys).  Called by all
+// kSampleThreads threads; every thread gets the result.
+template <typename KeyAt>
+__device__ uint32_t sample_threshold(KeyAt key_at, int len, int k, uint32_t* h, uint32_t* warp_sums,
+                                     int* s_d, uint32_t* s_above, uint32_t* s_n) {
+  const int64_t sb = sample_stride(len);
+  const int64_t ns = ((((int64_t)len + 31) / 32 + sb - 1) / sb) * 32;   // upper bound (ragged end)
+  auto sample_pos = [&](int64_t e) { return (e / 32) * 32 * sb + (e % 32); };
+  // rank rho in the sample ~ 1.5 k / sb + 32 (about 1.5 k + 32 sb candidates in the row)
+  const uint32_t rho = (uint32_t)((3 * (int64_t)k + 2 * sb - 1) / (2 * sb)) + 32;
+  for (int i = threadIdx.x; i < kTopkBins1; i += kSampleThreads) h[i] = 0;
+  if (threadIdx.x == 0) *s_n = 0;
+  __syncthreads();
+  uint32_t n_local = 0;
+  for (int64_t b = 0; b < ns; b += kSampleThreads) {              // uniform trip count
+    const int64_t e = b + threadIdx.x;
+    const int64_t pos = sample_pos(e);
+    const bool v = e < ns && pos < len;
+    const uint32_t key = v ? key_at(pos) : 0u;
+    n_local += v ? 1u : 0u;
+    hist_add(h, key >> 21, v);
+  }
+  atomicAdd(s_n, n_local);
+  __syncthreads();
+  if (*s_n < rho) {                            // short sample: take every key
+    __syncthreads();                           // every thread has read s_n
+    return 0u;
+  }
+  find_threshold<kTopkBins1, kSampleThreads>(h, rho, warp_sums, s_d, s_above);
+  const uint32_t d1 = (uint32_t)*s_d;
+  const uint32_t need = rho - *s_above;
+  __syncthreads();
+  for (int i = threadIdx.x; i < kTopkBins1; i += kSampleThreads) h[i] = 0;
+  __syncthreads();
+  for (int64_t b = 0; b < ns; b += kSampleThreads) {
+    const int64_t e = b + threadIdx.x;
+    const int64_t pos = sample_pos(e);
+    const bool v = e < ns && pos < len;
+    const uint32_t key = v ? key_at(pos) : 0u;
+    hist_add(h, (key >> 10) & 0x7FF, v && (key >> 21) == d1);
+  }
+  __syncthreads();
+  find_threshold<kTopkBins2, kSampleThreads>(h, need, warp_sums, s_d, s_above);
+  const uint32_t t = (d1 << 21) | ((uint32_t)*s_d << 10);
+  __syncthreads();                             // every thread has read s_d
+  return t;
+}
+
 __global__ void __launch_bounds__(kSampleThreads)
 topk_sample_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
                    int64_t max_len, int k, uint32_t* __restrict__ tau, uint32_t* __restrict__ cnt) {
@@ -137,45 +187,9 @@ topk_sample_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
   __shared__ int s_d;
   __shared__ uint32_t s_above, s_n;
   const float* row = scores + (size_t)r * ld;
-  const int64_t sb = sample_stride(len);
-  const int64_t ns = ((((int64_t)len + 31) / 32 + sb - 1) / sb) * 32;   // upper bound (ragged end)
-  auto sample_pos = [&](int64_t e) { return (e / 32) * 32 * sb + (e % 32); };
-  // rank rho in the sample ~ 1.5 k / sb + 32 (about 1.5 k + 32 sb candidates in the row)
-  const uint32_t rho = (uint32_t)((3 * (int64_t)k + 2 * sb - 1) / (2 * sb)) + 32;
-  for (int i = threadIdx.x; i < kTopkBins1; i += kSampleThreads) h[i] = 0;
-  if (threadIdx.x == 0) s_n = 0;
-  __syncthreads();
-  uint32_t n_local = 0;
-  for (int64_t b = 0; b < ns; b += kSampleThreads) {              // uniform trip count
-    const int64_t e = b + threadIdx.x;
-    const int64_t pos = sample_pos(e);
-    const bool v = e < ns && pos < len;
-    const uint32_t key = v ? ordered_key(row[pos]) : 0u;
-    n_local += v ? 1u : 0u;
-    hist_add(h, key >> 21, v);
-  }
-  atomicAdd(&s_n, n_local);
-  __syncthreads();
-  if (s_n < rho) {                             // short sample: take every key
-    if (threadIdx.x == 0) tau[r] = 0u;
-    return;
-  }
-  find_threshold<kTopkBins1, kSampleThreads>(h, rho, warp_sums, &s_d, &s_above);
-  const uint32_t d1 = (uint32_t)s_d;
-  const uint32_t need = rho - s_above;
-  __syncthreads();
-  for (int i = threadIdx.x; i < kTopkBins1; i += kSampleThreads) h[i] = 0;
-  __syncthreads();
-  for (int64_t b = 0; b < ns; b += kSampleThreads) {
-    const int64_t e = b + threadIdx.x;
-    const int64_t pos = sample_pos(e);
-    const bool v = e < ns && pos < len;
-    const uint32_t key = v ? ordered_key(row[pos]) : 0u;
-    hist_add(h, (key >> 10) & 0x7FF, v && (key >> 21) == d1);
-  }
-  __syncthreads();
-  find_threshold<kTopkBins2, kSampleThreads>(h, need, warp_sums, &s_d, &s_above);
-  if (threadIdx.x == 0) tau[r] = (d1 << 21) | ((uint32_t)s_d << 10);
+  const uint32_t t = sample_threshold([&](int64_t pos) { return ordered_key(row[pos]); }, len, k,
+                                      h, warp_sums, &s_d, &s_above, &s_n);
+  if (threadIdx.x == 0) tau[r] = t;
 }
 
 // ---- 2. candidates: every key >= tau -------------------------------------------
@@ -426,10 +440,169 @@ topk_finalize_kernel(const float* __restrict__ scores, int64_t ld,
   }
 }
 
+// ---- one CTA per row: rows that fit in shared memory ---------------------------
+// The row's keys are loaded once into shared memory (every load issued before
+// the first is used: one memory round trip).  The fixed sample of the
+// multi-launch path sets a candidate threshold tau; warp w owns a contiguous
+// segment of the row, counts its keys >= tau with ballots, and a 32-entry
+// scan places each warp's candidates, so the candidate positions land in
+// shared memory in position order.  If there are at least k and at most
+// kRowCand of them, the exact select runs over the candidates, else over the
+// whole row (the result is the same; only the work differs).  The kept
+// positions are then written in position order: over the items in order,
+//   slot = #(key > T before it) + min(#(key == T before it), need_eq),
+// a tie being kept when #(key == T before it) < need_eq.
+constexpr int kRowCap = 49152;                 // scores of a row held in shared memory
+constexpr int kRowCand = 6144;                 // candidate positions held in shared memory
+static_assert(kRowCap % (4 * kFinalThreads) == 0, "whole vectors per thread");
+
+size_t row_smem_bytes() {
+  return (sizeof(SelectSmem) + 15) / 16 * 16 + (size_t)(kRowCap + kRowCand) * 4;
+}
+
+// Exclusive count before this warp and total over the block of c (one value
+// per warp, in s[32]); all threads call it after s is filled and synced.
+__device__ __forceinline__ uint32_t warp_prefix(const uint32_t* s, uint32_t* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const uint32_t x = s[lane];
+  uint32_t before = lane < wid ? x : 0u, all = x;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    before += __shfl_xor_sync(0xffffffffu, before, o);
+    all += __shfl_xor_sync(0xffffffffu, all, o);
+  }
+  *total = all;
+  return before;
+}
+
+// Writes the kept items (key > T, or == T within the first need_eq ties) of
+// the n items, in item order, as positions pos_at(i) to out[0, k).
+template <typename PosAt>
+__device__ __forceinline__ void write_selected(const uint32_t* keys, PosAt pos_at, int n, uint32_t T,
+                                               uint32_t need_eq, int k, int32_t* out,
+                                               uint32_t* s_gt, uint32_t* s_eq) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int seg = (n + kFinalThreads - 1) / kFinalThreads * 32;    // multiple of 32
+  const int i_begin = wid * seg, i_end = min(n, i_begin + seg);
+  uint32_t cg = 0, ce = 0;
+  for (int i0 = i_begin; i0 < i_end; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t key = i < i_end ? keys[pos_at(i)] : 0u;
+    cg += __popc(__ballot_sync(0xffffffffu, i < i_end && key > T));
+    ce += __popc(__ballot_sync(0xffffffffu, i < i_end && key == T));
+  }
+  if (lane == 0) {
+    s_gt[wid] = cg;
+    s_eq[wid] = ce;
+  }
+  __syncthreads();
+  uint32_t tot;
+  uint32_t bg = warp_prefix(s_gt, &tot), be = warp_prefix(s_eq, &tot);
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int i0 = i_begin; i0 < i_end; i0 += 32) {
+    const int i = i0 + lane;
+    const int p = i < i_end ? pos_at(i) : 0;
+    const uint32_t key = i < i_end ? keys[p] : 0u;
+    const bool gt = i < i_end && key > T, eq = i < i_end && key == T;
+    const unsigned mg = __ballot_sync(0xffffffffu, gt), me = __ballot_sync(0xffffffffu, eq);
+    const uint32_t eq_before = be + __popc(me & lt);
+    const uint32_t slot = bg + __popc(mg & lt) + min(eq_before, need_eq);
+    if ((gt || (eq && eq_before < need_eq)) && slot < (uint32_t)k) out[slot] = p;
+    bg += __popc(mg);
+    be += __popc(me);
+  }
+}
+
+__global__ void __launch_bounds__(kFinalThreads, 1)
+topk_row_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
+                int64_t max_len, int k, int32_t* __restrict__ idx, uint32_t* status) {
+  static_assert(kFinalThreads == kSampleThreads, "the sample threshold runs on this block");
+  extern __shared__ __align__(16) uint8_t row_smem[];
+  SelectSmem& S = *reinterpret_cast<SelectSmem*>(row_smem);
+  uint32_t* keys = reinterpret_cast<uint32_t*>(row_smem + (sizeof(SelectSmem) + 15) / 16 * 16);
+  uint32_t* cand = keys + kRowCap;
+  __shared__ uint32_t s_gt[32], s_eq[32], s_cnt[32];
+  pdl_trigger();
+  pdl_wait();                                  // the scores
+  const int r = blockIdx.x;
+  const int len = row_len[r];
+  int32_t* out = idx + (size_t)r * k;
+  if (!row_ok(len, max_len) || len > kRowCap) {
+    if (threadIdx.x == 0) raise_dev(status, DSA_DEV_BAD_ROW);
+    for (int j = threadIdx.x; j < k; j += kFinalThreads) out[j] = -1;
+    return;
+  }
+  if (len <= k) {
+    for (int j = threadIdx.x; j < k; j += kFinalThreads) out[j] = j < len ? j : -1;
+    return;
+  }
+  // load (16-byte vectors; the row is 16-byte aligned and holds ld >= 4 ceil(len / 4) floats)
+  const float* row = scores + (size_t)r * ld;
+  const int n4 = (len + 3) >> 2;
+  constexpr int kVecPer = kRowCap / 4 / kFinalThreads;
+  float4 v[kVecPer];
+#pragma unroll
+  for (int u = 0; u < kVecPer; ++u) {
+    const int g = u * kFinalThreads + (int)threadIdx.x;
+    v[u] = g < n4 ? __ldg(reinterpret_cast<const float4*>(row) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+#pragma unroll
+  for (int u = 0; u < kVecPer; ++u) {
+    const int g = u * kFinalThreads + (int)threadIdx.x;
+    if (g < n4)
+      *reinterpret_cast<uint4*>(keys + 4 * g) = make_uint4(
+          ordered_key(v[u].x), ordered_key(v[u].y), ordered_key(v[u].z), ordered_key(v[u].w));
+  }
+  __syncthreads();
+  const uint32_t tau = sample_threshold([&](int64_t p) { return keys[p]; }, len, k, S.h,
+                                        S.warp_sums, &S.d, &S.above, &S.acc[0]);
+  // candidates: keys >= tau, counted per warp segment, then placed in position order
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int seg = (len + kFinalThreads - 1) / kFinalThreads * 32;
+  const int p_begin = wid * seg, p_end = min(len, p_begin + seg);
+  uint32_t c = 0;
+  for (int p0 = p_begin; p0 < p_end; p0 += 32) {
+    const int p = p0 + lane;
+    c += __popc(__ballot_sync(0xffffffffu, p < p_end && keys[p] >= tau));
+  }
+  if (lane == 0) s_cnt[wid] = c;
+  __syncthreads();
+  uint32_t n;
+  uint32_t base = warp_prefix(s_cnt, &n);
+  uint32_t T, need_eq, n_eq;
+  if (n >= (uint32_t)k && n <= (uint32_t)kRowCand) {            // uniform
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int p0 = p_begin; p0 < p_end; p0 += 32) {
+      const int p = p0 + lane;
+      const bool c1 = p < p_end && keys[p] >= tau;
+      const unsigned m = __ballot_sync(0xffffffffu, c1);
+      if (c1) cand[base + __popc(m & lt)] = (uint32_t)p;
+      base += __popc(m);
+    }
+    __syncthreads();
+    kth_key([&](uint32_t i) { return keys[cand[i]]; }, n, k, S, T, need_eq, n_eq);
+    write_selected(keys, [&](int i) { return (int)cand[i]; }, (int)n, T, need_eq, k, out, s_gt,
+                   s_eq);
+  } else {
+    kth_key([&](uint32_t i) { return keys[i]; }, (uint32_t)len, k, S, T, need_eq, n_eq);
+    write_selected(keys, [](int i) { return i; }, len, T, need_eq, k, out, s_gt, s_eq);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st) {
   if (a.R == 0) return cudaSuccess;
+  if (a.max_len <= kRowCap && (reinterpret_cast<uintptr_t>(a.scores) & 15) == 0 && a.ld % 4 == 0) {
+    cudaError_t e = cudaFuncSetAttribute(topk_row_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)row_smem_bytes());
+    if (e != cudaSuccess) return e;
+    e = launch_kernel(topk_row_kernel, dim3(a.R), dim3(kFinalThreads), row_smem_bytes(), st,
+                      a.chained, a.scores, a.ld, a.row_len, a.max_len, a.k, a.idx, a.status);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+  }
   const TopkLayout L(a.R, a.max_len);
   uint32_t* tau = reinterpret_cast<uint32_t*>(a.scratch + L.tau);
   uint32_t* cnt = reinterpret_cast<uint32_t*>(a.scratch + L.cnt);

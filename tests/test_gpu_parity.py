@@ -78,10 +78,19 @@ def test_indexer_scores_match_oracle(dsa, oracle_mod, wl):
 
 
 # ------------------------------------------------------------------- top-k
-def _topk_bitexact(dsa, oracle_mod, scores32, row_len, k):
+# Rows of at most 49152 scores are selected by one CTA per row in shared
+# memory, wider score buffers by the sample / collect / finalize kernels; a
+# buffer padded to WIDE columns (poison past the data) takes the second path.
+WIDE = 65536
+TOPK_PATHS = {"row_in_smem": None, "sample_collect": WIDE}
+
+
+def _topk_bitexact(dsa, oracle_mod, scores32, row_len, k, pad_to=None):
     R, ld = scores32.shape
     ld4 = (ld + 3) // 4 * 4
-    buf = np.zeros((R, ld4), np.float32)
+    if pad_to is not None:
+        ld4 = max(ld4, pad_to)
+    buf = np.full((R, ld4), 1e30, np.float32)
     buf[:, :ld] = scores32
     g = dsa.dsa_topk(torch.from_numpy(buf).to(DEV), torch.tensor(row_len, dtype=torch.int32,
                                                                  device=DEV), k)
@@ -96,17 +105,19 @@ def _topk_bitexact(dsa, oracle_mod, scores32, row_len, k):
         assert np.array_equal(gs[:n], np.sort(o[r, :n])), f"row {r}: selection differs"
 
 
+@pytest.mark.parametrize("path", list(TOPK_PATHS))
 @pytest.mark.parametrize("wl", SMALL, ids=[w.name for w in SMALL])
-def test_topk_bitexact_on_oracle_scores(dsa, oracle_mod, wl):
+def test_topk_bitexact_on_oracle_scores(dsa, oracle_mod, wl, path):
     host = inputs.to_numpy(inputs.make_inputs(wl, device="cpu"))
     ora = oracle_mod.indexer_scores(host["q_idx"], host["w"], host["key_cache"],
                                     host["block_table"], host["row_req"], host["row_len"],
                                     q_scale=host["q_idx_scale"])
     s32 = np.nan_to_num(ora, nan=0.0).astype(np.float32)
-    _topk_bitexact(dsa, oracle_mod, s32, list(host["row_len"]), wl.k)
+    _topk_bitexact(dsa, oracle_mod, s32, list(host["row_len"]), wl.k, TOPK_PATHS[path])
 
 
-def test_topk_ties_signs_and_edges(dsa, oracle_mod):
+@pytest.mark.parametrize("path", list(TOPK_PATHS))
+def test_topk_ties_signs_and_edges(dsa, oracle_mod, path):
     rng = np.random.default_rng(0)
     L = 20000
     rows = [
@@ -121,12 +132,18 @@ def test_topk_ties_signs_and_edges(dsa, oracle_mod):
     ]
     s = np.stack(rows)
     lens = [L, L, L, L, 2048, 2049, 4097, 1]
+    pad = TOPK_PATHS[path]
     for k in (2048, 1, 7, 1000):
-        _topk_bitexact(dsa, oracle_mod, s, lens, k)
-    _topk_bitexact(dsa, oracle_mod, s[:2], [0, 5], 16)
+        _topk_bitexact(dsa, oracle_mod, s, lens, k, pad)
+    _topk_bitexact(dsa, oracle_mod, s[:2], [0, 5], 16, pad)
+    # the largest row the one-CTA path holds, and one past it (other path)
+    for L2 in (49152, 49153):
+        big = rng.integers(0, 200, (1, L2)).astype(np.float32)
+        _topk_bitexact(dsa, oracle_mod, big, [L2], 2048, pad)
 
 
-def test_topk_rows_built_against_the_sample(dsa, oracle_mod):
+@pytest.mark.parametrize("path", list(TOPK_PATHS))
+def test_topk_rows_built_against_the_sample(dsa, oracle_mod, path):
     """The selection is exact whatever a fixed sample of the row suggests: rows
     whose best scores sit only outside, or only inside, the sampled blocks
     (every 16th block of 32 scores), so the candidate threshold is far too low
@@ -142,7 +159,7 @@ def test_topk_rows_built_against_the_sample(dsa, oracle_mod):
     short = rng.standard_normal(L).astype(np.float32)
     short[in_sample & (pos < 16384)] += 10.0             # 1024 sampled highs < k
     s = np.stack([hidden, only, short])
-    _topk_bitexact(dsa, oracle_mod, s, [L, L, 16384], 2048)
+    _topk_bitexact(dsa, oracle_mod, s, [L, L, 16384], 2048, TOPK_PATHS[path])
 
 
 def test_topk_long_row_split_over_chunks(dsa, oracle_mod):
@@ -287,7 +304,7 @@ def test_bounded_wait_runs_out_and_context_stays_usable(dsa):
 
 
 # ----------------------------------------------- full benchmark sizes, sampled
-FULL = [1, 2, 3]
+FULL = [1, 2, 3, 4]
 
 
 @pytest.mark.parametrize("ci", FULL, ids=[inputs.config(i).name for i in FULL])
