@@ -40,14 +40,10 @@ L2_FLUSH_BYTES = 256 << 20
 KERNELS_PER_STEP = 8
 
 # DRAM bytes (read + write) per call of a stage, summed over its kernels, from
-# the ncu launch list in profiles/decode_step_launches_16x4_ctx32768.md (taken
-# on the current kernels; cold cache, so the combine's L2-resident partials
-# count as DRAM reads).  Stages and workloads not captured report null.
-NCU_STAGE_TRAFFIC = {
-    ("decode_16x4_ctx32768_h64", "indexer_scan"): 70.40e6,
-    ("decode_16x4_ctx32768_h64", "topk"): 10.82e6,
-    ("decode_16x4_ctx32768_h64", "sparse_mla"): 115.44e6,
-}
+# the ncu launch list in profiles/ (taken on the current kernels; cold cache,
+# so L2-resident intermediates count as DRAM reads).  Stages and workloads not
+# captured report null.
+NCU_STAGE_TRAFFIC = {}
 
 
 def _peaks():
@@ -57,6 +53,11 @@ def _peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
     return 6800.0, 1900.0, "fallback"
+
+
+# Dense FP8 (E4M3) tensor rate = the bf16 rate x the nominal FP8 / bf16 ratio
+# (4.5 / 2.25 PFLOP/s): both contractions of the step run kind::f8f6f4.
+FP8_PER_BF16 = 2.0
 
 
 def _dist():
@@ -258,17 +259,36 @@ def run_gpu(args):
         stage_ms[name] = _time_launches(g.replay, max(20, min(args.steps, 200)), flush, stream)[0]
     eager_ms = _time_launches(step_eager, max(20, min(args.steps, 200)), flush, stream)[0]
     dominant = max((n for n in stages if stages[n][1] is not None), key=lambda n: stage_ms[n])
-    hbm_peak, _, peak_kind = _peaks()
-    dom_bytes = stages[dominant][1]
-    achieved = dom_bytes / (stage_ms[dominant] * 1e-3) / 1e9
-    roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1),
-                "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
-                "frac": round(achieved / hbm_peak, 4),
-                "traffic": NCU_STAGE_TRAFFIC.get((wl.name, dominant)),
-                "stage_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
-                "step_frac_of_8TBs": round(bytes_step / (ms_per_step * 1e-3) / 8e12, 4),
-                "step_frac_of_measured": round(bytes_step / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
-                                               4)}
+    hbm_peak, bf16_peak, peak_kind = _peaks()
+    fp8_peak = bf16_peak * FP8_PER_BF16
+    # algorithmic FLOPs of the two contractions (indexer scan, attention) per stage time
+    tflops = {"indexer_scan": traffic.scan_flops(wl) / (stage_ms["indexer_scan"] * 1e-3) / 1e12,
+              "sparse_mla": traffic.mla_flops(wl) / (stage_ms["sparse_mla"] * 1e-3) / 1e12}
+    tensor = {"unit": "TFLOP/s", "peak": round(fp8_peak, 1),
+              "peak_kind": f"{peak_kind} bf16 x {FP8_PER_BF16:g} (nominal FP8/bf16)",
+              "indexer_scan": round(tflops["indexer_scan"], 2),
+              "sparse_mla": round(tflops["sparse_mla"], 2),
+              "indexer_scan_frac": round(tflops["indexer_scan"] / fp8_peak, 4),
+              "sparse_mla_frac": round(tflops["sparse_mla"] / fp8_peak, 4)}
+    common = {"traffic": NCU_STAGE_TRAFFIC.get((wl.name, dominant)),
+              "stage_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
+              "step_frac_of_8TBs": round(bytes_step / (ms_per_step * 1e-3) / 8e12, 4),
+              "step_frac_of_measured": round(bytes_step / (ms_per_step * 1e-3) / 1e9 / hbm_peak,
+                                             4)}
+    if wl.q_idx_fp8:
+        # prefill chunk: the indexer is a dense FP8 GEMM, bound by the tensor cores
+        dominant = "indexer_scan"
+        achieved = tflops[dominant]
+        roofline = {"kernel": dominant, "bound": "tensor", "achieved": round(achieved, 2),
+                    "peak": round(fp8_peak, 1), "peak_kind": tensor["peak_kind"],
+                    "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4), **common}
+        roofline["traffic"] = NCU_STAGE_TRAFFIC.get((wl.name, dominant))
+    else:
+        dom_bytes = stages[dominant][1]
+        achieved = dom_bytes / (stage_ms[dominant] * 1e-3) / 1e9
+        roofline = {"kernel": dominant, "bound": "hbm", "achieved": round(achieved, 1),
+                    "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                    "frac": round(achieved / hbm_peak, 4), **common}
 
     # ---- end to end through the public API with host buffers -----------------
     host = {k: v.cpu().pin_memory() for k, v in inp.items()
@@ -320,6 +340,7 @@ def run_gpu(args):
                         "pinned host memory and outputs copied back inside the timed region; "
                         "the KV caches are resident layer state"},
         "roofline": roofline,
+        "tensor": tensor,
         "eager_ms_per_step": round(eager_ms, 5),
         "cpu_baseline": cpu,
         "gpu_launches": KERNELS_PER_STEP * args.steps,
@@ -402,7 +423,8 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", type=int, default=1,
-                    help="0 tiny, 1 16x4 rows @32K (default), 2 16x4 @256K, 3 1 row @1M")
+                    help="0 tiny, 1 16x4 rows @32K (default), 2 16x4 @256K, 3 1 row @1M, "
+                         "4 prefill chunk of 4096 rows @128K")
     ap.add_argument("--impl", default="dsa", choices=["dsa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -12,7 +12,7 @@
 namespace dsa {
 
 cudaError_t encode_tensor_map_u8(CUtensorMap* map, int rank, const void* base, const uint64_t* dims,
-                                 const uint64_t* strides, const uint32_t* box) {
+                                 const uint64_t* strides, const uint32_t* box, int swizzle_bytes) {
   static std::once_flag once;
   static PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
   std::call_once(once, [] {
@@ -25,6 +25,7 @@ cudaError_t encode_tensor_map_u8(CUtensorMap* map, int rank, const void* base, c
   });
   if (!enc) return cudaErrorNotSupported;
   if (rank < 1 || rank > 5) return cudaErrorInvalidValue;
+  if (swizzle_bytes != 128 && swizzle_bytes != 64) return cudaErrorInvalidValue;
   cuuint64_t d[5], st[4];
   cuuint32_t bx[5], es[5];
   for (int i = 0; i < rank; ++i) {
@@ -34,7 +35,8 @@ cudaError_t encode_tensor_map_u8(CUtensorMap* map, int rank, const void* base, c
     if (i + 1 < rank) st[i] = strides[i];
   }
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, (cuuint32_t)rank, const_cast<void*>(base),
-                         d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         d, st, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         swizzle_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

@@ -218,6 +218,7 @@ size_t selftest_workspace_bytes();
 // copied per load; 128-byte swizzle, out-of-range elements read as zero.
 // The driver entry point is looked up once per process.
 cudaError_t encode_tensor_map_u8(CUtensorMap* map, int rank, const void* base, const uint64_t* dims,
-                                 const uint64_t* strides, const uint32_t* box);
+                                 const uint64_t* strides, const uint32_t* box,
+                                 int swizzle_bytes = 128);
 
 }  // namespace dsa

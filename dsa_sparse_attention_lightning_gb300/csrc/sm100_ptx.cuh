@@ -219,6 +219,19 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for the 64-byte swizzle layout: rows of 64 bytes, 8-row groups
+// 512 bytes apart, 16-byte chunk c of row r stored at chunk (c ^ ((r / 2) % 4));
+// the tile base is 512-byte aligned.
+__device__ __forceinline__ uint64_t desc_kmajor_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address, bits 0-13
+  d |= (uint64_t)1 << 16;                     // leading byte offset (unused here), bits 16-29
+  d |= (uint64_t)(512 >> 4) << 32;            // stride byte offset, bits 32-45
+  d |= (uint64_t)1 << 46;                     // descriptor version for sm_100, bits 46-47
+  d |= (uint64_t)4 << 61;                     // layout: 64-byte swizzle, bits 61-63
+  return d;
+}
+
 // Instruction descriptor of kind::f16 with f16 A and B, f32 accumulator,
 // both operands K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {

@@ -21,8 +21,8 @@
 //  1. one warp gathers the 128 selected 576-byte FP8 latent rows (paged) into
 //     one of two shared-memory buffers with TMA tile::gather4 (four arbitrary
 //     rows x 128 bytes per instruction, landing in the K-major 128-byte-swizzle
-//     layout; 576 bytes span 4.5 swizzle atoms, the tail of the fifth box is
-//     past the row and zero-filled), while the previous tile is computed.
+//     layout for dims 0..511; the RoPE dims 512..575 come as 64-byte boxes into
+//     a K-major 64-byte-swizzle block), while the previous tile is computed.
 //     Masked slots use an out-of-range row, which TMA fills with zeros;
 //  2. S[(head, term), token] = Q8 . L8^T on tcgen05 kind::f8f6f4, M = 128,
 //     N = 128 tokens, K = 576.  The bf16 query is split exactly into two E4M3
@@ -55,8 +55,9 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kLatAtoms = 5;                          // 576 B = 4.5 x 128 B, padded
-constexpr int kAtom = kMlaTile * 128;                 // 128 token rows x 128 B
+constexpr int kLatAtoms = 5;                          // 576 B = 4 x 128 B + 64 B
+constexpr int kAtom = kMlaTile * 128;                 // 128 token rows x 128 B (dims 0..511)
+constexpr int kRopeAtom = kMlaTile * 64;              // 128 token rows x 64 B (dims 512..575)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleT = 8.f;                      // log2 headroom of P before a rescale
 constexpr uint32_t kTmemCols = 512;
@@ -155,22 +156,23 @@ constexpr int kGatherWarp0 = 2;
 constexpr int kGatherLanes = 27;                       // 6 x 27 >= 160 loads per tile
 constexpr int kSmWarp0 = 8;                            // first softmax warp
 constexpr int kSmThreads = 256;
-constexpr int kTileBytes = kLatAtoms * kAtom;          // one latent buffer
+constexpr int kTileBytes = 4 * kAtom + kRopeAtom;     // one latent buffer
+static_assert(kTileBytes % 1024 == 0, "swizzle atoms stay 1024-byte aligned");
 constexpr uint32_t kQCol = 0;                          // A operand: Q (dims 0..511), 128 cols
 constexpr uint32_t kSCol = 128;                        // S: [(head, term)] x [128 tokens]
 constexpr uint32_t kOCol = 256;                        // O^T: 4 blocks x HG cols
 
 template <int HG>
 struct MlaSmem {
-  static constexpr int lat = 0;                                      // [2][5][128][128]
+  static constexpr int lat = 0;                                      // [2][4][128][128] + [2][128][64]
   static constexpr int qrope = 2 * kTileBytes;                       // [128 rows][128 B]
   static constexpr int p = qrope + kMlaTile * 128;                   // [2 terms][HG][128]
   static constexpr int corr = p + 2 * HG * 128;                      // [64] f32
   static constexpr int red = corr + 64 * 4;                          // [2 halves][64] f32
   static constexpr int lsum = red + 2 * 64 * 4;                      // [2 halves][64] f32
   static constexpr int flag = lsum + 2 * 64 * 4;                     // [2] int
-  static constexpr int bar = (flag + 8 + 7) / 8 * 8;                 // 10 mbarriers
-  static constexpr int tmem = bar + 10 * 8;
+  static constexpr int bar = (flag + 8 + 7) / 8 * 8;                 // 18 mbarriers
+  static constexpr int tmem = bar + 18 * 8;
   static constexpr int bytes = tmem + 16;
   static constexpr int alloc = bytes + 1024;
 };
@@ -220,7 +222,8 @@ struct TileIt {
 
 template <int HG>  // heads per CTA: 16, 32 or 64
 __global__ void __launch_bounds__(kThreads, 1)
-smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restrict__ q8,
+smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__ CUtensorMap rope_map,
+            const uint8_t* __restrict__ q8,
             const float* __restrict__ qc, int H, int64_t num_pages, float latent_scale,
             const int32_t* __restrict__ block_table, int B, int max_pages,
             const int32_t* __restrict__ row_req, const int32_t* __restrict__ row_len,
@@ -240,12 +243,13 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
   int* flag_s = reinterpret_cast<int*>(smem + L::flag);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::bar);
   uint64_t* lat_full = bars;          // [2] gathered tile landed
-  uint64_t* lat_empty = bars + 2;     // [2] P.V of the tile finished with the buffer
-  uint64_t* s_full = bars + 4;        // S of a tile is in TMEM
-  uint64_t* s_empty = bars + 5;       // S read (and Q in place) for the next score MMA
-  uint64_t* p_full = bars + 6;        // P in shared memory, O rescaled
-  uint64_t* p_empty = bars + 7;       // P.V finished (O complete up to this tile)
-  uint64_t* mma_done = bars + 8;      // [2] every MMA of an issuer finished
+  uint64_t* lat_empty = bars + 2;     // [2][5] atom a of the buffer is free again: the RoPE
+                                      // atom 4 after S, atom a < 4 after M-block a of P.V
+  uint64_t* s_full = bars + 12;       // S of a tile is in TMEM
+  uint64_t* s_empty = bars + 13;      // S read (and Q in place) for the next score MMA
+  uint64_t* p_full = bars + 14;       // P in shared memory, O rescaled
+  uint64_t* p_empty = bars + 15;      // P.V finished (O complete up to this tile)
+  uint64_t* mma_done = bars + 16;     // [2] every MMA of an issuer finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem);
 
   const int groups = H / HG;
@@ -259,10 +263,8 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&lat_full[b], 1);
-      mbar_init(&lat_empty[b], 1);
-    }
+    for (int b = 0; b < 2; ++b) mbar_init(&lat_full[b], 1);
+    for (int x = 0; x < 2 * kLatAtoms; ++x) mbar_init(&lat_empty[x], 1);
     mbar_init(s_full, 1);
     mbar_init(s_empty, 8);
     mbar_init(p_full, 8);
@@ -300,8 +302,9 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
 #pragma unroll
       for (int j = 0; j < 2; ++j)                     // dims 512..575 from shared
         mma_e4m3_ss(tmem_base + kSCol, desc_kmajor_sw128(smem_u32(qrope) + j * 32),
-                    desc_kmajor_sw128(lb + 4 * kAtom + j * 32), idesc_s, 1u);
+                    desc_kmajor_sw64(lb + 4 * kAtom + j * 32), idesc_s, 1u);
       mma_commit(s_full);
+      mma_commit(&lat_empty[(i & 1) * kLatAtoms + 4]);   // the RoPE atom is read by S only
     };
     auto issue_o = [&](int i, bool first) {
       const uint32_t lb = smem_u32(lat + (i & 1) * kTileBytes);
@@ -316,9 +319,9 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
                       (!first || kk > 0) ? 1u : 0u);
           mma_e4m3_ss(d, ad, desc_kmajor_sw128(pb + HG * 128 + kk * 32), idesc_o, 1u);
         }
+        mma_commit(&lat_empty[(i & 1) * kLatAtoms + a]);   // M-block a was the last reader of atom a
       }
       mma_commit(p_empty);
-      mma_commit(&lat_empty[i & 1]);
     };
     if (lane == 0 && n > 0) {
       if (warp == 0) {
@@ -378,15 +381,21 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const uint8_t* __restri
       gt.next(NT);
     };
     if (op_ok && n > 0) lookup();
-    for (int i = 0; i < n; ++i) {
+    // Each lane waits for its own atom of the buffer only, so most of a tile is
+    // already in flight while the P.V that frees the buffer's last atoms runs.
+    for (int i = 0; i < n && op_ok; ++i) {
       const int b = i & 1;
-      if (!wwait(&lat_empty[b], ((uint32_t)(i >> 1) & 1) ^ 1, status)) break;
-      // complete_tx of other warps may land before this arrive: the phase
+      if (!mbar_wait(&lat_empty[b * kLatAtoms + a], ((uint32_t)(i >> 1) & 1) ^ 1, status)) break;
+      // complete_tx of other lanes may land before this arrive: the phase
       // cannot complete until the single arrival has come
       if (warp == kGatherWarp0 && lane == 0) mbar_arrive_expect_tx(&lat_full[b], kTileBytes);
-      if (op_ok) {
-        tma_gather4(lat + b * kTileBytes + a * kAtom + g * 512, &lat_map, a * 128, y[0], y[1],
-                    y[2], y[3], &lat_full[b]);
+      {
+        if (a < 4)
+          tma_gather4(lat + b * kTileBytes + a * kAtom + g * 512, &lat_map, a * 128, y[0], y[1],
+                      y[2], y[3], &lat_full[b]);
+        else                                          // RoPE dims: 4 rows x 64 B
+          tma_gather4(lat + b * kTileBytes + 4 * kAtom + g * 256, &rope_map, 512, y[0], y[1],
+                      y[2], y[3], &lat_full[b]);
         if (i + 1 < n) lookup();
       }
     }
@@ -762,27 +771,30 @@ mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ p
 }
 
 // The latent cache as a 2-D tensor of 576-byte rows (one per token slot); a box
-// is 128 bytes of one row, stored with the 128-byte swizzle.
-cudaError_t latent_tensor_map(CUtensorMap* map, const uint8_t* cache, int64_t num_pages) {
+// is box_bytes (128 or 64) of one row, stored with the swizzle of that span.
+cudaError_t latent_tensor_map(CUtensorMap* map, const uint8_t* cache, int64_t num_pages,
+                              uint32_t box_bytes) {
   // Row coordinates are signed 32-bit.  With no pages every lookup is rejected
   // before a coordinate is formed, so a one-page map is never dereferenced.
   if (num_pages * kPage > INT32_MAX) return cudaErrorInvalidValue;
   const int64_t rows = (num_pages > 0 ? num_pages : 1) * kPage;
   const uint64_t dims[2] = {(uint64_t)kLatDim, (uint64_t)rows};
   const uint64_t strides[1] = {(uint64_t)kLatDim};
-  const uint32_t box[2] = {128, 1};
-  return encode_tensor_map_u8(map, 2, cache, dims, strides, box);
+  const uint32_t box[2] = {box_bytes, 1};
+  return encode_tensor_map_u8(map, 2, cache, dims, strides, box, (int)box_bytes);
 }
 
 template <int HG>
 cudaError_t launch_smla(const MlaArgs& a, const MlaLayout& L, int G, cudaStream_t st) {
   using S = MlaSmem<HG>;
-  alignas(64) CUtensorMap map;
-  cudaError_t e = latent_tensor_map(&map, a.latent_cache, a.num_pages);
+  alignas(64) CUtensorMap map, rope;
+  cudaError_t e = latent_tensor_map(&map, a.latent_cache, a.num_pages, 128);
+  if (e != cudaSuccess) return e;
+  e = latent_tensor_map(&rope, a.latent_cache, a.num_pages, 64);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(smla_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::alloc);
   if (e != cudaSuccess) return e;
-  e = launch_kernel(smla_kernel<HG>, dim3(G), dim3(kThreads), S::alloc, st, true, map,
+  e = launch_kernel(smla_kernel<HG>, dim3(G), dim3(kThreads), S::alloc, st, true, map, rope,
                     (const uint8_t*)(a.scratch + L.q8),
                     reinterpret_cast<const float*>(a.scratch + L.qc), a.H, a.num_pages,
                     a.latent_scale, a.block_table, a.B, a.max_pages, a.row_req, a.row_len, a.idx,
