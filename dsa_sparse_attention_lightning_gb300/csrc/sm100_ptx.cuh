@@ -120,6 +120,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Brings a kernel-parameter tensor map into the descriptor cache ahead of its
+// first TMA use.
+__device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // Generic-proxy writes to shared memory become visible to the async proxy
 // (tensor-core operand reads) after this fence.
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -263,6 +263,8 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
+    prefetch_tensor_map(&lat_map);
+    prefetch_tensor_map(&rope_map);
     for (int b = 0; b < 2; ++b) mbar_init(&lat_full[b], 1);
     for (int x = 0; x < 2 * kLatAtoms; ++x) mbar_init(&lat_empty[x], 1);
     mbar_init(s_full, 1);
@@ -418,24 +420,26 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
     // Q of unit u: rows (head, term) -> TMEM columns [0, 128) (dims 0..511)
     // and the RoPE dims 512..575 -> shared (A operand of the last two K steps)
     auto load_q = [&](int r, int hg0) {
-      if (th != 0) return;
+      // token half th loads dims 256 th .. 256 th + 255 and RoPE chunks 2 th, 2 th + 1
+      // of its lane quarter's rows, four rounds of four 16-byte loads
       const int term = lane >> 4;
       const uint4* src = reinterpret_cast<const uint4*>(
           q8 + (((size_t)r * H + hg0 + (head_ok ? hl : 0)) * 2 + term) * kLatDim);
+      const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll 1
-      for (int c8 = 0; c8 < 8; ++c8) {                // 8 x 16 columns = 512 bytes
+      for (int c8 = 4 * th; c8 < 4 * th + 4; ++c8) {      // 16 columns per round
         uint32_t v[16];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint4 x = head_ok ? __ldg(src + c8 * 4 + u) : make_uint4(0, 0, 0, 0);
+          const uint4 x = head_ok ? __ldg(src + c8 * 4 + u) : z;
           v[4 * u + 0] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
         }
         tmem_st_32x32b_x16(tmem_base + ((uint32_t)(quarter * 32) << 16) + kQCol + c8 * 16, v);
       }
       const int m = quarter * 32 + lane;
 #pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        const uint4 x = head_ok ? __ldg(src + 32 + c4) : make_uint4(0, 0, 0, 0);
+      for (int c4 = 2 * th; c4 < 2 * th + 2; ++c4) {
+        const uint4 x = head_ok ? __ldg(src + 32 + c4) : z;
         *reinterpret_cast<uint4*>(qrope + m * 128 + ((c4 ^ (m & 7)) << 4)) = x;
       }
       tmem_wait_st();

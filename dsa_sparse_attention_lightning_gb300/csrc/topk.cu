@@ -126,24 +126,34 @@ __device__ __forceinline__ int64_t sample_stride(int len) {
 // Candidate threshold of a row from its fixed sample: the key of the
 // sample's rank-rho element rounded down to its 22-bit prefix (0: take every
 // key, when the sample holds fewer than rho keys).  Called by all
-// kSampleThreads threads; every thread gets the result.
-template <typename KeyAt>
-__device__ uint32_t sample_threshold(KeyAt key_at, int len, int k, uint32_t* h, uint32_t* warp_sums,
+// kSampleThreads threads; every thread gets the result.  Thread t holds the
+// sample elements e = u * kSampleThreads + t, u < kSamplePer, as key_of(u, pos).
+constexpr int kSamplePer = kSampleBlocks * 32 / kSampleThreads;   // sample elements per thread
+
+__device__ __forceinline__ int64_t sample_count(int len, int64_t sb) {
+  return ((((int64_t)len + 31) / 32 + sb - 1) / sb) * 32;          // upper bound (ragged end)
+}
+__device__ __forceinline__ int64_t sample_pos(int64_t e, int64_t sb) {
+  return (e / 32) * 32 * sb + (e % 32);
+}
+
+template <typename KeyOf>
+__device__ uint32_t sample_threshold(KeyOf key_of, int len, int k, uint32_t* h, uint32_t* warp_sums,
                                      int* s_d, uint32_t* s_above, uint32_t* s_n) {
   const int64_t sb = sample_stride(len);
-  const int64_t ns = ((((int64_t)len + 31) / 32 + sb - 1) / sb) * 32;   // upper bound (ragged end)
-  auto sample_pos = [&](int64_t e) { return (e / 32) * 32 * sb + (e % 32); };
+  const int64_t ns = sample_count(len, sb);
   // rank rho in the sample ~ 1.5 k / sb + 32 (about 1.5 k + 32 sb candidates in the row)
   const uint32_t rho = (uint32_t)((3 * (int64_t)k + 2 * sb - 1) / (2 * sb)) + 32;
   for (int i = threadIdx.x; i < kTopkBins1; i += kSampleThreads) h[i] = 0;
   if (threadIdx.x == 0) *s_n = 0;
   __syncthreads();
   uint32_t n_local = 0;
-  for (int64_t b = 0; b < ns; b += kSampleThreads) {              // uniform trip count
-    const int64_t e = b + threadIdx.x;
-    const int64_t pos = sample_pos(e);
+#pragma unroll
+  for (int u = 0; u < kSamplePer; ++u) {                          // uniform trip count
+    const int64_t e = (int64_t)u * kSampleThreads + threadIdx.x;
+    const int64_t pos = sample_pos(e, sb);
     const bool v = e < ns && pos < len;
-    const uint32_t key = v ? key_at(pos) : 0u;
+    const uint32_t key = v ? key_of(u, pos) : 0u;
     n_local += v ? 1u : 0u;
     hist_add(h, key >> 21, v);
   }
@@ -159,11 +169,12 @@ __device__ uint32_t sample_threshold(KeyAt key_at, int len, int k, uint32_t* h, 
   __syncthreads();
   for (int i = threadIdx.x; i < kTopkBins1; i += kSampleThreads) h[i] = 0;
   __syncthreads();
-  for (int64_t b = 0; b < ns; b += kSampleThreads) {
-    const int64_t e = b + threadIdx.x;
-    const int64_t pos = sample_pos(e);
+#pragma unroll
+  for (int u = 0; u < kSamplePer; ++u) {
+    const int64_t e = (int64_t)u * kSampleThreads + threadIdx.x;
+    const int64_t pos = sample_pos(e, sb);
     const bool v = e < ns && pos < len;
-    const uint32_t key = v ? key_at(pos) : 0u;
+    const uint32_t key = v ? key_of(u, pos) : 0u;
     hist_add(h, (key >> 10) & 0x7FF, v && (key >> 21) == d1);
   }
   __syncthreads();
@@ -187,8 +198,18 @@ topk_sample_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
   __shared__ int s_d;
   __shared__ uint32_t s_above, s_n;
   const float* row = scores + (size_t)r * ld;
-  const uint32_t t = sample_threshold([&](int64_t pos) { return ordered_key(row[pos]); }, len, k,
-                                      h, warp_sums, &s_d, &s_above, &s_n);
+  // every sample load is issued before the first is used: one memory round trip
+  const int64_t sb = sample_stride(len);
+  const int64_t ns = sample_count(len, sb);
+  uint32_t sk[kSamplePer];
+#pragma unroll
+  for (int u = 0; u < kSamplePer; ++u) {
+    const int64_t e = (int64_t)u * kSampleThreads + threadIdx.x;
+    const int64_t pos = sample_pos(e, sb);
+    sk[u] = (e < ns && pos < len) ? ordered_key(__ldg(row + pos)) : 0u;
+  }
+  const uint32_t t = sample_threshold([&](int u, int64_t) { return sk[u]; }, len, k, h, warp_sums,
+                                      &s_d, &s_above, &s_n);
   if (threadIdx.x == 0) tau[r] = t;
 }
 
@@ -554,7 +575,7 @@ topk_row_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __r
           ordered_key(v[u].x), ordered_key(v[u].y), ordered_key(v[u].z), ordered_key(v[u].w));
   }
   __syncthreads();
-  const uint32_t tau = sample_threshold([&](int64_t p) { return keys[p]; }, len, k, S.h,
+  const uint32_t tau = sample_threshold([&](int, int64_t p) { return keys[p]; }, len, k, S.h,
                                         S.warp_sums, &S.d, &S.above, &S.acc[0]);
   // candidates: keys >= tau, counted per warp segment, then placed in position order
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
