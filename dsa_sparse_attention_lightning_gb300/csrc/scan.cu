@@ -31,10 +31,10 @@
 //    ReLU-weighted head sum is a per-thread loop: no shuffles.
 //  * Persistent CTAs, one per SM, each taking a contiguous run of (group,
 //    tile) work items; warp roles: 0-1 MMA issuers (tile i by warp i % 2;
-//    warp 0 owns TMEM), 2-4 TMA producers (keys, key scales, group queries;
-//    page ids looked up 32 tiles ahead; tile i is loaded by producer i % 3
+//    warp 0 owns TMEM), 2-5 TMA producers (keys, key scales, group queries;
+//    page ids looked up 32 tiles ahead; tile i is loaded by producer i % 4
 //    -- the TMA loads one thread issues complete at well under the HBM
-//    rate, so each SM runs three streams), 5-20 epilogue in two groups of
+//    rate, so each SM runs four streams), 6-21 epilogue in two groups of
 //    eight that take alternate tiles (TMEM -> scores; a warp takes TMEM
 //    lane quarter w % 4, i.e. 32 tokens, of two of the group's rows).  A key
 //    stage is released by the MMA's completion alone; the key scales live in
@@ -55,14 +55,14 @@ constexpr int kMaxGroupRows = 4;
 constexpr int kQAtom = kMaxGroupRows * kIdxHeads * kIdxDim;  // 128 rows x 128 B: one query term
 constexpr int kQBytes = 2 * kQAtom;                     // one group's query operand (hi, lo)
 constexpr int kQBufs = 1;
-constexpr int kStages = 6;                              // key tiles in flight per SM
+constexpr int kStages = 8;                              // key tiles in flight per SM
 constexpr int kKeyTileBytes = kTileTok * kIdxDim;       // 2 pages x 64 x 128 B
 constexpr int kPageKeyBytes = kPage * kIdxDim;          // 8192
 constexpr int kPageBytes = kPage * (kIdxDim + 4);       // 8448: keys, then 64 f32 scales
-constexpr int kScRing = 12;                             // key-scale slots (outlive their key stage)
+constexpr int kScRing = 16;                             // key-scale slots (outlive their key stage)
 constexpr int kMmaWarps = 2;                            // warps 0-1: lane 0 issues tiles i % 2 == warp
-constexpr int kProdWarps = 3;                           // warps 2-4: one TMA stream per warp
-constexpr int kEpiWarp0 = kMmaWarps + kProdWarps;       // warps 5-20
+constexpr int kProdWarps = 4;                           // warps 2-5: one TMA stream per warp
+constexpr int kEpiWarp0 = kMmaWarps + kProdWarps;       // warps 6-21
 constexpr int kEpiGroups = 2;                           // epilogue group g takes tiles i % 2 == g
 constexpr int kEpiWarpsPerGroup = 8;
 constexpr int kEpiWarps = kEpiGroups * kEpiWarpsPerGroup;
