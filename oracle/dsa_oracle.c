@@ -13,6 +13,9 @@
  *   - oracle_e4m3_decode       the OCP FP8 E4M3 ("E4M3FN") value of a byte
  *   - oracle_indexer_scores    lightning-indexer score of every visible token
  *   - oracle_topk              top-k positions, ties to the lower token index
+ *   - oracle_topk_dcp          the same top-k by the decode-context-parallel
+ *                              exchange (W token shards, candidates, cutoff,
+ *                              resend of shards that may hide winners)
  *   - oracle_sparse_mla        exact softmax attention over the selected rows
  *
  * Sources (web pages on Kimi K3.1 Pro's sparse attention):
@@ -25,7 +28,9 @@
  *          the paragraph after it) and "Sparse attention cuts long-context
  *          decode bandwidth".
  *   [SGL]  "Kimi K3.1 Pro: Day-0 Inference and RL Support with SGLang and
- *          Miles", section "What's new in Kimi K3.1 Pro".
+ *          Miles", sections "What's new in Kimi K3.1 Pro" and "Decode: DSA
+ *          with decode context parallelism".
+ *   [VLLM] also section "An exact top-k merge with about 10x less traffic".
  *   [AMD]  "Kimi K3.1 Pro on AMD Instinct GPUs" (dev48.org, in Russian),
  *          overview table, row "MLA" (KV LoRA rank 512 + 64 RoPE dims).
  *
@@ -222,6 +227,89 @@ int oracle_topk(const double* scores, int64_t ld, const int32_t* row_len, int R,
         for (int j = 0; j < k; ++j)
             idx[(size_t)r * k + j] = (j < len) ? items[j].index : -1;
         free(items);
+    }
+    return ORA_OK;
+}
+
+/*
+ * Top-k by the decode-context-parallel exchange ([SGL] "Decode: DSA with
+ * decode context parallelism": token p lives on GPU p mod W, each GPU ranks
+ * its own tokens, shares its best candidates, takes the k-th best shared
+ * score as the cutoff, and a GPU whose candidates all beat the cutoff has its
+ * full local top-k read; [VLLM] "An exact top-k merge with about 10x less
+ * traffic": 1.5 k / W candidates per GPU, a resend when a GPU may hold more
+ * winners than it sent).  The W shards are taken in turn here.  Per row, in
+ * the order of oracle_topk (score descending, token index ascending):
+ *   1. shard s owns tokens p < row_len with p % W == s (n_s of them) and
+ *      orders them; its local top-k is its first min(k, n_s) tokens;
+ *   2. it sends its first min(c, n_s) tokens, c = ceil(1.5 k / W);
+ *   3. the cutoff E is the k-th of all sent tokens in the order (there is no
+ *      cutoff when fewer than k were sent);
+ *   4. shard s may hide winners when it kept tokens back (n_s > c) and there
+ *      is no cutoff or its c-th token precedes E (a token it kept back comes
+ *      after its c-th in the order, so otherwise it comes after E); the full
+ *      local top-k of such a shard is gathered;
+ *   5. the result is the top-k of the gathered tokens (the sent ones and the
+ *      resent local top-ks).
+ * idx[r][0..k) receives it in rank order, -1 padded; resend[r] has bit s set
+ * when shard s's local top-k was gathered.
+ * Pinned by: equality with oracle_topk on random, tied, short and
+ * shard-concentrated rows for several W; the resend pattern of rows built so
+ * that one shard holds every winner, none does, or all tie.
+ */
+int oracle_topk_dcp(const double* scores, int64_t ld, const int32_t* row_len, int R, int k,
+                    int W, int32_t* idx, uint32_t* resend) {
+    if (k < 1 || W < 1 || W > 32) return ORA_BAD_ARG;
+    for (int r = 0; r < R; ++r)
+        if (row_len[r] < 0 || (int64_t)row_len[r] > ld) return ORA_BAD_ARG;
+    const int64_t c = (3 * (int64_t)k + 2 * W - 1) / (2 * W);
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < R; ++r) {
+        const int64_t len = row_len[r];
+        const double* row = scores + (size_t)r * ld;
+        ora_item* all = (ora_item*)malloc(sizeof(ora_item) * (size_t)(len > 0 ? len : 1));
+        ora_item* sent = (ora_item*)malloc(sizeof(ora_item) * (size_t)(len > 0 ? len : 1));
+        ora_item* gathered = (ora_item*)malloc(sizeof(ora_item) * (size_t)(len > 0 ? len : 1));
+        int64_t start[33], n[32];
+        /* 1. each shard's own tokens, ordered (stored one shard after the other) */
+        int64_t off = 0;
+        for (int s = 0; s < W; ++s) {
+            start[s] = off;
+            n[s] = 0;
+            for (int64_t p = s; p < len; p += W) {
+                all[off + n[s]].score = row[p];
+                all[off + n[s]].index = (int32_t)p;
+                ++n[s];
+            }
+            qsort(all + off, (size_t)n[s], sizeof(ora_item), ora_item_cmp);
+            off += n[s];
+        }
+        /* 2. the sent candidates; 3. the cutoff */
+        int64_t nsent = 0;
+        for (int s = 0; s < W; ++s)
+            for (int64_t j = 0; j < n[s] && j < c; ++j) sent[nsent++] = all[start[s] + j];
+        qsort(sent, (size_t)nsent, sizeof(ora_item), ora_item_cmp);
+        const int has_cut = nsent >= k;
+        ora_item cut = {0.0, 0};
+        if (has_cut) cut = sent[k - 1];
+        /* 4. shards that may hide winners */
+        uint32_t mask = 0;
+        for (int s = 0; s < W; ++s)
+            if (n[s] > c && (!has_cut || ora_item_cmp(&all[start[s] + c - 1], &cut) < 0))
+                mask |= 1u << s;
+        /* 5. the top-k of everything gathered */
+        int64_t ng = 0;
+        for (int s = 0; s < W; ++s) {
+            const int64_t m = ((mask >> s) & 1u) ? (n[s] < k ? n[s] : k) : (n[s] < c ? n[s] : c);
+            for (int64_t j = 0; j < m; ++j) gathered[ng++] = all[start[s] + j];
+        }
+        qsort(gathered, (size_t)ng, sizeof(ora_item), ora_item_cmp);
+        for (int j = 0; j < k; ++j)
+            idx[(size_t)r * k + j] = (j < len && j < ng) ? gathered[j].index : -1;
+        resend[r] = mask;
+        free(all);
+        free(sent);
+        free(gathered);
     }
     return ORA_OK;
 }

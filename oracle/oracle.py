@@ -65,6 +65,8 @@ def _load():
         lib.oracle_indexer_scores.restype = ctypes.c_int
         lib.oracle_topk.argtypes = [P, i64, P, i32, i32, P]
         lib.oracle_topk.restype = ctypes.c_int
+        lib.oracle_topk_dcp.argtypes = [P, i64, P, i32, i32, i32, P, P]
+        lib.oracle_topk_dcp.restype = ctypes.c_int
         lib.oracle_sparse_mla.argtypes = [P, i32, dbl, P, i64, dbl, P, i32, i32, P, P, P, i32, i32,
                                           P, P]
         lib.oracle_sparse_mla.restype = ctypes.c_int
@@ -135,6 +137,24 @@ def topk(scores, row_len, k):
     if st != 0:
         raise ValueError(f"oracle_topk failed with status {st}")
     return idx
+
+
+def topk_dcp(scores, row_len, k, W):
+    """Top-k by the decode-context-parallel exchange over W token shards.
+
+    Returns (idx int32 [R, k] in rank order, -1 padded; resend uint32 [R],
+    bit s set when shard s's full local top-k was gathered)."""
+    lib = _load()
+    scores = _c(scores, np.float64)
+    R, ld = scores.shape
+    row_len = _c(row_len, np.int32)
+    idx = np.empty((R, k), dtype=np.int32)
+    resend = np.empty(R, dtype=np.uint32)
+    st = lib.oracle_topk_dcp(_ptr(scores), ld, _ptr(row_len), R, int(k), int(W), _ptr(idx),
+                             _ptr(resend))
+    if st != 0:
+        raise ValueError(f"oracle_topk_dcp failed with status {st}")
+    return idx, resend
 
 
 def sparse_mla(q, softmax_scale, latent_cache, latent_scale, block_table, row_req, row_len, idx):

@@ -32,6 +32,9 @@ MUTATIONS = [
      "mag = ldexp((double)m / 8.0, -7);"),
     ("e4m3_bias", "mag = ldexp(1.0 + (double)m / 8.0, e - 7);",
      "mag = ldexp(1.0 + (double)m / 8.0, e - 8);"),
+    ("dcp_never_resends", "                mask |= 1u << s;", "                mask |= 0u;"),
+    ("dcp_suspicion_inverted", "ora_item_cmp(&all[start[s] + c - 1], &cut) < 0",
+     "ora_item_cmp(&all[start[s] + c - 1], &cut) > 0"),
 ]
 
 PIN_TESTS = [
@@ -41,6 +44,8 @@ PIN_TESTS = [
     pins.test_indexer_relu_is_per_head_before_weighting,
     pins.test_indexer_einsum_crosscheck,
     lambda m: [pins.test_topk_brute_force_with_ties(m, L, k) for L, k in [(100, 8), (1000, 64)]],
+    lambda m: pins.test_topk_dcp_equals_single_shard_topk(m, 8),
+    pins.test_topk_dcp_resend_pattern,
     pins.test_mla_dense_matches_sdpa,
     pins.test_mla_single_token_and_zero_query,
     pins.test_mla_split_merge_by_lse,

@@ -266,6 +266,55 @@ def test_topk_len_below_k_and_zero(oracle_mod):
     assert np.array_equal(oracle_mod.topk(s, [0], 2)[0], [-1, -1])
 
 
+# ------------------------------------------- top-k by the context-parallel exchange
+# The pages state the invariant: the merged selection matches a single-GPU
+# top-k exactly (SGLang post, "Decode: DSA with decode context parallelism";
+# vLLM post, "An exact top-k merge with about 10x less traffic").
+def _dcp_rows(rng, L, W):
+    base = rng.standard_normal(L)
+    conc = base.copy()
+    conc[(W - 1)::W] += 10.0                    # shard W-1 holds every winner
+    first = base.copy()
+    first[:: 2 * W] += 10.0                     # half of shard 0's tokens win
+    ties = rng.integers(0, 20, L).astype(np.float64)
+    return np.stack([base, conc, first, ties, np.zeros(L)])
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 8])
+def test_topk_dcp_equals_single_shard_topk(oracle_mod, W):
+    rng = np.random.default_rng(20 + W)
+    L = 6000
+    s = _dcp_rows(rng, L, W)
+    for k in (7, 300, 2048):
+        for lens in ([L] * 5, [L, 5000, 4097, 2 * W + 1, W - 1 if W > 1 else 0]):
+            got, _ = oracle_mod.topk_dcp(s, lens, k, W)
+            assert np.array_equal(got, oracle_mod.topk(s, lens, k))
+            for r in range(s.shape[0]):
+                assert np.array_equal(got[r], _brute_topk(s[r], lens[r], k))
+
+
+def test_topk_dcp_resend_pattern(oracle_mod):
+    W, k, L = 8, 2048, 32768
+    rng = np.random.default_rng(3)
+    base = rng.standard_normal(L)
+    conc = base.copy()
+    conc[3::W] += 10.0                          # shard 3: 4096 tokens above all others
+    s = np.stack([conc, base, np.zeros(L)])
+    idx, mask = oracle_mod.topk_dcp(s, [L, L, L], k, W)
+    # only the shard holding every winner can hide any; spread winners (about
+    # 256 per shard, below the 384 sent) and all-equal scores (the lowest
+    # 2048 positions, 256 per shard) need no resend
+    assert list(mask) == [1 << 3, 0, 0]
+    assert np.all(idx[0] % W == 3)
+    assert np.array_equal(idx[0], _brute_topk(conc, L, k))
+    # one shard holds everything: 1.5 k candidates always cover the top-k
+    _, m1 = oracle_mod.topk_dcp(s, [L, L, L], k, 1)
+    assert list(m1) == [0, 0, 0]
+    # short rows: no shard keeps a token back
+    _, m2 = oracle_mod.topk_dcp(s, [300, 3000, 0], k, W)
+    assert list(m2) == [0, 0, 0]
+
+
 # ------------------------------------------------------------------ sparse MLA
 def _mla_case(rng, n, H):
     codes = _e4m3(np.clip(rng.standard_normal((n, LAT)) * 100, -448, 448))
