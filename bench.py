@@ -264,6 +264,24 @@ def run_gpu(args):
             g.replay()
         stage_ms[name] = _time_launches(g.replay, max(20, min(args.steps, 200)), flush, stream)[0]
     eager_ms = _time_launches(step_eager, max(20, min(args.steps, 200)), flush, stream)[0]
+
+    # ---- the same selection by the decode-context-parallel exchange (8 token
+    # shards emulated on this GPU), on the step's scores
+    DCP_W = 8
+    dcp_idx = torch.empty((R, wl.k), dtype=torch.int32, device=dev)
+    dcp_res = torch.empty((R,), dtype=torch.int32, device=dev)
+    ws_d = torch.empty(dsa.topk_dcp_workspace_size(R, scores.shape[1], wl.k, DCP_W),
+                       dtype=torch.uint8, device=dev)
+    dcp_fn = lambda: dsa.dsa_topk_dcp(scores, inp["row_len"], wl.k, DCP_W, idx=dcp_idx,  # noqa: E731
+                                      resend=dcp_res, workspace=ws_d)
+    g = _graph(dcp_fn, stream)
+    for _ in range(3):
+        g.replay()
+    dcp_ms = _time_launches(g.replay, max(20, min(args.steps, 200)), flush, stream)[0]
+    torch.cuda.synchronize()
+    dcp = {"shards": DCP_W, "us": round(dcp_ms * 1e3, 2), "topk_us": round(stage_ms["topk"] * 1e3, 2),
+           "rows_with_resend": int((dcp_res != 0).sum().item()),
+           "equals_topk": bool(torch.equal(dcp_idx, idx))}
     dominant = max((n for n in stages if stages[n][1] is not None), key=lambda n: stage_ms[n])
     hbm_peak, bf16_peak, peak_kind = _peaks()
     fp8_peak = bf16_peak * FP8_PER_BF16
@@ -347,6 +365,7 @@ def run_gpu(args):
                         "the KV caches are resident layer state"},
         "roofline": roofline,
         "tensor": tensor,
+        "dcp_topk": dcp,
         "eager_ms_per_step": round(eager_ms, 5),
         "cpu_baseline": cpu,
         "gpu_launches": KERNELS_PER_STEP * args.steps,

@@ -43,6 +43,8 @@ SIGNATURES = [
                                         P]),
     ("dsa_topk_workspace_size", SZ, [I32, I64, I32]),
     ("dsa_topk", I32, [P, I64, P, I32, I64, I32, P, P, SZ, P]),
+    ("dsa_topk_dcp_workspace_size", SZ, [I32, I64, I32, I32]),
+    ("dsa_topk_dcp", I32, [P, I64, P, I32, I64, I32, I32, P, P, P, SZ, P]),
     ("dsa_sparse_mla_workspace_size", SZ, [I32, I32, I32]),
     ("dsa_sparse_mla_decode", I32, [P, I32, F32, P, I64, F32, P, I32, I32, P, P, P, I32, I32, P,
                                     P, P, SZ, P]),
@@ -187,6 +189,30 @@ def dsa_topk(scores, row_len, k, *, max_len=None, idx=None, workspace=None):
     _check("dsa_topk", load().dsa_topk(_ptr(scores), ld, _ptr(row_len), R, max_len, int(k),
                                        _ptr(idx), _ptr(ws), ws.numel(), _stream(dev)))
     return idx
+
+
+def topk_dcp_workspace_size(R: int, max_len: int, k: int, W: int) -> int:
+    return int(load().dsa_topk_dcp_workspace_size(int(R), int(max_len), int(k), int(W)))
+
+
+def dsa_topk_dcp(scores, row_len, k, W, *, max_len=None, idx=None, resend=None, workspace=None):
+    """(idx int32 [R, k], resend uint32 [R]): dsa_topk by the context-parallel exchange."""
+    dev = scores.device
+    _need(scores, "scores", torch.float32, dev)
+    _need(row_len, "row_len", torch.int32, dev)
+    R, ld = scores.shape
+    max_len = ld if max_len is None else int(max_len)
+    if idx is None:
+        idx = torch.empty((R, k), dtype=torch.int32, device=dev)
+    if resend is None:
+        resend = torch.empty((R,), dtype=torch.int32, device=dev)
+    _need(idx, "idx", torch.int32, dev)
+    _need(resend, "resend", torch.int32, dev)
+    ws = _workspace(topk_dcp_workspace_size(R, max_len, k, W), dev, workspace)
+    _check("dsa_topk_dcp", load().dsa_topk_dcp(_ptr(scores), ld, _ptr(row_len), R, max_len, int(k),
+                                               int(W), _ptr(idx), _ptr(resend), _ptr(ws),
+                                               ws.numel(), _stream(dev)))
+    return idx, resend
 
 
 def sparse_mla_workspace_size(R: int, H: int, k: int) -> int:

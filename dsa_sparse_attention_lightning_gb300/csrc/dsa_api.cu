@@ -179,6 +179,32 @@ int dsa_topk(const float* scores, int64_t ld, const int32_t* row_len, int R, int
   return to_status(launch_topk(a, st));
 }
 
+// ------------------------------------ Select under decode context parallelism
+size_t dsa_topk_dcp_workspace_size(int R, int64_t max_len, int k, int W) {
+  if (R < 0 || max_len < 0 || k < 1 || W < 1) return 0;
+  return kStatusBytes + dcp_scratch_bytes(R, max_len, k, W);
+}
+
+int dsa_topk_dcp(const float* scores, int64_t ld, const int32_t* row_len, int R, int64_t max_len,
+                 int k, int W, int32_t* idx, uint32_t* resend, void* workspace, size_t ws_bytes,
+                 void* stream) {
+  if (R < 0 || max_len < 0 || ld < max_len || ld % 4 != 0) return DSA_ERR_INVALID_ARG;
+  if (k < 1 || W < 1) return DSA_ERR_INVALID_ARG;
+  if (k > kMaxTopk || W > DSA_MAX_DCP_SHARDS) return DSA_ERR_UNSUPPORTED;
+  if (max_len > ((int64_t)1 << 31) - 1) return DSA_ERR_UNSUPPORTED;
+  if ((int64_t)R * W > 65535) return DSA_ERR_UNSUPPORTED;
+  if (R > 0 && (!scores || !row_len || !idx)) return DSA_ERR_INVALID_ARG;
+  if (scores && !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
+  int s = check_workspace(workspace, ws_bytes, dsa_topk_dcp_workspace_size(R, max_len, k, W));
+  if (s) return s;
+  cudaStream_t st = as_stream(stream);
+  if ((s = clear_status(workspace, st))) return s;
+  if (R == 0) return DSA_OK;
+  DcpArgs a{scores, ld, row_len, R, max_len, k, W, idx, resend,
+            static_cast<uint8_t*>(workspace) + kStatusBytes, static_cast<uint32_t*>(workspace)};
+  return to_status(launch_topk_dcp(a, st));
+}
+
 // ---------------------------------------------------------------- Attend
 size_t dsa_sparse_mla_workspace_size(int R, int H, int k) {
   if (R < 0 || H < 1 || k < 1) return 0;

@@ -197,6 +197,18 @@ struct TopkArgs {
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st);
 
+// Top-k under decode context parallelism, W token shards emulated on one GPU
+// (dcp.cu): every row's result equals launch_topk's.
+struct DcpArgs {
+  const float* scores; int64_t ld; const int32_t* row_len; int R; int64_t max_len; int k; int W;
+  int32_t* idx; uint32_t* resend;  // resend [R] or NULL: bit s = shard s's local top-k was read
+  uint8_t* scratch;                // dcp_scratch_bytes(R, max_len, k, W) bytes
+  uint32_t* status;
+  bool chained = false;
+};
+size_t dcp_scratch_bytes(int R, int64_t max_len, int k, int W);
+cudaError_t launch_topk_dcp(const DcpArgs& a, cudaStream_t st);
+
 struct MlaArgs {
   const void* q; int H; float softmax_scale; const uint8_t* latent_cache; int64_t num_pages;
   float latent_scale; const int32_t* block_table; int B; int max_pages; const int32_t* row_req;

@@ -176,6 +176,33 @@ int dsa_topk(const float* scores, int64_t ld, const int32_t* row_len, int R, int
              int k, int32_t* idx, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * dsa_topk_dcp -- step 2 as decode context parallelism runs it, the W GPUs
+ * emulated on one.
+ *
+ * Token p of a row belongs to shard p mod W (SGLang post on Kimi K3.1 Pro,
+ * "Decode: DSA with decode context parallelism": token p is stored on GPU
+ * p mod 8).  Each shard ranks its own tokens; it shares its best
+ * c = ceil(1.5 k / W) (vLLM post, "An exact top-k merge with about 10x less
+ * traffic"); the k-th best shared token is the cutoff; a shard that kept
+ * tokens back and whose c-th candidate still beats the cutoff may hide
+ * winners, so its full local top-k joins the shared candidates; the top-k of
+ * those is the result.  Order and ties as dsa_topk, so idx equals what
+ * dsa_topk returns for the same scores (the exchange is exact).
+ *
+ *  scores, ld, row_len, max_len, k, idx: as dsa_topk.
+ *  W       shards, 1..DSA_MAX_DCP_SHARDS; R * W <= 65535.
+ *  resend  uint32 [R] or NULL: bit s set when shard s's full local top-k was
+ *          read (the exchange's second round).
+ * Errors: DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED (k > 2048, W > 32,
+ * R * W > 65535), DSA_ERR_WORKSPACE, DSA_ERR_CUDA; device-side DSA_DEV_BAD_ROW.
+ * ---------------------------------------------------------------------- */
+#define DSA_MAX_DCP_SHARDS 32
+size_t dsa_topk_dcp_workspace_size(int R, int64_t max_len, int k, int W);
+int dsa_topk_dcp(const float* scores, int64_t ld, const int32_t* row_len, int R, int64_t max_len,
+                 int k, int W, int32_t* idx, uint32_t* resend, void* workspace, size_t ws_bytes,
+                 void* stream);
+
+/* ------------------------------------------------------------------------
  * dsa_sparse_mla_decode -- step 3 alone (Attend).
  *
  * For row r, head h and the valid selected tokens j (0 <= idx[r][j] <

@@ -170,6 +170,58 @@ def test_topk_long_row_split_over_chunks(dsa, oracle_mod):
     _topk_bitexact(dsa, oracle_mod, s, [L], 2048)
 
 
+# ------------------------------------------- top-k by the context-parallel exchange
+def _dcp_rows(rng, L, W):
+    base = rng.standard_normal(L).astype(np.float32)
+    conc = base.copy()
+    conc[(W - 1)::W] += 10.0                    # shard W-1 holds every winner
+    first = base.copy()
+    first[:: 2 * W] += 10.0                     # half of shard 0's tokens win
+    ties = rng.integers(0, 20, L).astype(np.float32)
+    return np.stack([base, conc, first, ties, np.zeros(L, np.float32)])
+
+
+def _dcp_check(dsa, oracle_mod, s32, lens, k, W):
+    sc = torch.from_numpy(s32).to(DEV)
+    rl = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    g_idx, g_res = dsa.dsa_topk_dcp(sc, rl, k, W)
+    t_idx = dsa.dsa_topk(sc, rl, k)
+    torch.cuda.synchronize()
+    g_idx, t_idx = g_idx.cpu().numpy(), t_idx.cpu().numpy()
+    assert np.array_equal(g_idx, t_idx), "exchange differs from the single-shard top-k"
+    o_idx, o_res = oracle_mod.topk_dcp(s32.astype(np.float64), lens, k, W)
+    assert np.array_equal(g_res.cpu().numpy().view(np.uint32), o_res), "resend pattern"
+    for r in range(s32.shape[0]):
+        n = min(k, lens[r])
+        assert np.array_equal(g_idx[r, :n], np.sort(o_idx[r, :n]))
+        assert np.all(g_idx[r, n:] == -1)
+    return o_res
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 8])
+def test_topk_dcp_matches_topk_and_oracle(dsa, oracle_mod, W):
+    rng = np.random.default_rng(40 + W)
+    L = 20000
+    s32 = _dcp_rows(rng, L, W)
+    for k in (7, 300, 2048):
+        for lens in ([L] * 5, [L, 5000, 4097, 2 * W + 1, max(W - 1, 0)]):
+            _dcp_check(dsa, oracle_mod, s32, lens, k, W)
+
+
+def test_topk_dcp_full_size_rows(dsa, oracle_mod):
+    """256K rows (shards of 32K: one-CTA top-k; the member rows: the
+    sample / collect path) and one 1M row, eight shards."""
+    rng = np.random.default_rng(7)
+    W, k = 8, 2048
+    s32 = _dcp_rows(rng, 262144, W)[:3]
+    res = _dcp_check(dsa, oracle_mod, s32, [262144, 262144, 200000], k, W)
+    assert res[1] == 1 << (W - 1)
+    big = rng.standard_normal((1, 1 << 20)).astype(np.float32)
+    big[0, 5::W] += 5.0
+    res = _dcp_check(dsa, oracle_mod, big, [1 << 20], k, W)
+    assert res[0] == 1 << 5
+
+
 # --------------------------------------------------------------- sparse MLA
 @pytest.mark.parametrize("wl", SMALL + MLA_WIDE, ids=[w.name for w in SMALL + MLA_WIDE])
 def test_sparse_mla_matches_oracle(dsa, oracle_mod, wl):
