@@ -17,6 +17,10 @@
  *                              exchange (W token shards, candidates, cutoff,
  *                              resend of shards that may hide winners)
  *   - oracle_sparse_mla        exact softmax attention over the selected rows
+ *   - oracle_e4m3_encode       nearest E4M3 value of a real (ties to even)
+ *   - oracle_write_kv          the Write step: LayerNorm of a new token's index
+ *                              key, FP8 quantization with one scale, paged
+ *                              write; the latent row's FP8 write
  *
  * Sources (web pages on Kimi K3.1 Pro's sparse attention):
  *   [TS]   TokenSpeed post on Kimi K3.1 Pro (lightseek.org), sections
@@ -111,6 +115,102 @@ static double f32_at(const uint8_t* p) {
     float f;
     memcpy(&f, p, sizeof f);
     return (double)f;
+}
+
+/*
+ * E4M3 encoding of a real value, the inverse of oracle_e4m3_decode on the
+ * finite codes: the nearest finite E4M3 value, a tie going to the code whose
+ * mantissa is even (round to nearest even), magnitudes of 448 and above
+ * saturating to 448 ("satfinite"); the sign is kept (-0 encodes as 0x80).
+ * By brute force over the 127 non-negative finite codes.
+ * Pinned by: the round trip over every finite code, torch's float8_e4m3fn
+ * cast on values in [-448, 448] including every midpoint, golden ties.
+ */
+uint8_t oracle_e4m3_encode(double x) {
+    const int sign = signbit(x) ? 1 : 0;
+    const double a = fabs(x);
+    if (a >= 448.0) return (uint8_t)((sign << 7) | 0x7E);
+    int best = 0;
+    double bestd = INFINITY;
+    for (int c = 0; c < 0x7F; ++c) {
+        const double d = fabs(a - oracle_e4m3_decode((uint8_t)c));
+        if (d < bestd || (d == bestd && (c & 1) == 0)) {
+            best = c;
+            bestd = d;
+        }
+    }
+    return (uint8_t)((sign << 7) | best);
+}
+
+/*
+ * The Write step ([TS] step 1 "Write": one fused kernel normalizes the new
+ * token's index key, quantizes it to FP8 with a single scale and writes it
+ * into the cache, and one kernel writes the latent row; [TS] "Integrating
+ * sparse attention with the K3 stack": the only key normalization accepted
+ * is LayerNorm; [TS] "Storing index keys in the flat KV cache": 128 FP8
+ * values and one four-byte scale per token).  For new token t of request
+ * tok_req[t] at position tok_pos[t]:
+ *   x      = k_raw[t] (128 bf16 values)
+ *   k      = gamma * (x - mean(x)) / sqrt(var(x) + eps) + beta
+ *            (mean and biased variance over the 128 dims)
+ *   ks     = max_d |k[d]| / 448   (1 when k is all zero)
+ *   codes  = e4m3_encode(k / ks)
+ * go to page block_table[req][pos / 64], slot pos % 64 of key_cache: the 128
+ * codes at slot * 128, ks as fp32 at 64 * 128 + slot * 4; and the latent row
+ * e4m3_encode(latent[t] / latent_scale) (576 bf16 values in) to
+ * latent_cache[page][slot][0..576).  The values before rounding (k / ks and
+ * latent / latent_scale) are returned in key_pre [T][128] and lat_pre
+ * [T][576], and ks in key_scale [T], so that a test can see codes that sit
+ * at a rounding midpoint.
+ * Pinned by: LayerNorm against torch's float64 layer_norm, the absmax code
+ * being exactly 448, a zero key, the latent codes against the generator's
+ * torch cast, placement through a shuffled block table.
+ */
+int oracle_write_kv(const uint16_t* k_raw, const double* gamma, const double* beta, double eps,
+                    const uint16_t* latent, double latent_scale, const int32_t* block_table,
+                    int B, int max_pages, const int32_t* tok_req, const int32_t* tok_pos, int T,
+                    uint8_t* key_cache, uint8_t* latent_cache, int64_t num_pages,
+                    double* key_pre, double* lat_pre, double* key_scale) {
+    if (T < 0 || !(latent_scale > 0.0) || !(eps >= 0.0)) return ORA_BAD_ARG;
+    for (int t = 0; t < T; ++t) {
+        const int req = tok_req[t], pos = tok_pos[t];
+        if (req < 0 || req >= B || pos < 0 || pos >= max_pages * ORA_PAGE) return ORA_BAD_ARG;
+        const int page = block_table[(size_t)req * max_pages + pos / ORA_PAGE];
+        if (page < 0 || (int64_t)page >= num_pages) return ORA_BAD_PAGE;
+        const int slot = pos % ORA_PAGE;
+        /* index key: LayerNorm, absmax scale, E4M3 codes */
+        double x[ORA_IDX_DIM], k[ORA_IDX_DIM];
+        double mean = 0.0, var = 0.0, amax = 0.0;
+        for (int d = 0; d < ORA_IDX_DIM; ++d) {
+            x[d] = bf16_to_double(k_raw[(size_t)t * ORA_IDX_DIM + d]);
+            mean += x[d];
+        }
+        mean /= ORA_IDX_DIM;
+        for (int d = 0; d < ORA_IDX_DIM; ++d) var += (x[d] - mean) * (x[d] - mean);
+        var /= ORA_IDX_DIM;
+        for (int d = 0; d < ORA_IDX_DIM; ++d) {
+            k[d] = gamma[d] * (x[d] - mean) / sqrt(var + eps) + beta[d];
+            if (fabs(k[d]) > amax) amax = fabs(k[d]);
+        }
+        const double ks = amax > 0.0 ? amax / 448.0 : 1.0;
+        uint8_t* kp = key_cache + (size_t)page * ORA_KEY_PAGE_BYTES;
+        for (int d = 0; d < ORA_IDX_DIM; ++d) {
+            const double v = k[d] / ks;
+            kp[(size_t)slot * ORA_IDX_DIM + d] = oracle_e4m3_encode(v);
+            if (key_pre) key_pre[(size_t)t * ORA_IDX_DIM + d] = v;
+        }
+        const float ksf = (float)ks;
+        memcpy(kp + ORA_PAGE * ORA_IDX_DIM + (size_t)slot * 4, &ksf, sizeof ksf);
+        if (key_scale) key_scale[t] = ks;
+        /* latent row */
+        uint8_t* lp = latent_cache + ((size_t)page * ORA_PAGE + slot) * ORA_LAT_DIM;
+        for (int d = 0; d < ORA_LAT_DIM; ++d) {
+            const double v = bf16_to_double(latent[(size_t)t * ORA_LAT_DIM + d]) / latent_scale;
+            lp[d] = oracle_e4m3_encode(v);
+            if (lat_pre) lat_pre[(size_t)t * ORA_LAT_DIM + d] = v;
+        }
+    }
+    return ORA_OK;
 }
 
 /*

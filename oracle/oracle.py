@@ -67,6 +67,11 @@ def _load():
         lib.oracle_topk.restype = ctypes.c_int
         lib.oracle_topk_dcp.argtypes = [P, i64, P, i32, i32, i32, P, P]
         lib.oracle_topk_dcp.restype = ctypes.c_int
+        lib.oracle_e4m3_encode.argtypes = [dbl]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_write_kv.argtypes = [P, P, P, dbl, P, dbl, P, i32, i32, P, P, i32, P, P, i64,
+                                        P, P, P]
+        lib.oracle_write_kv.restype = ctypes.c_int
         lib.oracle_sparse_mla.argtypes = [P, i32, dbl, P, i64, dbl, P, i32, i32, P, P, P, i32, i32,
                                           P, P]
         lib.oracle_sparse_mla.restype = ctypes.c_int
@@ -137,6 +142,39 @@ def topk(scores, row_len, k):
     if st != 0:
         raise ValueError(f"oracle_topk failed with status {st}")
     return idx
+
+
+def e4m3_encode(x: float) -> int:
+    return int(_load().oracle_e4m3_encode(float(x)))
+
+
+def write_kv(k_raw, gamma, beta, eps, latent, latent_scale, block_table, tok_req, tok_pos,
+             key_cache, latent_cache):
+    """The Write step on copies of the caches.
+
+    ``k_raw`` uint16 bf16 bits [T,128], ``latent`` uint16 bf16 bits [T,576].
+    Returns (key_cache, latent_cache, key_pre [T,128], lat_pre [T,576],
+    key_scale [T]): the written caches and the float64 values before rounding."""
+    lib = _load()
+    k_raw = _c(k_raw, np.uint16)
+    latent = _c(latent, np.uint16)
+    T = k_raw.shape[0]
+    block_table = _c(block_table, np.int32)
+    B, max_pages = block_table.shape
+    key_cache = np.array(key_cache, dtype=np.uint8, copy=True, order="C")
+    latent_cache = np.array(latent_cache, dtype=np.uint8, copy=True, order="C")
+    num_pages = key_cache.size // KEY_PAGE_BYTES
+    key_pre = np.zeros((T, IDX_DIM))
+    lat_pre = np.zeros((T, LAT_DIM))
+    key_scale = np.zeros(T)
+    st = lib.oracle_write_kv(_ptr(k_raw), _ptr(_c(gamma, np.float64)), _ptr(_c(beta, np.float64)),
+                             float(eps), _ptr(latent), float(latent_scale), _ptr(block_table), B,
+                             max_pages, _ptr(_c(tok_req, np.int32)), _ptr(_c(tok_pos, np.int32)), T,
+                             _ptr(key_cache), _ptr(latent_cache), num_pages, _ptr(key_pre),
+                             _ptr(lat_pre), _ptr(key_scale))
+    if st != 0:
+        raise ValueError(f"oracle_write_kv failed with status {st}")
+    return key_cache, latent_cache, key_pre, lat_pre, key_scale
 
 
 def topk_dcp(scores, row_len, k, W):

@@ -35,6 +35,10 @@ MUTATIONS = [
     ("dcp_never_resends", "                mask |= 1u << s;", "                mask |= 0u;"),
     ("dcp_suspicion_inverted", "ora_item_cmp(&all[start[s] + c - 1], &cut) < 0",
      "ora_item_cmp(&all[start[s] + c - 1], &cut) > 0"),
+    ("layernorm_unbiased_variance", "var /= ORA_IDX_DIM;", "var /= (ORA_IDX_DIM - 1);"),
+    ("key_scale_next_slot", "memcpy(kp + ORA_PAGE * ORA_IDX_DIM + (size_t)slot * 4,",
+     "memcpy(kp + ORA_PAGE * ORA_IDX_DIM + (size_t)((slot + 1) % ORA_PAGE) * 4,"),
+    ("e4m3_ties_to_odd", "(d == bestd && (c & 1) == 0)", "(d == bestd && (c & 1) == 1)"),
 ]
 
 PIN_TESTS = [
@@ -46,6 +50,9 @@ PIN_TESTS = [
     lambda m: [pins.test_topk_brute_force_with_ties(m, L, k) for L, k in [(100, 8), (1000, 64)]],
     lambda m: pins.test_topk_dcp_equals_single_shard_topk(m, 8),
     pins.test_topk_dcp_resend_pattern,
+    pins.test_e4m3_encode_round_trip_and_torch_cast,
+    pins.test_write_kv_layernorm_scale_codes_and_placement,
+    pins.test_write_kv_zero_key,
     pins.test_mla_dense_matches_sdpa,
     pins.test_mla_single_token_and_zero_query,
     pins.test_mla_split_merge_by_lse,

@@ -315,6 +315,100 @@ def test_topk_dcp_resend_pattern(oracle_mod):
     assert list(m2) == [0, 0, 0]
 
 
+# --------------------------------------------------------------- the Write step
+def _e4m3_midpoints(oracle_mod):
+    vals = sorted({oracle_mod.e4m3_decode(c) for c in range(0x7F)})
+    return np.array([(a + b) / 2 for a, b in zip(vals[:-1], vals[1:])])
+
+
+def _near_midpoint(v, mids, rel=1e-5):
+    """True where |v| lies within rel * |v| of a rounding midpoint of E4M3."""
+    a = np.abs(np.asarray(v, np.float64))
+    j = np.clip(np.searchsorted(mids, a), 1, len(mids) - 1)
+    d = np.minimum(np.abs(a - mids[j - 1]), np.abs(a - mids[j]))
+    return d <= rel * np.maximum(a, 1e-30)
+
+
+def test_e4m3_encode_round_trip_and_torch_cast(oracle_mod):
+    for c in range(256):
+        if c & 0x7F != 0x7F:
+            assert oracle_mod.e4m3_encode(oracle_mod.e4m3_decode(c)) == c, hex(c)
+    # golden ties (round to nearest even): 1.0625 between 1.0 (0x38) and 1.125
+    # (0x39); 1.1875 between 1.125 and 1.25 (0x3A); saturation at 448 (0x7E)
+    assert [oracle_mod.e4m3_encode(v) for v in (1.0625, 1.1875, 600.0, -1000.0)] == \
+        [0x38, 0x3A, 0x7E, 0xFE]
+    mids = _e4m3_midpoints(oracle_mod)
+    rng = np.random.default_rng(0)
+    xs = np.concatenate([rng.uniform(-448, 448, 3000), rng.standard_normal(3000) * 0.02,
+                         mids, -mids]).astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle_mod.e4m3_encode(float(x)) for x in xs], np.uint8)
+    assert np.array_equal(got, ref)
+
+
+def _write_case(rng, T=40, B=3, max_pages=4):
+    num_pages = B * max_pages
+    bt = rng.permutation(num_pages).astype(np.int32).reshape(B, max_pages)
+    req = np.repeat(np.arange(B), T // B + 1)[:T].astype(np.int32)
+    pos = np.zeros(T, np.int32)
+    for b in range(B):
+        sel = req == b
+        pos[sel] = rng.choice(max_pages * PAGE, int(sel.sum()), replace=False)
+    x = rng.standard_normal((T, D)) * 3.0 + 0.5
+    lat = rng.standard_normal((T, LAT))
+    key_cache = np.full((num_pages, PAGE * D + PAGE * 4), 0x7F, np.uint8)
+    latent_cache = np.full((num_pages, PAGE, LAT), 0x7F, np.uint8)
+    return bt, req, pos, x, lat, key_cache, latent_cache
+
+
+def test_write_kv_layernorm_scale_codes_and_placement(oracle_mod):
+    rng = np.random.default_rng(5)
+    bt, req, pos, x, lat, kc0, lc0 = _write_case(rng)
+    gamma = rng.uniform(0.5, 1.5, D)
+    beta = rng.standard_normal(D) * 0.1
+    eps, ls = 1e-6, 0.0125
+    kb, lb = _bf16_bits(x), _bf16_bits(lat)
+    kc, lc, kpre, lpre, ks = oracle_mod.write_kv(kb, gamma, beta, eps, lb, ls, bt, req, pos,
+                                                 kc0, lc0)
+    # LayerNorm: torch's float64 layer_norm of the same bf16 inputs
+    ln = torch.nn.functional.layer_norm(torch.from_numpy(_bf16_vals(kb)), (D,),
+                                        torch.from_numpy(gamma), torch.from_numpy(beta), eps)
+    assert np.allclose(kpre * ks[:, None], ln.numpy(), rtol=0, atol=1e-12)
+    assert np.allclose(ks, np.abs(ln.numpy()).max(1) / 448.0, rtol=1e-15)
+    mids = _e4m3_midpoints(oracle_mod)
+    written = np.zeros(kc0.shape, bool)
+    for t in range(len(req)):
+        page, slot = bt[req[t], pos[t] // PAGE], pos[t] % PAGE
+        codes = kc[page, slot * D:(slot + 1) * D]
+        vals = _e4m3_vals(codes)
+        assert np.abs(vals).max() == 448.0            # the absmax element is exactly 448
+        ref = torch.from_numpy(kpre[t].astype(np.float32)).to(torch.float8_e4m3fn)
+        ok = ~_near_midpoint(kpre[t], mids)
+        assert np.array_equal(codes[ok], ref.view(torch.uint8).numpy()[ok])
+        assert kc[page, PAGE * D + slot * 4:PAGE * D + slot * 4 + 4].view(np.float32)[0] == \
+            np.float32(ks[t])
+        # the latent row: the generator's quantizer (torch cast of the fp32 quotient)
+        lref = torch.from_numpy(_bf16_vals(lb[t]).astype(np.float32) / np.float32(ls))
+        lref = lref.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        lok = ~_near_midpoint(lpre[t], mids)
+        assert np.array_equal(lc[page, slot][lok], lref[lok])
+        written[page, slot * D:(slot + 1) * D] = True
+        written[page, PAGE * D + slot * 4:PAGE * D + slot * 4 + 4] = True
+    assert np.all(kc[~written] == 0x7F)                # nothing else is touched
+
+
+def test_write_kv_zero_key(oracle_mod):
+    rng = np.random.default_rng(6)
+    bt, req, pos, x, lat, kc0, lc0 = _write_case(rng, T=3)
+    x[:] = 1.5                                         # constant key: LayerNorm gives beta = 0
+    kc, _, _, _, ks = oracle_mod.write_kv(_bf16_bits(x), np.ones(D), np.zeros(D), 1e-6,
+                                          _bf16_bits(lat), 1.0, bt, req, pos, kc0, lc0)
+    assert np.all(ks == 1.0)
+    for t in range(3):
+        page, slot = bt[req[t], pos[t] // PAGE], pos[t] % PAGE
+        assert np.all(kc[page, slot * D:(slot + 1) * D] == 0)
+
+
 # ------------------------------------------------------------------ sparse MLA
 def _mla_case(rng, n, H):
     codes = _e4m3(np.clip(rng.standard_normal((n, LAT)) * 100, -448, 448))
