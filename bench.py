@@ -341,6 +341,23 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl, inp)
 
+    # ---- the Write step for the step's new tokens (each row's newest position),
+    # timed last because it overwrites those tokens in the caches
+    gen = torch.Generator(device=dev).manual_seed(wl.seed + 17)
+    k_new = torch.randn((R, inputs.IDX_DIM), device=dev, generator=gen).to(torch.bfloat16)
+    lat_new = torch.randn((R, inputs.LAT_DIM), device=dev, generator=gen).to(torch.bfloat16)
+    ln_w = torch.ones(inputs.IDX_DIM, device=dev)
+    ln_b = torch.zeros(inputs.IDX_DIM, device=dev)
+    new_pos = (inp["row_len"] - 1).clamp(min=0)
+    write_fn = lambda: dsa.dsa_write_kv(k_new, ln_w, ln_b, 1e-6, lat_new,  # noqa: E731
+                                        inp["latent_scale"], inp["block_table"], inp["row_req"],
+                                        new_pos, inp["key_cache"], inp["latent_cache"])
+    g = _graph(write_fn, stream)
+    write_ms = _time_launches(g.replay, max(20, min(args.steps, 200)), flush, stream)[0]
+    write = {"tokens": R, "us": round(write_ms * 1e3, 2),
+             "bytes": R * (inputs.IDX_DIM * 2 + inputs.LAT_DIM * 2 + inputs.IDX_DIM + 4 +
+                           inputs.LAT_DIM)}
+
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank != 0:
@@ -366,6 +383,7 @@ def run_gpu(args):
         "roofline": roofline,
         "tensor": tensor,
         "dcp_topk": dcp,
+        "write": write,
         "eager_ms_per_step": round(eager_ms, 5),
         "cpu_baseline": cpu,
         "gpu_launches": KERNELS_PER_STEP * args.steps,

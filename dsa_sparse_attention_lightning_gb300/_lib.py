@@ -43,6 +43,7 @@ SIGNATURES = [
                                         P]),
     ("dsa_topk_workspace_size", SZ, [I32, I64, I32]),
     ("dsa_topk", I32, [P, I64, P, I32, I64, I32, P, P, SZ, P]),
+    ("dsa_write_kv", I32, [P, P, P, F32, P, F32, P, I32, I32, P, P, I32, P, P, I64, P, P]),
     ("dsa_topk_dcp_workspace_size", SZ, [I32, I64, I32, I32]),
     ("dsa_topk_dcp", I32, [P, I64, P, I32, I64, I32, I32, P, P, P, SZ, P]),
     ("dsa_sparse_mla_workspace_size", SZ, [I32, I32, I32]),
@@ -189,6 +190,29 @@ def dsa_topk(scores, row_len, k, *, max_len=None, idx=None, workspace=None):
     _check("dsa_topk", load().dsa_topk(_ptr(scores), ld, _ptr(row_len), R, max_len, int(k),
                                        _ptr(idx), _ptr(ws), ws.numel(), _stream(dev)))
     return idx
+
+
+def dsa_write_kv(k_raw, gamma, beta, eps, latent, latent_scale, block_table, tok_req, tok_pos,
+                 key_cache, latent_cache, *, dev_status=None):
+    """The Write step: new tokens' index keys and latent rows into the caches (in place)."""
+    dev = key_cache.device
+    _need(k_raw, "k_raw", torch.bfloat16, dev)
+    _need(latent, "latent", torch.bfloat16, dev)
+    _need(gamma, "gamma", torch.float32, dev)
+    _need(beta, "beta", torch.float32, dev)
+    _need(key_cache, "key_cache", torch.uint8, dev)
+    _need(latent_cache, "latent_cache", torch.uint8, dev)
+    for n, t in (("block_table", block_table), ("tok_req", tok_req), ("tok_pos", tok_pos)):
+        _need(t, n, torch.int32, dev)
+    T = k_raw.shape[0]
+    B, max_pages = block_table.shape
+    num_pages = key_cache.numel() // KEY_PAGE_BYTES
+    _check("dsa_write_kv", load().dsa_write_kv(
+        _ptr(k_raw), _ptr(gamma), _ptr(beta), float(eps), _ptr(latent), float(latent_scale),
+        _ptr(block_table), B, max_pages, _ptr(tok_req), _ptr(tok_pos), T, _ptr(key_cache),
+        _ptr(latent_cache), num_pages, _ptr(dev_status) if dev_status is not None else None,
+        _stream(dev)))
+    return key_cache, latent_cache
 
 
 def topk_dcp_workspace_size(R: int, max_len: int, k: int, W: int) -> int:

@@ -179,6 +179,29 @@ int dsa_topk(const float* scores, int64_t ld, const int32_t* row_len, int R, int
   return to_status(launch_topk(a, st));
 }
 
+// ---------------------------------------------------------------- Write
+int dsa_write_kv(const void* k_raw, const float* gamma, const float* beta, float eps,
+                 const void* latent, float latent_scale, const int32_t* block_table, int B,
+                 int max_pages, const int32_t* tok_req, const int32_t* tok_pos, int T,
+                 uint8_t* key_cache, uint8_t* latent_cache, int64_t num_pages,
+                 uint32_t* dev_status, void* stream) {
+  if (T < 0 || B < 0 || max_pages < 0 || num_pages < 0) return DSA_ERR_INVALID_ARG;
+  if (!(latent_scale > 0.f) || !(latent_scale < INFINITY) || !(eps >= 0.f)) return DSA_ERR_INVALID_ARG;
+  if (T > 0 && (B < 1 || max_pages < 1 || !k_raw || !gamma || !beta || !latent || !block_table ||
+                !tok_req || !tok_pos || !key_cache || !latent_cache))
+    return DSA_ERR_INVALID_ARG;
+  if ((k_raw && !aligned(k_raw, 8)) || (latent && !aligned(latent, 16)) ||
+      (gamma && !aligned(gamma, 16)) || (beta && !aligned(beta, 16)) ||
+      (key_cache && !aligned(key_cache, 16)) || (latent_cache && !aligned(latent_cache, 16)))
+    return DSA_ERR_INVALID_ARG;
+  cudaStream_t st = as_stream(stream);
+  if (dev_status && cudaMemsetAsync(dev_status, 0, 4, st) != cudaSuccess) return DSA_ERR_CUDA;
+  if (T == 0) return DSA_OK;
+  WriteArgs a{k_raw, gamma, beta, eps, latent, latent_scale, block_table, B, max_pages,
+              tok_req, tok_pos, T, key_cache, latent_cache, num_pages, dev_status};
+  return to_status(launch_write_kv(a, st));
+}
+
 // ------------------------------------ Select under decode context parallelism
 size_t dsa_topk_dcp_workspace_size(int R, int64_t max_len, int k, int W) {
   if (R < 0 || max_len < 0 || k < 1 || W < 1) return 0;

@@ -197,6 +197,18 @@ struct TopkArgs {
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t st);
 
+// The Write step (write.cu): T new tokens' index keys (LayerNorm, absmax
+// scale, E4M3) and latent rows (E4M3 with the cache's scale) into the caches.
+struct WriteArgs {
+  const void* k_raw; const float* gamma; const float* beta; float eps;
+  const void* latent; float latent_scale; const int32_t* block_table; int B; int max_pages;
+  const int32_t* tok_req; const int32_t* tok_pos; int T;
+  uint8_t* key_cache; uint8_t* latent_cache; int64_t num_pages;
+  uint32_t* status;   // may be NULL: the device checks are then not reported
+  bool chained = false;
+};
+cudaError_t launch_write_kv(const WriteArgs& a, cudaStream_t st);
+
 // Top-k under decode context parallelism, W token shards emulated on one GPU
 // (dcp.cu): every row's result equals launch_topk's.
 struct DcpArgs {

@@ -176,6 +176,42 @@ int dsa_topk(const float* scores, int64_t ld, const int32_t* row_len, int R, int
              int k, int32_t* idx, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * dsa_write_kv -- step 0 (Write): the new tokens' index keys and latent rows
+ * into the paged caches.
+ *
+ * One fused kernel normalizes a new token's index key, quantizes it to FP8
+ * with a single scale and writes it into the cache; the latent row is written
+ * next to it (TokenSpeed post on Kimi K3.1 Pro, "Integrating sparse attention
+ * with the K3 stack", step 1 "Write"; the key normalization is LayerNorm).
+ * For new token t of request tok_req[t] at position tok_pos[t]:
+ *   k     = gamma * (x - mean(x)) / sqrt(var(x) + eps) + beta
+ *           (x = k_raw[t], 128 values; mean and biased variance over them)
+ *   ks    = max|k| / 448 (1 when k is all zero); codes = E4M3(k / ks)
+ *   latent row codes = E4M3(latent[t] / latent_scale)
+ * (E4M3: round to nearest even, saturating at 448), written at page
+ * block_table[req][pos / 64], slot pos % 64, in the layouts of
+ * dsa_indexer_score (key codes, then the fp32 scale in the page's scale
+ * block) and dsa_sparse_mla_decode (576 latent bytes).
+ *
+ *  k_raw        bf16 [T][128], 8-byte aligned.
+ *  gamma, beta  fp32 [128] (LayerNorm weight and bias), 16-byte aligned.
+ *  eps          >= 0.
+ *  latent       bf16 [T][576], 16-byte aligned.
+ *  latent_scale the latent cache's fp32 scale, > 0.
+ *  key_cache, latent_cache  the caches (written in place), 16-byte aligned.
+ *  dev_status   optional device uint32: cleared, then receives the DSA_DEV_*
+ *               bits of tokens skipped for an out-of-range request, position
+ *               or page; NULL to skip the report.
+ * Tokens of one call must not share a (page, slot).  No workspace.
+ * Errors: DSA_ERR_INVALID_ARG, DSA_ERR_CUDA.
+ * ---------------------------------------------------------------------- */
+int dsa_write_kv(const void* k_raw, const float* gamma, const float* beta, float eps,
+                 const void* latent, float latent_scale, const int32_t* block_table, int B,
+                 int max_pages, const int32_t* tok_req, const int32_t* tok_pos, int T,
+                 uint8_t* key_cache, uint8_t* latent_cache, int64_t num_pages,
+                 uint32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
  * dsa_topk_dcp -- step 2 as decode context parallelism runs it, the W GPUs
  * emulated on one.
  *

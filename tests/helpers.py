@@ -50,3 +50,18 @@ def assert_out_close(gpu_out, ora_out):
     assert np.isfinite(err).all(), "non-finite attention output"
     assert err.max() <= OUT_ATOL, f"max |out - oracle| = {err.max():.3g} > {OUT_ATOL}"
     return float(err.max())
+
+
+def e4m3_midpoints(oracle_mod):
+    """Midpoints between consecutive non-negative finite E4M3 values."""
+    vals = sorted({oracle_mod.e4m3_decode(c) for c in range(0x7F)})
+    return np.array([(a + b) / 2 for a, b in zip(vals[:-1], vals[1:])])
+
+
+def near_midpoint(v, mids, rel=1e-5):
+    """True where |v| lies within rel * |v| of an E4M3 rounding midpoint: there
+    fp32 and float64 arithmetic may round to neighbouring codes."""
+    a = np.abs(np.asarray(v, np.float64))
+    j = np.clip(np.searchsorted(mids, a), 1, len(mids) - 1)
+    d = np.minimum(np.abs(a - mids[j - 1]), np.abs(a - mids[j]))
+    return d <= rel * np.maximum(a, 1e-30)

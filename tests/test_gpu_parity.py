@@ -170,6 +170,79 @@ def test_topk_long_row_split_over_chunks(dsa, oracle_mod):
     _topk_bitexact(dsa, oracle_mod, s, [L], 2048)
 
 
+# ------------------------------------------------------------------ the Write step
+def test_write_kv_matches_oracle(dsa, oracle_mod):
+    rng = np.random.default_rng(11)
+    T, B, max_pages = 200, 4, 16
+    num_pages = B * max_pages
+    bt = rng.permutation(num_pages).astype(np.int32).reshape(B, max_pages)
+    req = np.repeat(np.arange(B), T // B).astype(np.int32)
+    pos = np.concatenate([rng.choice(max_pages * 64, T // B, replace=False)
+                          for _ in range(B)]).astype(np.int32)
+    x = (rng.standard_normal((T, 128)) * 3.0 + 0.5).astype(np.float32)
+    x[5] = 1.5                                        # constant key: a zero normalized key
+    lat = rng.standard_normal((T, 576)).astype(np.float32)
+    gamma = rng.uniform(0.5, 1.5, 128).astype(np.float32)
+    beta = (rng.standard_normal(128) * 0.1).astype(np.float32)
+    beta_zero = np.zeros(128, np.float32)
+    eps, ls = 1e-6, 0.0125
+    kc0 = np.full((num_pages, 8448), 0x7F, np.uint8)
+    lc0 = np.full((num_pages, 64, 576), 0x7F, np.uint8)
+    for b_vec in (beta, beta_zero):
+        kb = torch.from_numpy(x).to(torch.bfloat16)
+        lb = torch.from_numpy(lat).to(torch.bfloat16)
+        kc = torch.from_numpy(kc0).to(DEV)
+        lc = torch.from_numpy(lc0).to(DEV)
+        st = torch.full((1,), 7, dtype=torch.int32, device=DEV)
+        dsa.dsa_write_kv(kb.to(DEV), torch.from_numpy(gamma).to(DEV), torch.from_numpy(b_vec).to(DEV),
+                         eps, lb.to(DEV), ls, torch.from_numpy(bt).to(DEV),
+                         torch.from_numpy(req).to(DEV), torch.from_numpy(pos).to(DEV), kc, lc,
+                         dev_status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        kcg, lcg = kc.cpu().numpy(), lc.cpu().numpy()
+        okc, olc, kpre, lpre, ks = oracle_mod.write_kv(
+            kb.view(torch.int16).numpy().view(np.uint16), gamma.astype(np.float64),
+            b_vec.astype(np.float64), eps, lb.view(torch.int16).numpy().view(np.uint16), ls, bt,
+            req, pos, kc0, lc0)
+        mids = helpers.e4m3_midpoints(oracle_mod)
+        written_k = np.zeros(kc0.shape, bool)
+        written_l = np.zeros(lc0.shape[:2], bool)
+        for t in range(T):
+            page, slot = bt[req[t], pos[t] // 64], pos[t] % 64
+            # the scale within 1e-6 relative; the codes equal except at rounding midpoints
+            g_ks = kcg[page, 8192 + 4 * slot:8196 + 4 * slot].view(np.float32)[0]
+            assert abs(g_ks - ks[t]) <= 1e-6 * ks[t], t
+            keys = slice(128 * slot, 128 * slot + 128)
+            ok = helpers.near_midpoint(kpre[t], mids) | (kcg[page, keys] == okc[page, keys])
+            assert ok.all(), (t, np.flatnonzero(~ok))
+            ok = helpers.near_midpoint(lpre[t], mids) | (lcg[page, slot] == olc[page, slot])
+            assert ok.all(), (t, np.flatnonzero(~ok))
+            written_k[page, keys] = True
+            written_k[page, 8192 + 4 * slot:8196 + 4 * slot] = True
+            written_l[page, slot] = True
+        # bytes of slots the call does not own are untouched
+        assert np.array_equal(kcg[~written_k], kc0[~written_k])
+        assert np.array_equal(lcg[~written_l], lc0[~written_l])
+
+
+def test_write_kv_flags_bad_tokens(dsa):
+    kc = torch.full((4, 8448), 0x7F, dtype=torch.uint8, device=DEV)
+    lc = torch.full((4, 64, 576), 0x7F, dtype=torch.uint8, device=DEV)
+    bt = torch.tensor([[0, 1], [2, 3]], dtype=torch.int32, device=DEV)
+    kb = torch.randn(3, 128, device=DEV).to(torch.bfloat16)
+    lb = torch.randn(3, 576, device=DEV).to(torch.bfloat16)
+    one, zero = torch.ones(128, device=DEV), torch.zeros(128, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    req = torch.tensor([0, 5, 1], dtype=torch.int32, device=DEV)     # request 5 does not exist
+    pos = torch.tensor([3, 0, 200], dtype=torch.int32, device=DEV)   # 200 >= 2 pages x 64
+    dsa.dsa_write_kv(kb, one, zero, 1e-6, lb, 0.05, bt, req, pos, kc, lc, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0x1                       # DSA_DEV_BAD_ROW
+    assert (kc[0, 3 * 128:4 * 128] != 0x7F).any()      # the valid token was written
+    assert (kc[1:] == 0x7F).all() and (lc[1:] == 0x7F).all()
+
+
 # ------------------------------------------- top-k by the context-parallel exchange
 def _dcp_rows(rng, L, W):
     base = rng.standard_normal(L).astype(np.float32)
