@@ -32,6 +32,9 @@ SMALL = [
     inputs.Workload("short_rows", [1, 63, 65, 2047, 2049], [1, 1, 2, 1, 3], H=32, seed=2),
     inputs.Workload("h128", [9000], [3], H=128, k=1024, seed=3, shift_frac=0.05),
     inputs.Workload("fp8_query", [6000, 2500], [4, 2], H=64, k=2048, seed=4, q_idx_fp8=True),
+    # more than four rows per request with an E4M3 query: groups 4 + 4 + 3 and 4 + 1
+    inputs.Workload("fp8_query_wide", [6000, 3000], [11, 5], H=32, k=1024, seed=7,
+                    q_idx_fp8=True),
 ]
 
 
