@@ -95,6 +95,35 @@ def test_mla_and_step_reject_bad_shapes(lib):
                                  100, FAKE, 1 << 20, None) == 1   # ld < max_pages * 64
 
 
+def test_topk_dcp_rejects_bad_arguments(lib):
+    ws = lib.dsa_topk_dcp_workspace_size(2, 128, 16, 8)
+    assert ws > lib.dsa_topk_workspace_size(2, 128, 16)
+    assert lib.dsa_topk_dcp_workspace_size(2, 128, 16, 0) == 0
+    call = lambda k, W, ws_bytes=ws, R=2, work=FAKE: lib.dsa_topk_dcp(
+        FAKE, 128, FAKE, R, 128, k, W, FAKE, None, work, ws_bytes, None)
+    assert call(16, 0) == 1                          # no shards
+    assert call(16, 33) == 2                         # more shards than the resend mask holds
+    assert call(4096, 8) == 2                        # k > 2048
+    assert call(0, 8) == 1
+    assert call(16, 8, R=9000) == 2                  # R * W > 65535
+    assert call(16, 8, ws_bytes=ws - 1) == 3
+    assert call(16, 8, work=None) == 3
+
+
+def test_write_kv_rejects_bad_arguments(lib):
+    odd = ctypes.c_void_p((1 << 20) + 4)             # 4-byte aligned only
+    call = lambda T=2, ls=1.0, eps=1e-6, k=FAKE, lat=FAKE, kc=FAKE: lib.dsa_write_kv(
+        k, FAKE, FAKE, eps, lat, ls, FAKE, 1, 4, FAKE, FAKE, T, kc, FAKE, 4, None, None)
+    assert call(T=-1) == 1
+    assert call(ls=0.0) == 1 and call(ls=-2.0) == 1 and call(ls=float("inf")) == 1
+    assert call(eps=-1.0) == 1
+    assert call(k=None) == 1
+    assert call(k=odd) == 1                          # k_raw must be 8-byte aligned
+    assert call(lat=ctypes.c_void_p((1 << 20) + 8)) == 1   # latent must be 16-byte aligned
+    assert call(kc=odd) == 1
+    assert call(T=0) == 0                            # nothing to write: no GPU work at all
+
+
 def test_selftest_rejects_bad_arguments(lib):
     need = lib.dsa_selftest_workspace_size()
     assert need >= 768
