@@ -35,9 +35,14 @@ from dsa_sparse_attention_lightning_gb300 import inputs, traffic  # noqa: E402
 
 METRIC = "DSA decode-step µs/layer and achieved HBM GB/s vs 8 TB/s roofline, 1 GB300"
 L2_FLUSH_BYTES = 256 << 20
-# scan 2 (query split + grouping, scan), top-k 3 (sample, collect, finalize),
-# sparse MLA 3 (query split, attention, combine of cut units)
-KERNELS_PER_STEP = 8
+# Kernels one step launches: scan 2 (query split + grouping, scan); top-k 1
+# (one CTA per row, rows of at most 49,152 scores) or 3 (sample, collect,
+# finalize); sparse MLA 3 (query split, attention, combine of cut units).
+TOPK_ROW_CAP = 49152
+
+
+def kernels_per_step(wl) -> int:
+    return 2 + (1 if wl.max_pages * inputs.PAGE <= TOPK_ROW_CAP else 3) + 3
 
 # DRAM bytes (read + write) per call of a stage, summed over its kernels, from
 # the ncu launch list in profiles/ (taken on the current kernels; cold cache,
@@ -386,7 +391,7 @@ def run_gpu(args):
         "write": write,
         "eager_ms_per_step": round(eager_ms, 5),
         "cpu_baseline": cpu,
-        "gpu_launches": KERNELS_PER_STEP * args.steps,
+        "gpu_launches": kernels_per_step(wl) * args.steps,
     }
     print(json.dumps(line), flush=True)
 

@@ -18,11 +18,14 @@
 // decode context parallelism", step 4).
 //
 // Per 128-slot tile, one CTA (a query row, a split, up to 64 heads):
-//  1. one warp gathers the 128 selected 576-byte FP8 latent rows (paged) into
+//  1. six warps gather the 128 selected 576-byte FP8 latent rows (paged) into
 //     one of two shared-memory buffers with TMA tile::gather4 (four arbitrary
-//     rows x 128 bytes per instruction, landing in the K-major 128-byte-swizzle
-//     layout for dims 0..511; the RoPE dims 512..575 come as 64-byte boxes into
-//     a K-major 64-byte-swizzle block), while the previous tile is computed.
+//     rows x 128 bytes per instruction, one instruction per lane, landing in
+//     the K-major 128-byte-swizzle layout for dims 0..511; the RoPE dims
+//     512..575 come as 64-byte boxes into a K-major 64-byte-swizzle block),
+//     while the previous tile is computed.  Each lane waits only until its own
+//     atom of the buffer is free again (the RoPE block after S, atom a after
+//     M-block a of P.V), so most of a tile is in flight while P.V still runs.
 //     Masked slots use an out-of-range row, which TMA fills with zeros;
 //  2. S[(head, term), token] = Q8 . L8^T on tcgen05 kind::f8f6f4, M = 128,
 //     N = 128 tokens, K = 576.  The bf16 query is split exactly into two E4M3

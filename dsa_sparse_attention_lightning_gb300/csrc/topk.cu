@@ -3,7 +3,10 @@
 // Keeps the min(k, len) highest-scoring positions of each row, ties to the
 // lower position (TokenSpeed post on Kimi K3.1 Pro, step 3 "Select": a radix
 // top-k keeps the 2,048 highest-scoring positions for each query).  Scores are
-// compared as order-preserving uint32 keys.  Three launches:
+// compared as order-preserving uint32 keys.  A row of at most 49,152 scores is
+// selected by one CTA (topk_row_kernel, described where it is defined: the
+// row in shared memory, the same sample threshold, the exact select over the
+// candidates); longer rows take three launches:
 //
 //   1. sample   (one CTA per row): a fixed sample of the row (every sb-th
 //               block of 32 scores, sb >= 16, at most 16384 scores) gives a
