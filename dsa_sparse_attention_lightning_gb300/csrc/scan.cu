@@ -98,7 +98,13 @@ struct ScanWs {
   int4* groups;    // [R]
   int* gstart;     // [R + 1] first tile of each group
   int* meta;       // {groups, tiles}
+  int4* cta;       // [kMaxScanCtas] {first group, first tile, end tile, groups} of each scan CTA
 };
+
+// The prep kernel hands every scan CTA its tile range and first group, so a
+// CTA starts with one load instead of a search of the group table; a grid of
+// more CTAs searches.
+constexpr int kMaxScanCtas = 256;
 
 ScanWs scan_ws(uint8_t* base, int R) {
   ScanWs w;
@@ -107,7 +113,8 @@ ScanWs scan_ws(uint8_t* base, int R) {
   w.weff = reinterpret_cast<float*>(base + o); o = align_up(o + (size_t)R * kIdxHeads * 4);
   w.groups = reinterpret_cast<int4*>(base + o); o = align_up(o + (size_t)R * 16);
   w.gstart = reinterpret_cast<int*>(base + o);  o = align_up(o + (size_t)(R + 1) * 4);
-  w.meta = reinterpret_cast<int*>(base + o);
+  w.meta = reinterpret_cast<int*>(base + o);  o = align_up(o + 16);
+  w.cta = reinterpret_cast<int4*>(base + o);
   return w;
 }
 
@@ -159,8 +166,8 @@ __device__ __forceinline__ bool row_valid(const int32_t* row_req, const int32_t*
 __global__ void __launch_bounds__(kPrepThreads)
 scan_prep_kernel(const void* __restrict__ q_idx, int q_dtype, const float* __restrict__ q_scale,
                  const float* __restrict__ w, const int32_t* __restrict__ row_req,
-                 const int32_t* __restrict__ row_len, int R, int B, int max_pages, ScanWs ws,
-                 uint32_t* status) {
+                 const int32_t* __restrict__ row_len, int R, int B, int max_pages, int nctas,
+                 ScanWs ws, uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == (unsigned)R) {
@@ -209,6 +216,21 @@ scan_prep_kernel(const void* __restrict__ q_idx, int q_dtype, const float* __res
       ws.gstart[s_carry[1]] = s_carry[2];
       ws.meta[0] = s_carry[1];
       ws.meta[1] = s_carry[2];
+    }
+    // each scan CTA's tile range and the group holding its first tile (the
+    // last group whose first tile is <= it, as TileCursor::seek finds it)
+    const int ngroups = s_carry[1], total = s_carry[2];
+    if (nctas <= kMaxScanCtas) {
+      for (int c = threadIdx.x; c < nctas; c += kPrepThreads) {
+        const int tb = (int)((int64_t)total * c / nctas);
+        const int te = (int)((int64_t)total * (c + 1) / nctas);
+        int lo = 0, hi = ngroups;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (ws.gstart[mid] <= tb) lo = mid; else hi = mid;
+        }
+        ws.cta[c] = make_int4(lo, tb, te, ngroups);
+      }
     }
     return;
   }
@@ -265,6 +287,11 @@ struct TileCursor {
     gs = gstart[g];
     ge = gstart[g + 1];
     G = groups[g];
+  }
+  __device__ void start(int g0, int tile) {   // tile lies in group g0 (non-empty)
+    g = g0;
+    load();
+    t = tile - gs;
   }
   __device__ void seek(int tile) {
     int lo = 0, hi = ngroups;              // last g in [0, ngroups) with gstart[g] <= tile
@@ -406,16 +433,29 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
   pdl_trigger();                                    // after the tensor-memory allocation
   pdl_wait();                                       // the prep kernel's groups and query terms
 
-  const int ngroups = ws.meta[0];
-  const int total = ws.meta[1];
-  const int t_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
-  const int t_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+  const bool handed = gridDim.x <= (unsigned)kMaxScanCtas;   // range from the prep kernel
+  int ngroups, t_begin, t_end, g_begin = 0;
+  if (handed) {
+    const int4 cs = ws.cta[blockIdx.x];
+    g_begin = cs.x;
+    t_begin = cs.y;
+    t_end = cs.z;
+    ngroups = cs.w;
+  } else {
+    ngroups = ws.meta[0];
+    const int total = ws.meta[1];
+    t_begin = (int)((int64_t)total * blockIdx.x / gridDim.x);
+    t_end = (int)((int64_t)total * (blockIdx.x + 1) / gridDim.x);
+  }
   const int ntiles = t_end - t_begin;
   TileCursor cur;
   cur.groups = ws.groups;
   cur.gstart = ws.gstart;
   cur.ngroups = ngroups;
-  if (ntiles > 0) cur.seek(t_begin);
+  if (ntiles > 0) {
+    if (handed) cur.start(g_begin, t_begin);
+    else cur.seek(t_begin);
+  }
 
   if (ntiles > 0 && warp < kMmaWarps) {
     // ---------------- MMA issuers: lane 0 of warp m issues the tiles i with
@@ -643,7 +683,8 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
 
 size_t scan_scratch_bytes(int R) {
   return align_up((size_t)2 * R * kIdxHeads * kIdxDim) + align_up((size_t)R * kIdxHeads * 4) +
-         align_up((size_t)R * 16) + align_up((size_t)(R + 1) * 4) + align_up(16);
+         align_up((size_t)R * 16) + align_up((size_t)(R + 1) * 4) + align_up(16) +
+         align_up((size_t)kMaxScanCtas * 16);
 }
 
 cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st) {
@@ -674,7 +715,8 @@ cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st) {
   e = encode_tensor_map_u8(&qmap, 2, ws.q8, qdims, qstr, qbox);
   if (e != cudaSuccess) return e;
   scan_prep_kernel<<<a.R + 1, kPrepThreads, 0, st>>>(a.q_idx, a.q_dtype, a.q_scale, a.w, a.row_req,
-                                             a.row_len, a.R, a.B, a.max_pages, ws, a.status);
+                                             a.row_len, a.R, a.B, a.max_pages, sms, ws,
+                                             a.status);
   e = launch_kernel(scan_kernel, dim3(sms), dim3(kThreads), kSmemAlloc, st, true, kmap, qmap,
                     a.key_cache, a.num_pages, a.block_table, a.max_pages, a.row_len, a.scores,
                     a.ld, a.R, a.q_dtype == DSA_E4M3 ? 1 : 2, ws, a.status);
