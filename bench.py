@@ -49,11 +49,11 @@ def kernels_per_step(wl) -> int:
 # so L2-resident intermediates count as DRAM reads).  Stages and workloads not
 # captured report null.
 NCU_STAGE_TRAFFIC = {
-    ("decode_16x4_ctx32768_h64", "indexer_scan"): 70.42e6,
-    ("decode_16x4_ctx32768_h64", "topk"): 8.45e6,
-    ("decode_16x4_ctx32768_h64", "sparse_mla"): 104.42e6,
+    ("decode_16x4_ctx32768_h64", "indexer_scan"): 70.40e6,
+    ("decode_16x4_ctx32768_h64", "topk"): 8.46e6,
+    ("decode_16x4_ctx32768_h64", "sparse_mla"): 104.41e6,
     # prefill chunk: scan_kernel alone (profiles/prefill_4096rows_ctx131072_tensor.md)
-    ("prefill_4096rows_ctx131072_h64", "indexer_scan"): 2099.82e6,
+    ("prefill_4096rows_ctx131072_h64", "indexer_scan"): 2098.86e6,
 }
 
 
