@@ -11,7 +11,7 @@
 //   1. sample   (one CTA per row): a fixed sample of the row (every sb-th
 //               block of 32 scores, sb >= 16, at most 16384 scores) gives a
 //               threshold tau low enough that the row should hold about
-//               1.5 k + 32 sb keys >= tau: the key of the sample's rank-rho
+//               1.25 k + 16 sb keys >= tau: the key of the sample's rank-rho
 //               element, rounded down to its 22-bit prefix (two radix digits
 //               over the sample).
 //   2. collect  (row x 4096-score chunk CTAs): every key >= tau is appended,
@@ -145,8 +145,8 @@ __device__ uint32_t sample_threshold(KeyOf key_of, int len, int k, uint32_t* h, 
                                      int* s_d, uint32_t* s_above, uint32_t* s_n) {
   const int64_t sb = sample_stride(len);
   const int64_t ns = sample_count(len, sb);
-  // rank rho in the sample ~ 1.5 k / sb + 32 (about 1.5 k + 32 sb candidates in the row)
-  const uint32_t rho = (uint32_t)((3 * (int64_t)k + 2 * sb - 1) / (2 * sb)) + 32;
+  // rank rho in the sample ~ 1.25 k / sb + 16 (about 1.25 k + 16 sb candidates in the row)
+  const uint32_t rho = (uint32_t)((5 * (int64_t)k + 4 * sb - 1) / (4 * sb)) + 16;
   for (int i = threadIdx.x; i < kTopkBins1; i += kSampleThreads) h[i] = 0;
   if (threadIdx.x == 0) *s_n = 0;
   __syncthreads();
