@@ -21,6 +21,9 @@
  *   - oracle_write_kv          the Write step: LayerNorm of a new token's index
  *                              key, FP8 quantization with one scale, paged
  *                              write; the latent row's FP8 write
+ *   - oracle_e2m1_decode, oracle_e8m0_decode, oracle_mx_quantize_key,
+ *     oracle_indexer_scores_mx  MXFP4 index keys (68 bytes per token) and the
+ *                              indexer over them
  *
  * Sources (web pages on Kimi K3.1 Pro's sparse attention):
  *   [TS]   TokenSpeed post on Kimi K3.1 Pro (lightseek.org), sections
@@ -36,7 +39,11 @@
  *          with decode context parallelism".
  *   [VLLM] also section "An exact top-k merge with about 10x less traffic".
  *   [AMD]  "Kimi K3.1 Pro on AMD Instinct GPUs" (dev48.org, in Russian),
- *          overview table, row "MLA" (KV LoRA rank 512 + 64 RoPE dims).
+ *          overview table, row "MLA" (KV LoRA rank 512 + 64 RoPE dims), and
+ *          the quantization list (MXFP4: one E8M0 scale per 32 values).
+ *   [VLLM] also "Hybrid KV cache without padding" (index keys at 68 bytes in
+ *          MXFP4) and "Native MXFP4 indexer" (68 bytes including scales;
+ *          FP4 products, FP32 accumulation, weighted reduction over heads).
  *
  * The pages do not print the indexer formula; they point to DeepSeek-V3.2 for
  * it.  The form used here is the DeepSeek-V3.2 lightning indexer:
@@ -60,6 +67,12 @@
 #define ORA_IDX_DIM 128
 #define ORA_IDX_HEADS 32
 #define ORA_KEY_PAGE_BYTES (ORA_PAGE * ORA_IDX_DIM + ORA_PAGE * 4)
+/* MXFP4 index-key page: 64 tokens x 64 bytes of packed E2M1 codes, then 64 x 4
+ * E8M0 block scales (one per 32 dims); 68 bytes per token. */
+#define ORA_MX_BLOCK 32
+#define ORA_MX_KEY_BYTES (ORA_IDX_DIM / 2)
+#define ORA_MX_SCALES (ORA_IDX_DIM / ORA_MX_BLOCK)
+#define ORA_MX_KEY_PAGE_BYTES (ORA_PAGE * ORA_MX_KEY_BYTES + ORA_PAGE * ORA_MX_SCALES)
 /* Latent row: 512 compressed-KV dims + 64 RoPE dims ([AMD] overview, "MLA"). */
 #define ORA_LAT_DIM 576
 #define ORA_V_DIM 512
@@ -142,6 +155,22 @@ uint8_t oracle_e4m3_encode(double x) {
     return (uint8_t)((sign << 7) | best);
 }
 
+/* k = gamma * (x - mean(x)) / sqrt(var(x) + eps) + beta over the 128 dims of one
+ * bf16 key, with the biased variance. */
+static void layer_norm_key(const uint16_t* k_raw, const double* gamma, const double* beta,
+                           double eps, double* k) {
+    double x[ORA_IDX_DIM], mean = 0.0, var = 0.0;
+    for (int d = 0; d < ORA_IDX_DIM; ++d) {
+        x[d] = bf16_to_double(k_raw[d]);
+        mean += x[d];
+    }
+    mean /= ORA_IDX_DIM;
+    for (int d = 0; d < ORA_IDX_DIM; ++d) var += (x[d] - mean) * (x[d] - mean);
+    var /= ORA_IDX_DIM;
+    for (int d = 0; d < ORA_IDX_DIM; ++d)
+        k[d] = gamma[d] * (x[d] - mean) / sqrt(var + eps) + beta[d];
+}
+
 /*
  * The Write step ([TS] step 1 "Write": one fused kernel normalizes the new
  * token's index key, quantizes it to FP8 with a single scale and writes it
@@ -179,19 +208,10 @@ int oracle_write_kv(const uint16_t* k_raw, const double* gamma, const double* be
         if (page < 0 || (int64_t)page >= num_pages) return ORA_BAD_PAGE;
         const int slot = pos % ORA_PAGE;
         /* index key: LayerNorm, absmax scale, E4M3 codes */
-        double x[ORA_IDX_DIM], k[ORA_IDX_DIM];
-        double mean = 0.0, var = 0.0, amax = 0.0;
-        for (int d = 0; d < ORA_IDX_DIM; ++d) {
-            x[d] = bf16_to_double(k_raw[(size_t)t * ORA_IDX_DIM + d]);
-            mean += x[d];
-        }
-        mean /= ORA_IDX_DIM;
-        for (int d = 0; d < ORA_IDX_DIM; ++d) var += (x[d] - mean) * (x[d] - mean);
-        var /= ORA_IDX_DIM;
-        for (int d = 0; d < ORA_IDX_DIM; ++d) {
-            k[d] = gamma[d] * (x[d] - mean) / sqrt(var + eps) + beta[d];
+        double k[ORA_IDX_DIM], amax = 0.0;
+        layer_norm_key(k_raw + (size_t)t * ORA_IDX_DIM, gamma, beta, eps, k);
+        for (int d = 0; d < ORA_IDX_DIM; ++d)
             if (fabs(k[d]) > amax) amax = fabs(k[d]);
-        }
         const double ks = amax > 0.0 ? amax / 448.0 : 1.0;
         uint8_t* kp = key_cache + (size_t)page * ORA_KEY_PAGE_BYTES;
         for (int d = 0; d < ORA_IDX_DIM; ++d) {
@@ -279,6 +299,214 @@ int oracle_indexer_scores(const uint16_t* q_bf16, const uint8_t* q_e4m3, const f
                 double x = dot * ks;
                 double relu = x > 0.0 ? x : 0.0;
                 acc += (double)w[(size_t)r * ORA_IDX_HEADS + h] * relu;
+            }
+            scores[(size_t)r * ld + s] = acc;
+        }
+        if (row_status != ORA_OK) status = row_status;
+    }
+    return status;
+}
+
+/*
+ * ---- MXFP4 index keys ----
+ * [VLLM] "Hybrid KV cache without padding": an index key takes 68 bytes in
+ * MXFP4 against 132 in FP8; "Native MXFP4 indexer": the 68 bytes include the
+ * scales, the products are FP4 with FP32 accumulation and a weighted
+ * reduction over heads; [AMD] quantization list: MXFP4 keeps one E8M0 scale
+ * per 32 values.  128 dims = 64 bytes of 4-bit codes + 4 one-byte scales.
+ * The element and scale encodings are those of the OCP Microscaling (MX)
+ * specification v1.0; the pages name the format and nothing finer.
+ */
+
+/*
+ * E2M1: one sign bit (bit 3), two exponent bits with bias 1, one mantissa
+ * bit.  Exponent field 0 is subnormal (0 or 0.5); no infinities, no NaN.
+ * The eight magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+ * Pinned by: the 16 codes against their closed form (golden table), the MX
+ * cross-format identity with the E4M3 scorer.
+ */
+double oracle_e2m1_decode(uint8_t nibble) {
+    const int sign = (nibble >> 3) & 1;
+    const int e = (nibble >> 1) & 0x3;
+    const int m = nibble & 0x1;
+    const double mag = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return sign ? -mag : mag;
+}
+
+/*
+ * E2M1 encoding: the nearest of the eight magnitudes, a tie going to the code
+ * with an even mantissa bit, magnitudes above 6 saturating to 6 (the MX
+ * conversion clamps to the element format's largest normal); the sign is
+ * kept.  By brute force over the 8 non-negative codes.
+ * Pinned by: the round trip over all 16 codes, every midpoint, saturation.
+ */
+uint8_t oracle_e2m1_encode(double x) {
+    const int sign = signbit(x) ? 1 : 0;
+    const double a = fabs(x);
+    int best = 0;
+    double bestd = INFINITY;
+    for (int c = 0; c < 8; ++c) {
+        const double d = fabs(a - oracle_e2m1_decode((uint8_t)c));
+        if (d < bestd || (d == bestd && c % 2 == 0)) {
+            best = c;
+            bestd = d;
+        }
+    }
+    return (uint8_t)((sign << 3) | best);
+}
+
+/*
+ * E8M0: an unsigned exponent with bias 127, value 2^(code - 127); code 0xFF
+ * is NaN.  Pinned by: every code against torch.float8_e8m0fnu where the
+ * installed torch has it, and against ldexp otherwise.
+ */
+double oracle_e8m0_decode(uint8_t code) {
+    if (code == 0xFF) return NAN;
+    return ldexp(1.0, (int)code - 127);
+}
+
+/*
+ * MX quantization of n values (n a multiple of 32), per block of 32:
+ *   shared = floor(log2(max |v|)) - 2       (2 = E2M1's largest exponent)
+ *   scale  = 2^shared as E8M0, shared clamped to [-127, 127]; an all-zero
+ *            block takes shared = -127
+ *   code_i = e2m1_encode(v_i / scale)        (saturating at 6)
+ * Codes are packed two to a byte, element 2j in the low nibble of byte j.
+ * Returns ORA_BAD_ARG if n is not a multiple of 32 or a value is not finite.
+ * Pinned by: the scale exponent against frexp on random blocks, exactness on
+ * values that are E2M1 times a power of two, the error bound
+ * |v - dec(code) * scale| <= scale (and <= scale / 2 below 6 * scale).
+ */
+int oracle_mx_quantize(const double* v, int n, uint8_t* codes, uint8_t* scales) {
+    if (n < 0 || n % ORA_MX_BLOCK != 0) return ORA_BAD_ARG;
+    for (int i = 0; i < n; ++i)
+        if (!isfinite(v[i])) return ORA_BAD_ARG;
+    for (int b = 0; b < n / ORA_MX_BLOCK; ++b) {
+        const double* vb = v + (size_t)b * ORA_MX_BLOCK;
+        double amax = 0.0;
+        for (int i = 0; i < ORA_MX_BLOCK; ++i)
+            if (fabs(vb[i]) > amax) amax = fabs(vb[i]);
+        int shared = -127;
+        if (amax > 0.0) {
+            shared = (int)floor(log2(amax)) - 2;
+            if (shared < -127) shared = -127;
+            if (shared > 127) shared = 127;
+        }
+        scales[b] = (uint8_t)(shared + 127);
+        const double scale = ldexp(1.0, shared);
+        for (int i = 0; i < ORA_MX_BLOCK; ++i) {
+            const uint8_t c = oracle_e2m1_encode(vb[i] / scale);
+            const int j = b * ORA_MX_BLOCK + i;
+            if (j % 2 == 0)
+                codes[j / 2] = c;
+            else
+                codes[j / 2] |= (uint8_t)(c << 4);
+        }
+    }
+    return ORA_OK;
+}
+
+/* Element d of a packed MX vector, decoded with its block scale. */
+static double mx_value(const uint8_t* codes, const uint8_t* scales, int d) {
+    const uint8_t nib = (d % 2 == 0) ? (codes[d / 2] & 0xF) : (codes[d / 2] >> 4);
+    return oracle_e2m1_decode(nib) * oracle_e8m0_decode(scales[d / ORA_MX_BLOCK]);
+}
+
+/*
+ * The Write step for MXFP4 index keys: the LayerNorm of oracle_write_kv, then
+ * mx_quantize of the 128 normalized values (no per-token scale: the block
+ * scales replace it).  Page block_table[req][pos / 64], slot pos % 64 of
+ * key_cache (ORA_MX_KEY_PAGE_BYTES per page): the 64 code bytes at slot * 64,
+ * the 4 scale bytes at 64 * 64 + slot * 4.  The normalized key is returned in
+ * key_pre [T][128] when non-NULL.  The latent row is written as in
+ * oracle_write_kv (the two caches are quantized independently: [VLLM] "Hybrid
+ * KV cache without padding").
+ * Pinned by: the LayerNorm shared with the FP8 Write step (pinned there), the
+ * bytes against mx_quantize of that LayerNorm's output, placement through a
+ * shuffled block table.
+ */
+int oracle_write_key_mx(const uint16_t* k_raw, const double* gamma, const double* beta,
+                        double eps, const int32_t* block_table, int B, int max_pages,
+                        const int32_t* tok_req, const int32_t* tok_pos, int T,
+                        uint8_t* key_cache, int64_t num_pages, double* key_pre) {
+    if (T < 0 || !(eps >= 0.0)) return ORA_BAD_ARG;
+    for (int t = 0; t < T; ++t) {
+        const int req = tok_req[t], pos = tok_pos[t];
+        if (req < 0 || req >= B || pos < 0 || pos >= max_pages * ORA_PAGE) return ORA_BAD_ARG;
+        const int page = block_table[(size_t)req * max_pages + pos / ORA_PAGE];
+        if (page < 0 || (int64_t)page >= num_pages) return ORA_BAD_PAGE;
+        const int slot = pos % ORA_PAGE;
+        double k[ORA_IDX_DIM];
+        layer_norm_key(k_raw + (size_t)t * ORA_IDX_DIM, gamma, beta, eps, k);
+        uint8_t* pg = key_cache + (size_t)page * ORA_MX_KEY_PAGE_BYTES;
+        const int rc = oracle_mx_quantize(k, ORA_IDX_DIM, pg + (size_t)slot * ORA_MX_KEY_BYTES,
+                                          pg + ORA_PAGE * ORA_MX_KEY_BYTES +
+                                              (size_t)slot * ORA_MX_SCALES);
+        if (rc != ORA_OK) return rc;
+        if (key_pre) memcpy(key_pre + (size_t)t * ORA_IDX_DIM, k, sizeof k);
+    }
+    return ORA_OK;
+}
+
+/*
+ * Lightning-indexer scores over MXFP4 keys with an MXFP4 query ([VLLM]
+ * "Native MXFP4 indexer": FP4 products, FP32 accumulation, weighted reduction
+ * across heads; the query front quantizes the query to FP8 or MXFP4 with the
+ * head weights folded in).
+ *
+ *   score[r][s] = sum_{h<32} w[r][h] * max(0, sum_{d<128} q[r][h][d] * key[s][d])
+ *
+ * with q[r][h][d] = e2m1(qc[r][h] element d) * e8m0(qs[r][h][d / 32]) and
+ * key[s][d] likewise from its page (codes at slot * 64, scales at 64 * 64 +
+ * slot * 4).  The block scales are powers of two, so the FP8 form's per-token
+ * scale inside the ReLU has no counterpart here.  qc is [R][32][64] bytes, qs
+ * [R][32][4].  Entries s >= row_len[r] are left untouched.
+ * Pinned by: the cross-format identity (keys and queries on the MX grid are
+ * exactly representable as E4M3 times a power-of-two per-token scale, so the
+ * FP8 scorer, pinned separately, must give the same scores), brute force of
+ * one score from the golden E2M1 table, linearity in w, q = 0.
+ */
+int oracle_indexer_scores_mx(const uint8_t* qc, const uint8_t* qs, const float* w,
+                             const uint8_t* key_cache, int64_t num_pages,
+                             const int32_t* block_table, int B, int max_pages,
+                             const int32_t* row_req, const int32_t* row_len, int R,
+                             double* scores, int64_t ld) {
+    int status = ORA_OK;
+    for (int r = 0; r < R; ++r) {
+        if (row_req[r] < 0 || row_req[r] >= B) return ORA_BAD_ARG;
+        if (row_len[r] < 0 || (int64_t)row_len[r] > ld ||
+            (int64_t)row_len[r] > (int64_t)max_pages * ORA_PAGE)
+            return ORA_BAD_ARG;
+    }
+    for (int r = 0; r < R; ++r) {
+        const int b = row_req[r];
+        const int64_t len = row_len[r];
+        double q[ORA_IDX_HEADS][ORA_IDX_DIM];
+        for (int h = 0; h < ORA_IDX_HEADS; ++h) {
+            const size_t rh = (size_t)r * ORA_IDX_HEADS + h;
+            for (int d = 0; d < ORA_IDX_DIM; ++d)
+                q[h][d] = mx_value(qc + rh * ORA_MX_KEY_BYTES, qs + rh * ORA_MX_SCALES, d);
+        }
+        int row_status = ORA_OK;
+#pragma omp parallel for schedule(static) reduction(max : row_status)
+        for (int64_t s = 0; s < len; ++s) {
+            int64_t page = block_table[(size_t)b * max_pages + s / ORA_PAGE];
+            if (page < 0 || page >= num_pages) {
+                row_status = ORA_BAD_PAGE;
+                continue;
+            }
+            const uint8_t* pg = key_cache + (size_t)page * ORA_MX_KEY_PAGE_BYTES;
+            const int slot = (int)(s % ORA_PAGE);
+            double key[ORA_IDX_DIM];
+            for (int d = 0; d < ORA_IDX_DIM; ++d)
+                key[d] = mx_value(pg + (size_t)slot * ORA_MX_KEY_BYTES,
+                                  pg + ORA_PAGE * ORA_MX_KEY_BYTES + (size_t)slot * ORA_MX_SCALES,
+                                  d);
+            double acc = 0.0;
+            for (int h = 0; h < ORA_IDX_HEADS; ++h) {
+                double qk = 0.0;
+                for (int d = 0; d < ORA_IDX_DIM; ++d) qk += q[h][d] * key[d];
+                acc += (double)w[(size_t)r * ORA_IDX_HEADS + h] * (qk > 0.0 ? qk : 0.0);
             }
             scores[(size_t)r * ld + s] = acc;
         }

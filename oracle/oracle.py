@@ -31,6 +31,10 @@ PAGE = 64
 IDX_HEADS = 32
 IDX_DIM = 128
 KEY_PAGE_BYTES = PAGE * IDX_DIM + PAGE * 4
+MX_BLOCK = 32
+MX_KEY_BYTES = IDX_DIM // 2
+MX_SCALES = IDX_DIM // MX_BLOCK
+MX_KEY_PAGE_BYTES = PAGE * (MX_KEY_BYTES + MX_SCALES)
 LAT_DIM = 576
 V_DIM = 512
 
@@ -75,6 +79,18 @@ def _load():
         lib.oracle_sparse_mla.argtypes = [P, i32, dbl, P, i64, dbl, P, i32, i32, P, P, P, i32, i32,
                                           P, P]
         lib.oracle_sparse_mla.restype = ctypes.c_int
+        lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_decode.restype = dbl
+        lib.oracle_e2m1_encode.argtypes = [dbl]
+        lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+        lib.oracle_e8m0_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e8m0_decode.restype = dbl
+        lib.oracle_mx_quantize.argtypes = [P, ctypes.c_int, P, P]
+        lib.oracle_mx_quantize.restype = ctypes.c_int
+        lib.oracle_write_key_mx.argtypes = [P, P, P, dbl, P, i32, i32, P, P, i32, P, i64, P]
+        lib.oracle_write_key_mx.restype = ctypes.c_int
+        lib.oracle_indexer_scores_mx.argtypes = [P, P, P, P, i64, P, i32, i32, P, P, i32, P, i64]
+        lib.oracle_indexer_scores_mx.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -175,6 +191,84 @@ def write_kv(k_raw, gamma, beta, eps, latent, latent_scale, block_table, tok_req
     if st != 0:
         raise ValueError(f"oracle_write_kv failed with status {st}")
     return key_cache, latent_cache, key_pre, lat_pre, key_scale
+
+
+def e2m1_decode(nibble: int) -> float:
+    return float(_load().oracle_e2m1_decode(int(nibble) & 0xF))
+
+
+def e2m1_encode(x: float) -> int:
+    return int(_load().oracle_e2m1_encode(float(x)))
+
+
+def e8m0_decode(code: int) -> float:
+    return float(_load().oracle_e8m0_decode(int(code) & 0xFF))
+
+
+def mx_quantize(v):
+    """MXFP4 of float64 values [..., n] (n a multiple of 32).
+
+    Returns (codes uint8 [..., n/2], two per byte, low nibble first; scales
+    uint8 E8M0 [..., n/32])."""
+    lib = _load()
+    v = _c(v, np.float64)
+    n = v.shape[-1]
+    flat = v.reshape(-1, n)
+    codes = np.zeros((flat.shape[0], n // 2), dtype=np.uint8)
+    scales = np.zeros((flat.shape[0], n // MX_BLOCK), dtype=np.uint8)
+    for i in range(flat.shape[0]):
+        st = lib.oracle_mx_quantize(_ptr(flat[i]), n, _ptr(codes[i]), _ptr(scales[i]))
+        if st != 0:
+            raise ValueError(f"oracle_mx_quantize failed with status {st}")
+    return codes.reshape(v.shape[:-1] + (n // 2,)), scales.reshape(v.shape[:-1] + (n // MX_BLOCK,))
+
+
+def write_key_mx(k_raw, gamma, beta, eps, block_table, tok_req, tok_pos, key_cache):
+    """The Write step of MXFP4 index keys on a copy of the key cache.
+
+    Returns (key_cache, key_pre [T,128]): the written cache and the float64
+    normalized keys."""
+    lib = _load()
+    k_raw = _c(k_raw, np.uint16)
+    T = k_raw.shape[0]
+    block_table = _c(block_table, np.int32)
+    B, max_pages = block_table.shape
+    key_cache = np.array(key_cache, dtype=np.uint8, copy=True, order="C")
+    num_pages = key_cache.size // MX_KEY_PAGE_BYTES
+    key_pre = np.zeros((T, IDX_DIM))
+    st = lib.oracle_write_key_mx(_ptr(k_raw), _ptr(_c(gamma, np.float64)),
+                                 _ptr(_c(beta, np.float64)), float(eps), _ptr(block_table), B,
+                                 max_pages, _ptr(_c(tok_req, np.int32)),
+                                 _ptr(_c(tok_pos, np.int32)), T, _ptr(key_cache), num_pages,
+                                 _ptr(key_pre))
+    if st != 0:
+        raise ValueError(f"oracle_write_key_mx failed with status {st}")
+    return key_cache, key_pre
+
+
+def indexer_scores_mx(q_codes, q_scales, w, key_cache, block_table, row_req, row_len, *,
+                      ld=None):
+    """Float64 scores [R, ld] over MXFP4 keys; entries past row_len are NaN.
+
+    ``q_codes`` uint8 [R,32,64] packed E2M1, ``q_scales`` uint8 E8M0 [R,32,4],
+    ``key_cache`` pages of MX_KEY_PAGE_BYTES."""
+    lib = _load()
+    R = int(np.asarray(row_len).shape[0])
+    row_len = _c(row_len, np.int32)
+    row_req = _c(row_req, np.int32)
+    block_table = _c(block_table, np.int32)
+    B, max_pages = block_table.shape
+    ld = int(ld if ld is not None else max(1, int(row_len.max(initial=0))))
+    scores = np.full((R, ld), np.nan, dtype=np.float64)
+    key_cache = _c(key_cache, np.uint8)
+    num_pages = key_cache.size // MX_KEY_PAGE_BYTES
+    st = lib.oracle_indexer_scores_mx(_ptr(_c(q_codes, np.uint8)), _ptr(_c(q_scales, np.uint8)),
+                                      _ptr(_c(w, np.float32)), _ptr(key_cache), num_pages,
+                                      _ptr(block_table), B, max_pages, _ptr(row_req),
+                                      _ptr(row_len), R, _ptr(scores), ld)
+    if st != 0:
+        raise ValueError(f"oracle_indexer_scores_mx failed with status {st}")
+    return scores
 
 
 def topk_dcp(scores, row_len, k, W):

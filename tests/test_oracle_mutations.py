@@ -39,6 +39,17 @@ MUTATIONS = [
     ("key_scale_next_slot", "memcpy(kp + ORA_PAGE * ORA_IDX_DIM + (size_t)slot * 4,",
      "memcpy(kp + ORA_PAGE * ORA_IDX_DIM + (size_t)((slot + 1) % ORA_PAGE) * 4,"),
     ("e4m3_ties_to_odd", "(d == bestd && (c & 1) == 0)", "(d == bestd && (c & 1) == 1)"),
+    ("e2m1_exponent_bias", "ldexp(1.0 + 0.5 * m, e - 1)", "ldexp(1.0 + 0.5 * m, e - 2)"),
+    ("e2m1_ties_to_odd", "(d == bestd && c % 2 == 0)", "(d == bestd && c % 2 == 1)"),
+    ("e8m0_bias", "return ldexp(1.0, (int)code - 127);", "return ldexp(1.0, (int)code - 126);"),
+    ("mx_emax_off_by_one", "(int)floor(log2(amax)) - 2;", "(int)floor(log2(amax)) - 1;"),
+    ("mx_packing_high_nibble_first", "if (j % 2 == 0)\n                codes[j / 2] = c;",
+     "if (j % 2 == 1)\n                codes[j / 2] = c;"),
+    ("mx_scale_wrong_block", "scales[d / ORA_MX_BLOCK]",
+     "scales[(d / ORA_MX_BLOCK + 1) % ORA_MX_SCALES]"),
+    ("mx_key_scales_next_slot", "(size_t)slot * ORA_MX_SCALES);",
+     "(size_t)((slot + 1) % ORA_PAGE) * ORA_MX_SCALES);"),
+    ("mx_relu_dropped", "(qk > 0.0 ? qk : 0.0)", "qk"),
 ]
 
 PIN_TESTS = [
@@ -56,6 +67,14 @@ PIN_TESTS = [
     pins.test_mla_dense_matches_sdpa,
     pins.test_mla_single_token_and_zero_query,
     pins.test_mla_split_merge_by_lse,
+    pins.test_e2m1_golden_table,
+    pins.test_e2m1_encode_round_trip_and_golden_rounding,
+    pins.test_e8m0_all_codes,
+    pins.test_mx_quantize_scale_exponent_and_packing,
+    pins.test_mx_quantize_exact_on_grid_and_error_bound,
+    pins.test_indexer_mx_equals_fp8_scorer_on_shared_grid,
+    pins.test_indexer_mx_last_dim_and_scale_slot,
+    pins.test_write_key_mx_codes_and_placement,
 ]
 
 

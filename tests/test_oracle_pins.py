@@ -517,3 +517,231 @@ def test_workload_bytes():
     assert traffic.algorithmic_bytes(inputs.config(3)) == 139_739_264
     assert round(traffic.scan_bytes(inputs.config(2)) / 16 / 1e6, 1) == 34.6
     assert inputs.config(4).row_lengths()[0] == 126_977    # row i sees tokens <= 126,976 + i
+
+
+# ------------------------------------------------------- MXFP4 index keys
+# Packed layout of one key: 64 bytes of E2M1 codes (dim 2j in the low nibble of
+# byte j, dim 2j+1 in the high nibble), then per 64-token page 64 x 4 E8M0
+# block scales (block b = dims 32b .. 32b+31).
+MX_PAGE_BYTES = PAGE * (D // 2 + D // 32)
+
+
+def _e2m1_grid():
+    return np.array([float(v[0]) for c, v in _read_golden("e2m1_codes.txt").items()
+                     if int(c, 16) < 8])
+
+
+def _mx_key_cache(codes, scales):
+    """Pack [ntok,64] code bytes and [ntok,4] scale bytes into identity-mapped pages."""
+    n = codes.shape[0]
+    npg = (n + PAGE - 1) // PAGE
+    cache = np.full((npg, MX_PAGE_BYTES), 0xFF, dtype=np.uint8)   # 0xFF: NaN scale if read
+    for t in range(n):
+        p, s = divmod(t, PAGE)
+        cache[p, s * 64:(s + 1) * 64] = codes[t]
+        cache[p, PAGE * 64 + s * 4:PAGE * 64 + (s + 1) * 4] = scales[t]
+    return cache, np.arange(npg, dtype=np.int32)[None, :]
+
+
+def _grid_values(rng, shape, lo=-3, hi=2):
+    """Values exactly on the MX grid: E2M1 magnitudes x sign x 2^p, p drawn per
+    32-value block; about a tenth of the blocks all zero."""
+    grid = _e2m1_grid()
+    v = grid[rng.integers(0, 8, shape)] * rng.choice([-1.0, 1.0], shape)
+    blocks = v.reshape(shape[:-1] + (shape[-1] // 32, 32))
+    p = rng.integers(lo, hi + 1, blocks.shape[:-1] + (1,))
+    blocks *= np.ldexp(1.0, p)
+    blocks[rng.random(blocks.shape[:-1]) < 0.1] = 0.0
+    return blocks.reshape(shape)
+
+
+def test_e2m1_golden_table(oracle_mod):
+    for code, (val,) in _read_golden("e2m1_codes.txt").items():
+        got = oracle_mod.e2m1_decode(int(code, 16))
+        assert got == float(val) and math.copysign(1, got) == math.copysign(1, float(val))
+
+
+def test_e2m1_encode_round_trip_and_golden_rounding(oracle_mod):
+    for c in range(16):
+        assert oracle_mod.e2m1_encode(oracle_mod.e2m1_decode(c)) == c
+    for val, (code,) in _read_golden("e2m1_rounding.txt").items():
+        assert oracle_mod.e2m1_encode(float(val)) == int(code, 16), val
+
+
+def test_e2m1_encode_is_nearest(oracle_mod):
+    """No grid point is strictly closer than the chosen one (brute force)."""
+    grid = _e2m1_grid()
+    rng = np.random.default_rng(40)
+    for x in rng.uniform(-6.0, 6.0, 2000):
+        got = oracle_mod.e2m1_decode(oracle_mod.e2m1_encode(x))
+        assert math.copysign(1, got) == math.copysign(1, x)
+        assert abs(x - got) <= np.min(np.abs(abs(x) - grid)) + 0.0
+
+
+def test_e8m0_all_codes(oracle_mod):
+    ours = np.array([oracle_mod.e8m0_decode(c) for c in range(256)])
+    assert np.isnan(ours[255]) and not np.isnan(ours[:255]).any()
+    assert all(ours[c] == math.ldexp(1.0, c - 127) for c in range(255))
+    if hasattr(torch, "float8_e8m0fnu"):
+        lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e8m0fnu).double().numpy()
+        assert np.array_equal(np.isnan(lib), np.isnan(ours))
+        assert np.array_equal(lib[:255], ours[:255])
+
+
+def test_mx_quantize_scale_exponent_and_packing(oracle_mod):
+    """The block exponent is floor(log2 amax) - 2 (via frexp); every code is the
+    E2M1 encoding of v / scale; dim 2j sits in the low nibble of byte j."""
+    rng = np.random.default_rng(41)
+    v = rng.standard_normal((50, 128)) * np.ldexp(1.0, rng.integers(-20, 20, (50, 1)))
+    v[3, 32:64] = 0.0
+    codes, scales = oracle_mod.mx_quantize(v)
+    assert codes.shape == (50, 64) and scales.shape == (50, 4)
+    for i in range(50):
+        for b in range(4):
+            blk = v[i, 32 * b:32 * (b + 1)]
+            amax = np.max(np.abs(blk))
+            if amax == 0.0:
+                assert scales[i, b] == 0
+                assert not codes[i, 16 * b:16 * (b + 1)].any()
+                continue
+            assert int(scales[i, b]) - 127 == math.frexp(amax)[1] - 3
+            sc = math.ldexp(1.0, int(scales[i, b]) - 127)
+            assert 4.0 <= amax / sc < 8.0
+            for j in (0, 1, 30, 31):
+                d = 32 * b + j
+                nib = codes[i, d // 2] & 0xF if d % 2 == 0 else codes[i, d // 2] >> 4
+                assert nib == oracle_mod.e2m1_encode(v[i, d] / sc)
+
+
+def test_mx_quantize_exact_on_grid_and_error_bound(oracle_mod):
+    rng = np.random.default_rng(42)
+    grid = _e2m1_grid()
+
+    def decode(codes, scales):
+        lo, hi = codes & 0xF, codes >> 4
+        nib = np.stack([lo, hi], -1).reshape(codes.shape[:-1] + (-1,))
+        mag = grid[nib & 7] * np.where(nib & 8, -1.0, 1.0)
+        return mag * np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=-1)
+
+    v = _grid_values(rng, (40, 128), lo=-12, hi=12)
+    assert np.array_equal(decode(*oracle_mod.mx_quantize(v)), v)
+    v = rng.standard_normal((40, 128)) * rng.uniform(0.01, 100.0, (40, 1))
+    codes, scales = oracle_mod.mx_quantize(v)
+    sc = np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=-1)
+    err = np.abs(decode(codes, scales) - v) / sc
+    # grid spacing 0.5 below 2, 1 below 4, 2 below 6; beyond 6 the clamp loses < 2
+    a = np.abs(v) / sc
+    bound = np.where(a <= 2, 0.25, np.where(a <= 4, 0.5, np.where(a <= 6, 1.0, 2.0)))
+    assert (err <= bound).all()
+
+
+def test_indexer_mx_equals_fp8_scorer_on_shared_grid(oracle_mod):
+    """Keys and queries on the MX grid are also E4M3 codes times a power-of-two
+    per-token (per-head) scale, exactly.  The FP8 scorer, pinned above, must then
+    give the same scores: this catches a wrong E2M1 value, nibble order, block
+    scale index or bias in the MX path."""
+    rng = np.random.default_rng(43)
+    n, R = 150, 2
+    kv = _grid_values(rng, (n, D))
+    kc, ks = oracle_mod.mx_quantize(kv)
+    cache_mx, bt = _mx_key_cache(kc, ks)
+    # FP8 form: codes of kv / 2^base with ks = 2^base, base the smallest block exponent
+    base = np.floor(np.log2(np.where(kv == 0, np.inf, np.abs(kv)).min(axis=1)))
+    base = np.where(np.isfinite(base), base, 0.0)
+    k8 = _e4m3(kv / np.ldexp(1.0, base.astype(np.int64))[:, None])
+    assert np.array_equal(_e4m3_vals(k8) * np.ldexp(1.0, base.astype(np.int64))[:, None], kv)
+    cache8, _ = _key_cache(k8, np.ldexp(1.0, base.astype(np.int64)).astype(np.float32))
+    qv = _grid_values(rng, (R, NH, D))
+    qc, qs = oracle_mod.mx_quantize(qv)
+    qbase = np.floor(np.log2(np.where(qv == 0, np.inf, np.abs(qv)).min(axis=2)))
+    qbase = np.where(np.isfinite(qbase), qbase, 0.0).astype(np.int64)
+    q8 = _e4m3(qv / np.ldexp(1.0, qbase)[..., None])
+    assert np.array_equal(_e4m3_vals(q8) * np.ldexp(1.0, qbase)[..., None], qv)
+    w = rng.uniform(-0.05, 0.1, (R, NH)).astype(np.float32)
+    row_len = [n, 97]
+    s_mx = oracle_mod.indexer_scores_mx(qc, qs, w, cache_mx, bt, [0, 0], row_len)
+    s_8 = oracle_mod.indexer_scores(q8, w, cache8, bt, [0, 0], row_len,
+                                    q_scale=np.ldexp(1.0, qbase).astype(np.float32))
+    assert np.array_equal(np.isnan(s_mx), np.isnan(s_8))
+    assert np.allclose(np.nan_to_num(s_mx), np.nan_to_num(s_8), rtol=1e-14, atol=1e-300)
+    assert (np.nan_to_num(s_mx) != 0).sum() > 100
+
+
+def test_indexer_mx_last_dim_and_scale_slot(oracle_mod):
+    """Key nonzero only in dim 127 (high nibble of byte 63, scale block 3), with a
+    per-token exponent: score = sum_h w_h relu(q_h[127] * 2^e_t)."""
+    n = 70  # crosses a page boundary
+    kc = np.zeros((n, 64), np.uint8)
+    kc[:, 63] = 0x20                        # dim 126 = 0, dim 127 = 1.0
+    ks = np.full((n, 4), 127, np.uint8)
+    e = np.array([t % 7 - 3 for t in range(n)])
+    ks[:, 3] = 127 + e
+    ks[:, :3] = 200                         # blocks 0-2 hold zeros; their scale must not leak
+    cache, bt = _mx_key_cache(kc, ks)
+    qc = np.zeros((1, NH, 64), np.uint8)
+    grid_codes = np.array([0x2, 0xA, 0x7, 0xF, 0x1, 0x0] * 6)[:NH]   # +-1, +-6, 0.5, 0
+    qc[0, :, 63] = (grid_codes << 4).astype(np.uint8)
+    qs = np.full((1, NH, 4), 127, np.uint8)
+    qs[0, :, 3] = 128                       # query block 3 scaled by 2
+    w = np.linspace(0.5, 1.5, NH).astype(np.float32)[None]
+    s = oracle_mod.indexer_scores_mx(qc, qs, w, cache, bt, [0], [n])
+    qv = np.array([1.0, -1.0, 6.0, -6.0, 0.5, 0.0] * 6)[:NH] * 2.0
+    per_head = np.maximum(0.0, qv)
+    ref = np.array([np.sum(w[0].astype(np.float64) * per_head * 2.0 ** et) for et in e])
+    assert np.allclose(s[0], ref, rtol=1e-14)
+
+
+def test_indexer_mx_zero_query_and_linearity(oracle_mod):
+    rng = np.random.default_rng(44)
+    n = 130
+    kc, ks = oracle_mod.mx_quantize(rng.standard_normal((n, D)))
+    cache, bt = _mx_key_cache(kc, ks)
+    qc, qs = oracle_mod.mx_quantize(rng.standard_normal((1, NH, D)))
+    w = rng.uniform(0.01, 0.1, (1, NH)).astype(np.float32)
+    s1 = oracle_mod.indexer_scores_mx(qc, qs, w, cache, bt, [0], [n])
+    s4 = oracle_mod.indexer_scores_mx(qc, qs, w * 4, cache, bt, [0], [n])
+    assert np.array_equal(s4, 4 * s1)
+    z = oracle_mod.indexer_scores_mx(np.zeros_like(qc), qs, w, cache, bt, [0], [n])
+    assert np.array_equal(z, np.zeros_like(z))
+
+
+def test_write_key_mx_codes_and_placement(oracle_mod):
+    """The MX Write step stores mx_quantize of torch's float64 layer_norm at the
+    slot the shuffled block table names, and touches nothing else."""
+    rng = np.random.default_rng(45)
+    T, max_pages, num_pages = 40, 4, 9
+    x = rng.standard_normal((T, D)) * 3 + 0.5
+    k_raw = _bf16_bits(x)
+    gamma = rng.uniform(0.5, 1.5, D)
+    beta = rng.uniform(-0.2, 0.2, D)
+    eps = 1e-6
+    bt = rng.permutation(num_pages)[:2 * max_pages].astype(np.int32).reshape(2, max_pages)
+    tok_req = rng.integers(0, 2, T).astype(np.int32)
+    tok_pos = rng.choice(max_pages * PAGE, T, replace=False).astype(np.int32)
+    cache0 = rng.integers(0, 256, (num_pages, MX_PAGE_BYTES)).astype(np.uint8)
+    cache, key_pre = oracle_mod.write_key_mx(k_raw, gamma, beta, eps, bt, tok_req, tok_pos,
+                                             cache0)
+    ln = torch.nn.functional.layer_norm(torch.from_numpy(_bf16_vals(k_raw)), (D,),
+                                        torch.from_numpy(gamma), torch.from_numpy(beta),
+                                        eps).numpy()
+    assert np.allclose(key_pre, ln, rtol=1e-12, atol=1e-12)
+    codes, scales = oracle_mod.mx_quantize(key_pre)
+    touched = np.zeros_like(cache0, dtype=bool)
+    for t in range(T):
+        pg = bt[tok_req[t], tok_pos[t] // PAGE]
+        s = tok_pos[t] % PAGE
+        assert np.array_equal(cache[pg, s * 64:(s + 1) * 64], codes[t])
+        assert np.array_equal(cache[pg, PAGE * 64 + s * 4:PAGE * 64 + (s + 1) * 4], scales[t])
+        touched[pg, s * 64:(s + 1) * 64] = True
+        touched[pg, PAGE * 64 + s * 4:PAGE * 64 + (s + 1) * 4] = True
+    assert np.array_equal(cache[~touched], cache0[~touched])
+
+
+def test_mx_byte_model_matches_pages(oracle_mod):
+    g = {k: float(v[0]) for k, v in _read_golden("byte_model.txt").items()}
+    assert MX_PAGE_BYTES // PAGE == g["mxfp4_index_key_bytes_per_token"]
+    assert oracle_mod.MX_KEY_PAGE_BYTES == MX_PAGE_BYTES
+    assert round(100 * (1 - MX_PAGE_BYTES / PAGE / traffic.KEY_BYTES), 1) == g[
+        "mxfp4_index_cache_saving"]
+    assert 24 * (g["nvfp4_latent_bytes_per_token"] + MX_PAGE_BYTES // PAGE) == g[
+        "kv_per_token_24_layers_k31_nvfp4_mxfp4"]
