@@ -26,6 +26,7 @@ PAGE = 64
 IDX_HEADS = 32
 IDX_DIM = 128
 KEY_PAGE_BYTES = 8448
+MXFP4_KEY_PAGE_BYTES = 4352   # 64 x 64 E2M1 code bytes, then 64 x 4 E8M0 scale bytes
 LAT_DIM = 576
 V_DIM = 512
 
@@ -39,11 +40,13 @@ SIGNATURES = [
     ("dsa_device_info", I32, [P, P, P]),
     ("dsa_indexer_score_workspace_size", SZ, [I32]),
     ("dsa_indexer_score", I32, [P, I32, P, P, P, I64, P, I32, I32, P, P, I32, P, I64, P, SZ, P]),
+    ("dsa_indexer_score_mxfp4", I32, [P, P, P, P, I64, P, I32, I32, P, P, I32, P, I64, P, SZ, P]),
     ("dsa_indexer_score_noalloc", I32, [P, I32, P, P, P, I64, P, I32, I32, P, P, I32, P, I64, P,
                                         P]),
     ("dsa_topk_workspace_size", SZ, [I32, I64, I32]),
     ("dsa_topk", I32, [P, I64, P, I32, I64, I32, P, P, SZ, P]),
     ("dsa_write_kv", I32, [P, P, P, F32, P, F32, P, I32, I32, P, P, I32, P, P, I64, P, P]),
+    ("dsa_write_kv_mxfp4", I32, [P, P, P, F32, P, F32, P, I32, I32, P, P, I32, P, P, I64, P, P]),
     ("dsa_topk_dcp_workspace_size", SZ, [I32, I64, I32, I32]),
     ("dsa_topk_dcp", I32, [P, I64, P, I32, I64, I32, I32, P, P, P, SZ, P]),
     ("dsa_sparse_mla_workspace_size", SZ, [I32, I32, I32]),
@@ -172,6 +175,35 @@ def dsa_indexer_score(q_idx, w, key_cache, block_table, row_req, row_len, *, q_s
     return scores
 
 
+def dsa_indexer_score_mxfp4(q_codes, q_scales, w, key_cache, block_table, row_req, row_len, *,
+                            scores=None, workspace=None):
+    """fp32 scores [R, max_pages*64] over MXFP4 keys and an MXFP4 query.
+
+    ``q_codes`` uint8 [R,32,64] (E2M1, dim 2j in the low nibble of byte j),
+    ``q_scales`` uint8 [R,32,4] (E8M0), ``key_cache`` uint8 pages of
+    MXFP4_KEY_PAGE_BYTES.  Entries at or past row_len are left unwritten."""
+    dev = key_cache.device
+    R = row_len.shape[0]
+    B, max_pages = block_table.shape
+    _need(q_codes, "q_codes", torch.uint8, dev)
+    _need(q_scales, "q_scales", torch.uint8, dev)
+    _need(w, "w", torch.float32, dev)
+    _need(key_cache, "key_cache", torch.uint8, dev)
+    for n, t in (("block_table", block_table), ("row_req", row_req), ("row_len", row_len)):
+        _need(t, n, torch.int32, dev)
+    ld = max_pages * PAGE
+    if scores is None:
+        scores = torch.empty((R, ld), dtype=torch.float32, device=dev)
+    _need(scores, "scores", torch.float32, dev)
+    ws = _workspace(indexer_score_workspace_size(R), dev, workspace)
+    _check("dsa_indexer_score_mxfp4", load().dsa_indexer_score_mxfp4(
+        _ptr(q_codes), _ptr(q_scales), _ptr(w), _ptr(key_cache),
+        key_cache.numel() // MXFP4_KEY_PAGE_BYTES, _ptr(block_table), B, max_pages,
+        _ptr(row_req), _ptr(row_len), R, _ptr(scores), scores.shape[1], _ptr(ws), ws.numel(),
+        _stream(dev)))
+    return scores
+
+
 def topk_workspace_size(R: int, max_len: int, k: int) -> int:
     return int(load().dsa_topk_workspace_size(int(R), int(max_len), int(k)))
 
@@ -193,8 +225,11 @@ def dsa_topk(scores, row_len, k, *, max_len=None, idx=None, workspace=None):
 
 
 def dsa_write_kv(k_raw, gamma, beta, eps, latent, latent_scale, block_table, tok_req, tok_pos,
-                 key_cache, latent_cache, *, dev_status=None):
-    """The Write step: new tokens' index keys and latent rows into the caches (in place)."""
+                 key_cache, latent_cache, *, dev_status=None, mxfp4_keys=False):
+    """The Write step: new tokens' index keys and latent rows into the caches (in place).
+
+    With ``mxfp4_keys`` the index keys go to pages of MXFP4_KEY_PAGE_BYTES
+    (dsa_write_kv_mxfp4)."""
     dev = key_cache.device
     _need(k_raw, "k_raw", torch.bfloat16, dev)
     _need(latent, "latent", torch.bfloat16, dev)
@@ -206,8 +241,9 @@ def dsa_write_kv(k_raw, gamma, beta, eps, latent, latent_scale, block_table, tok
         _need(t, n, torch.int32, dev)
     T = k_raw.shape[0]
     B, max_pages = block_table.shape
-    num_pages = key_cache.numel() // KEY_PAGE_BYTES
-    _check("dsa_write_kv", load().dsa_write_kv(
+    num_pages = key_cache.numel() // (MXFP4_KEY_PAGE_BYTES if mxfp4_keys else KEY_PAGE_BYTES)
+    name = "dsa_write_kv_mxfp4" if mxfp4_keys else "dsa_write_kv"
+    _check(name, getattr(load(), name)(
         _ptr(k_raw), _ptr(gamma), _ptr(beta), float(eps), _ptr(latent), float(latent_scale),
         _ptr(block_table), B, max_pages, _ptr(tok_req), _ptr(tok_pos), T, _ptr(key_cache),
         _ptr(latent_cache), num_pages, _ptr(dev_status) if dev_status is not None else None,

@@ -154,6 +154,30 @@ int dsa_indexer_score(const void* q_idx, int q_dtype, const float* q_scale, cons
   return to_status(launch_indexer_scan(a, st));
 }
 
+int dsa_indexer_score_mxfp4(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
+                            const uint8_t* key_cache, int64_t num_pages,
+                            const int32_t* block_table, int B, int max_pages,
+                            const int32_t* row_req, const int32_t* row_len, int R, float* scores,
+                            int64_t ld, void* workspace, size_t ws_bytes, void* stream) {
+  int s = check_rows(B, max_pages, block_table, row_req, row_len, R);
+  if (s) return s;
+  if (R > 0 && (!q_codes || !q_scales || !w || !key_cache || !scores)) return DSA_ERR_INVALID_ARG;
+  if (num_pages < 0 || ld < score_ld(max_pages) || ld % 4 != 0) return DSA_ERR_INVALID_ARG;
+  if ((scores && !aligned(scores, 16)) || (key_cache && !aligned(key_cache, 16)) ||
+      (q_codes && !aligned(q_codes, 16)) || (q_scales && !aligned(q_scales, 4)))
+    return DSA_ERR_INVALID_ARG;
+  s = check_workspace(workspace, ws_bytes, dsa_indexer_score_workspace_size(R));
+  if (s) return s;
+  cudaStream_t st = as_stream(stream);
+  if ((s = clear_status(workspace, st))) return s;
+  if (R == 0) return DSA_OK;
+  ScanArgs a{q_codes, kQMxfp4, nullptr, w, key_cache, num_pages, block_table, B, max_pages,
+             row_req, row_len, R, scores, ld, static_cast<uint8_t*>(workspace) + kStatusBytes,
+             static_cast<uint32_t*>(workspace)};
+  a.q_sf = q_scales;
+  return to_status(launch_indexer_scan(a, st));
+}
+
 // ---------------------------------------------------------------- Select
 size_t dsa_topk_workspace_size(int R, int64_t max_len, int k) {
   if (R < 0 || max_len < 0 || k < 1) return 0;
@@ -180,11 +204,12 @@ int dsa_topk(const float* scores, int64_t ld, const int32_t* row_len, int R, int
 }
 
 // ---------------------------------------------------------------- Write
-int dsa_write_kv(const void* k_raw, const float* gamma, const float* beta, float eps,
-                 const void* latent, float latent_scale, const int32_t* block_table, int B,
-                 int max_pages, const int32_t* tok_req, const int32_t* tok_pos, int T,
-                 uint8_t* key_cache, uint8_t* latent_cache, int64_t num_pages,
-                 uint32_t* dev_status, void* stream) {
+namespace {
+int write_kv(const void* k_raw, const float* gamma, const float* beta, float eps,
+             const void* latent, float latent_scale, const int32_t* block_table, int B,
+             int max_pages, const int32_t* tok_req, const int32_t* tok_pos, int T,
+             uint8_t* key_cache, uint8_t* latent_cache, int64_t num_pages, uint32_t* dev_status,
+             void* stream, bool mx_keys) {
   if (T < 0 || B < 0 || max_pages < 0 || num_pages < 0) return DSA_ERR_INVALID_ARG;
   if (!(latent_scale > 0.f) || !(latent_scale < INFINITY) || !(eps >= 0.f)) return DSA_ERR_INVALID_ARG;
   if (T > 0 && (B < 1 || max_pages < 1 || !k_raw || !gamma || !beta || !latent || !block_table ||
@@ -199,7 +224,29 @@ int dsa_write_kv(const void* k_raw, const float* gamma, const float* beta, float
   if (T == 0) return DSA_OK;
   WriteArgs a{k_raw, gamma, beta, eps, latent, latent_scale, block_table, B, max_pages,
               tok_req, tok_pos, T, key_cache, latent_cache, num_pages, dev_status};
+  a.mx_keys = mx_keys;
   return to_status(launch_write_kv(a, st));
+}
+}  // namespace
+
+int dsa_write_kv(const void* k_raw, const float* gamma, const float* beta, float eps,
+                 const void* latent, float latent_scale, const int32_t* block_table, int B,
+                 int max_pages, const int32_t* tok_req, const int32_t* tok_pos, int T,
+                 uint8_t* key_cache, uint8_t* latent_cache, int64_t num_pages,
+                 uint32_t* dev_status, void* stream) {
+  return write_kv(k_raw, gamma, beta, eps, latent, latent_scale, block_table, B, max_pages,
+                  tok_req, tok_pos, T, key_cache, latent_cache, num_pages, dev_status, stream,
+                  false);
+}
+
+int dsa_write_kv_mxfp4(const void* k_raw, const float* gamma, const float* beta, float eps,
+                       const void* latent, float latent_scale, const int32_t* block_table,
+                       int B, int max_pages, const int32_t* tok_req, const int32_t* tok_pos,
+                       int T, uint8_t* key_cache, uint8_t* latent_cache, int64_t num_pages,
+                       uint32_t* dev_status, void* stream) {
+  return write_kv(k_raw, gamma, beta, eps, latent, latent_scale, block_table, B, max_pages,
+                  tok_req, tok_pos, T, key_cache, latent_cache, num_pages, dev_status, stream,
+                  true);
 }
 
 // ------------------------------------ Select under decode context parallelism

@@ -19,6 +19,8 @@ constexpr int kIdxHeads = DSA_INDEX_HEADS;     // indexer heads
 constexpr int kIdxDim = DSA_INDEX_DIM;         // indexer head dim
 constexpr int kKeyPageBytes = DSA_KEY_PAGE_BYTES;
 constexpr int kKeyScaleOffset = kPage * kIdxDim;   // scales follow the 64 x 128 key bytes
+constexpr int kMxKeyPageBytes = DSA_MXFP4_KEY_PAGE_BYTES;   // 64 x 64 E2M1 bytes, 64 x 4 E8M0
+static_assert(kMxKeyPageBytes == kPage * (kIdxDim / 2 + 4), "MXFP4 page layout");
 constexpr int kLatDim = DSA_LATENT_DIM;
 constexpr int kVDim = DSA_V_DIM;
 constexpr int kMaxTopk = DSA_MAX_TOPK;
@@ -179,12 +181,17 @@ __device__ __forceinline__ uint32_t ordered_key(float f) {
 // ---- launchers (host side, one per kernel family) --------------------------
 namespace dsa {
 
+// Query format of the MXFP4 scorer: E2M1 codes [R][32][64] (two per byte) in
+// q_idx, E8M0 scales [R][32][4] in q_sf, keys in MXFP4 pages.
+constexpr int kQMxfp4 = 2;
+
 struct ScanArgs {
   const void* q_idx; int q_dtype; const float* q_scale; const float* w;
   const uint8_t* key_cache; int64_t num_pages; const int32_t* block_table; int B; int max_pages;
   const int32_t* row_req; const int32_t* row_len; int R; float* scores; int64_t ld;
   uint8_t* scratch;  // scan_scratch_bytes(R) bytes
   uint32_t* status;
+  const uint8_t* q_sf = nullptr;   // kQMxfp4 only
 };
 size_t scan_scratch_bytes(int R);
 cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st);
@@ -206,6 +213,7 @@ struct WriteArgs {
   uint8_t* key_cache; uint8_t* latent_cache; int64_t num_pages;
   uint32_t* status;   // may be NULL: the device checks are then not reported
   bool chained = false;
+  bool mx_keys = false;   // MXFP4 index keys (pages of kMxKeyPageBytes)
 };
 cudaError_t launch_write_kv(const WriteArgs& a, cudaStream_t st);
 

@@ -91,6 +91,23 @@ constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffTmem + 16;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 
+// MXFP4 keys (68 bytes per token: 64 bytes of E2M1 codes, then one E8M0 scale
+// per 32 dims).  Page: 64 x 64 code bytes, then 64 x 4 scale bytes.  The same
+// shared-memory plan with half-size key stages; the scale-factor rows that the
+// tensor core reads sit in the key region's unused second half.
+constexpr int kMxKeyBytes = kIdxDim / 2;
+constexpr int kMxPageKeyBytes = kPage * kMxKeyBytes;                // 4096
+constexpr int kMxKeyTileBytes = kTileTok * kMxKeyBytes;             // 8192
+constexpr int kMxQAtom = kMaxGroupRows * kIdxHeads * kMxKeyBytes;   // 128 rows x 64 B
+constexpr int kSfRowBytes = 32 * 16;                                // 32 rows x 16 B
+constexpr int kOffSfaMx = kOffKeys + kStages * kMxKeyTileBytes;     // [kScRing] key scale rows
+constexpr int kMxDBufs = 2;                                         // accumulators (TMEM holds the scales too)
+constexpr uint32_t kSfCol0 = kDCols * kMxDBufs;                     // scale columns: 8 per accumulator
+static_assert(kOffSfaMx + kScRing * kSfRowBytes <= kOffScale, "scale rows fit the key region");
+static_assert(kMxQAtom + kSfRowBytes <= kQBytes, "query codes and scale rows fit the query buffer");
+static_assert(kSfCol0 + 8 * kMxDBufs <= kTmemCols, "scale columns fit the allocation");
+static_assert(kMxDBufs % kEpiGroups == 0 && kMxDBufs % kMmaWarps == 0, "fixed accumulator owners");
+
 // group = {first row, rows, request, max row length}
 struct ScanWs {
   uint8_t* q8;     // [2 terms][R][32 heads][128] E4M3 query terms
@@ -126,6 +143,10 @@ ScanWs scan_ws(uint8_t* base, int R) {
 //    of one request; each run is cut into groups of up to 4 rows from its
 //    start.  Block-wide scans over chunks of 1024 rows give every row its run
 //    start, every group its index and every group its first tile.
+//  * MXFP4 query (q_dtype kQMxfp4): the codes are used as they are; CTA r
+//    only copies the head weights, and CTA R lays out each group's query
+//    scales as the tensor core's scale-factor rows (in the q8 area): row h,
+//    32-bit word j = the four E8M0 scales of head h of the group's row j.
 constexpr int kPrepThreads = 1024;
 
 template <typename T, typename Op>
@@ -165,7 +186,8 @@ __device__ __forceinline__ bool row_valid(const int32_t* row_req, const int32_t*
 
 __global__ void __launch_bounds__(kPrepThreads)
 scan_prep_kernel(const void* __restrict__ q_idx, int q_dtype, const float* __restrict__ q_scale,
-                 const float* __restrict__ w, const int32_t* __restrict__ row_req,
+                 const uint8_t* __restrict__ q_sf, const float* __restrict__ w,
+                 const int32_t* __restrict__ row_req,
                  const int32_t* __restrict__ row_len, int R, int B, int max_pages, int nctas,
                  ScanWs ws, uint32_t* status) {
   pdl_wait();
@@ -232,6 +254,22 @@ scan_prep_kernel(const void* __restrict__ q_idx, int q_dtype, const float* __res
         ws.cta[c] = make_int4(lo, tb, te, ngroups);
       }
     }
+    if (q_dtype == kQMxfp4) {
+      __syncthreads();                                    // every group is written
+      const uint32_t* qs = reinterpret_cast<const uint32_t*>(q_sf);   // [R][32] words
+      uint32_t* rows = reinterpret_cast<uint32_t*>(ws.q8);            // [groups][32][4] words
+      for (int e = threadIdx.x; e < ngroups * 128; e += kPrepThreads) {
+        const int g = e >> 7, h = (e >> 2) & 31, j = e & 3;
+        const int4 G = ws.groups[g];
+        rows[e] = j < G.y ? qs[(size_t)(G.x + j) * kIdxHeads + h] : 0x7F7F7F7Fu;
+      }
+    }
+    return;
+  }
+  if (q_dtype == kQMxfp4) {                         // the head weights as they are
+    const int r = blockIdx.x;
+    if (threadIdx.x < kIdxHeads)
+      ws.weff[(size_t)r * kIdxHeads + threadIdx.x] = w[(size_t)r * kIdxHeads + threadIdx.x];
     return;
   }
   // query split: warp h handles head h of row r, lane l dims [4l, 4l + 4)
@@ -378,6 +416,91 @@ __device__ __forceinline__ TilePages tile_pages(const TileCursor& c, const int32
   return t;
 }
 
+// MXFP4 MMA issuers (warps 0-1, tiles i % 2 == warp): the whole warp turns
+// the tile's key scales (landed in token order) into the tensor core's
+// scale-factor rows -- row l = the four scale bytes of tokens l, l + 32,
+// l + 64, l + 96 -- and lane 0 copies them and the group's query scale rows
+// into tensor memory, then issues the two K = 64 block-scaled MMAs (scale
+// bytes 0-1, then 2-3).  The copies and MMAs of one thread run in issue
+// order; the scale columns of accumulator db are rewritten only after the
+// epilogue has released db, i.e. after the MMAs that read them completed.
+__device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int ntiles,
+                                              uint32_t tmem_base, uint64_t* bars,
+                                              uint32_t* status) {
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* sc_full = bars + 2 * kStages;
+  uint64_t* sc_empty = sc_full + kScRing;
+  uint64_t* d_full = sc_empty + kScRing;
+  uint64_t* d_empty = d_full + kDBufs;
+  uint64_t* q_full = d_empty + kDBufs;
+  uint64_t* q_empty = q_full + kQBufs;
+  uint64_t* mma_done = q_empty + kQBufs;
+  const int m = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int cur_group = -1, gi = -1, left = 0;
+  bool issued_in_group = false;
+  uint32_t idesc0 = 0, idesc1 = 0;
+  const uint64_t a_desc_base = desc_kmajor_sw64(smem_u32(smem + kOffKeys));
+  const uint64_t b_desc = desc_kmajor_sw64(smem_u32(smem + kOffQ));
+  const uint64_t sfb_desc = desc_sf_rows16(smem_u32(smem + kOffQ + kMxQAtom));
+  int s = 0;
+  uint32_t s_phase = 0;
+  for (int i = 0; i < ntiles; ++i) {
+    if (cur.g != cur_group) {
+      cur_group = cur.g;
+      ++gi;
+      left = (cur.ge - cur.gs) - cur.t;
+      issued_in_group = false;
+      idesc0 = idesc_mxf4(kTileTok, kIdxHeads * cur.G.y, 0, 0);
+      idesc1 = idesc_mxf4(kTileTok, kIdxHeads * cur.G.y, 2, 2);
+      if (!warp_wait(&q_full[gi % kQBufs], (uint32_t)(gi / kQBufs) & 1, status)) break;
+    }
+    if (i % kMmaWarps == m) {
+      const int db = i % kMxDBufs, x = i % kScRing;
+      if (!warp_wait(&full[s], s_phase, status)) break;
+      if (!warp_wait(&sc_full[x], (uint32_t)(i / kScRing) & 1, status)) break;
+      if (!warp_wait(&d_empty[db], ((uint32_t)(i / kMxDBufs) & 1) ^ 1, status)) break;
+      const uint32_t* tok = reinterpret_cast<const uint32_t*>(smem + kOffScale + x * kTileTok * 4);
+      uint8_t* sf_rows = smem + kOffSfaMx + x * kSfRowBytes;
+      *reinterpret_cast<uint4*>(sf_rows + lane * 16) =
+          make_uint4(tok[lane], tok[lane + 32], tok[lane + 64], tok[lane + 96]);
+      fence_proxy_async_smem();                       // visible to the tensor core's copy
+      __syncwarp();
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(db * kDCols);
+        const uint32_t sfa = tmem_base + kSfCol0 + (uint32_t)(db * 8), sfb = sfa + 4;
+        tmem_cp_32x128b_warpx4(sfa, desc_sf_rows16(smem_u32(sf_rows)));
+        tmem_cp_32x128b_warpx4(sfb, sfb_desc);
+        const uint64_t a_desc = a_desc_base + (uint64_t)((s * kMxKeyTileBytes) >> 4);
+        mma_mxf4_ss(d_tmem, a_desc, b_desc, idesc0, sfa, sfb, 0u);
+        mma_mxf4_ss(d_tmem, a_desc + 2, b_desc + 2, idesc1, sfa, sfb, 1u);   // + 32 bytes of K
+        mma_commit(&empty[s]);
+        mma_commit(&sc_empty[x]);
+        mma_commit(&d_full[db]);
+      }
+      __syncwarp();
+      issued_in_group = true;
+    }
+    --left;
+    if ((i + 1 == ntiles || left == 0) && lane == 0) {   // the group's query operand is released
+      if (issued_in_group) mma_commit(&q_empty[gi % kQBufs]);
+      else mbar_arrive(&q_empty[gi % kQBufs]);
+    }
+    if (++s == kStages) {
+      s = 0;
+      s_phase ^= 1u;
+    }
+    if (left == 0 && i + 1 < ntiles) cur.advance(cur.ge - cur.gs - cur.t);   // next group
+  }
+  if (lane == 0) {
+    mma_commit(&mma_done[m]);                         // tensor memory is freed only after this
+    mbar_wait(&mma_done[m], 0, status);
+  }
+  __syncwarp();
+}
+
+template <bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
 scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__ CUtensorMap q_map,
             const uint8_t* __restrict__ key_cache, int64_t num_pages,
@@ -409,7 +532,7 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
     }
     for (int x = 0; x < kScRing; ++x) {
       mbar_init(&sc_full[x], 1);
-      mbar_init(&sc_empty[x], kEpiWarpsPerGroup);
+      mbar_init(&sc_empty[x], kEpiWarpsPerGroup + (kMx ? 1 : 0));   // MXFP4: + the MMA commit
     }
     for (int b = 0; b < kDBufs; ++b) {
       mbar_init(&d_full[b], 1);
@@ -458,64 +581,68 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
   }
 
   if (ntiles > 0 && warp < kMmaWarps) {
-    // ---------------- MMA issuers: lane 0 of warp m issues the tiles i with
-    // i % kMmaWarps == m.  An issuing thread is held at every tcgen05.mma
-    // until the tensor core takes it, and its barrier waits and commits cost
-    // about as much again per tile; with two issuers one thread's
-    // bookkeeping overlaps the other's MMAs.  Both walk every tile to follow
-    // the group, stage and accumulator sequence.
-    if (lane == 0) {
-      const int m = warp;
-      int cur_group = -1, gi = -1, left = 0;          // tiles left in the current group
-      bool issued_in_group = false;
-      uint32_t idesc = 0;
-      uint64_t b_desc = 0;
-      const uint64_t a_desc_base = desc_kmajor_sw128(smem_u32(smem + kOffKeys));
-      int s = 0;                                      // key stage of tile i
-      uint32_t s_phase = 0;
-      for (int i = 0; i < ntiles; ++i) {
-        if (cur.g != cur_group) {
-          cur_group = cur.g;
-          ++gi;
-          left = (cur.ge - cur.gs) - cur.t;
-          issued_in_group = false;
-          idesc = idesc_e4m3_f32(kTileTok, kIdxHeads * cur.G.y, false, false);
-          b_desc = desc_kmajor_sw128(smem_u32(smem + kOffQ + (gi % kQBufs) * kQBytes));
-          if (!mbar_wait(&q_full[gi % kQBufs], (uint32_t)(gi / kQBufs) & 1, status)) break;
-        }
-        if (i % kMmaWarps == m) {
-          const int db = i % kDBufs;
-          if (!mbar_wait(&full[s], s_phase, status)) break;
-          if (!mbar_wait(&d_empty[db], ((uint32_t)(i / kDBufs) & 1) ^ 1, status)) break;
-          tc_fence_after();
-          const uint64_t a_desc = a_desc_base + (uint64_t)((s * kKeyTileBytes) >> 4);
-          const uint32_t d_tmem = tmem_base + (uint32_t)(db * kDCols);
-#pragma unroll
-          for (int j = 0; j < 2 * kIdxDim / 32; ++j) {  // K = q_terms x 128 bytes in steps of 32
-            if (j >= q_terms * (kIdxDim / 32)) break;
-            mma_e4m3_ss(d_tmem, a_desc + (uint64_t)((j & 3) * 2),
-                        b_desc + (uint64_t)(((j >> 2) * kQAtom + (j & 3) * 32) >> 4), idesc,
-                        j > 0 ? 1u : 0u);
+    if constexpr (kMx) {
+      mx_mma_issuer(smem, cur, ntiles, tmem_base, bars, status);
+    } else {
+      // ---------------- MMA issuers: lane 0 of warp m issues the tiles i with
+      // i % kMmaWarps == m.  An issuing thread is held at every tcgen05.mma
+      // until the tensor core takes it, and its barrier waits and commits cost
+      // about as much again per tile; with two issuers one thread's
+      // bookkeeping overlaps the other's MMAs.  Both walk every tile to follow
+      // the group, stage and accumulator sequence.
+      if (lane == 0) {
+        const int m = warp;
+        int cur_group = -1, gi = -1, left = 0;          // tiles left in the current group
+        bool issued_in_group = false;
+        uint32_t idesc = 0;
+        uint64_t b_desc = 0;
+        const uint64_t a_desc_base = desc_kmajor_sw128(smem_u32(smem + kOffKeys));
+        int s = 0;                                      // key stage of tile i
+        uint32_t s_phase = 0;
+        for (int i = 0; i < ntiles; ++i) {
+          if (cur.g != cur_group) {
+            cur_group = cur.g;
+            ++gi;
+            left = (cur.ge - cur.gs) - cur.t;
+            issued_in_group = false;
+            idesc = idesc_e4m3_f32(kTileTok, kIdxHeads * cur.G.y, false, false);
+            b_desc = desc_kmajor_sw128(smem_u32(smem + kOffQ + (gi % kQBufs) * kQBytes));
+            if (!mbar_wait(&q_full[gi % kQBufs], (uint32_t)(gi / kQBufs) & 1, status)) break;
           }
-          mma_commit(&empty[s]);
-          mma_commit(&d_full[db]);
-          issued_in_group = true;
+          if (i % kMmaWarps == m) {
+            const int db = i % kDBufs;
+            if (!mbar_wait(&full[s], s_phase, status)) break;
+            if (!mbar_wait(&d_empty[db], ((uint32_t)(i / kDBufs) & 1) ^ 1, status)) break;
+            tc_fence_after();
+            const uint64_t a_desc = a_desc_base + (uint64_t)((s * kKeyTileBytes) >> 4);
+            const uint32_t d_tmem = tmem_base + (uint32_t)(db * kDCols);
+  #pragma unroll
+            for (int j = 0; j < 2 * kIdxDim / 32; ++j) {  // K = q_terms x 128 bytes in steps of 32
+              if (j >= q_terms * (kIdxDim / 32)) break;
+              mma_e4m3_ss(d_tmem, a_desc + (uint64_t)((j & 3) * 2),
+                          b_desc + (uint64_t)(((j >> 2) * kQAtom + (j & 3) * 32) >> 4), idesc,
+                          j > 0 ? 1u : 0u);
+            }
+            mma_commit(&empty[s]);
+            mma_commit(&d_full[db]);
+            issued_in_group = true;
+          }
+          --left;
+          if (i + 1 == ntiles || left == 0) {           // the group's query operand is released
+            if (issued_in_group) mma_commit(&q_empty[gi % kQBufs]);
+            else mbar_arrive(&q_empty[gi % kQBufs]);
+          }
+          if (++s == kStages) {
+            s = 0;
+            s_phase ^= 1u;
+          }
+          if (left == 0 && i + 1 < ntiles) cur.advance(cur.ge - cur.gs - cur.t);   // next group
         }
-        --left;
-        if (i + 1 == ntiles || left == 0) {           // the group's query operand is released
-          if (issued_in_group) mma_commit(&q_empty[gi % kQBufs]);
-          else mbar_arrive(&q_empty[gi % kQBufs]);
-        }
-        if (++s == kStages) {
-          s = 0;
-          s_phase ^= 1u;
-        }
-        if (left == 0 && i + 1 < ntiles) cur.advance(cur.ge - cur.gs - cur.t);   // next group
+        mma_commit(&mma_done[m]);                       // tensor memory is freed only after this
+        mbar_wait(&mma_done[m], 0, status);
       }
-      mma_commit(&mma_done[m]);                       // tensor memory is freed only after this
-      mbar_wait(&mma_done[m], 0, status);
+      __syncwarp();
     }
-    __syncwarp();
   } else if (ntiles > 0 && warp >= kMmaWarps && warp < kEpiWarp0) {
     // ---------------- TMA producers: warp kMmaWarps + p loads the tiles i with
     // i % kProdWarps == p.  Page ids are looked up a batch of 32 tiles ahead:
@@ -563,12 +690,19 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
         }
         if (!warp_wait(&q_empty[gi % kQBufs], ((uint32_t)(gi / kQBufs) & 1) ^ 1, status)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&q_full[gi % kQBufs], q_terms * kQAtom);
           uint8_t* qd = smem + kOffQ + (gi % kQBufs) * kQBytes;
-          tma_load_2d(qd, &q_map, 0, cur.G.x * kIdxHeads, &q_full[gi % kQBufs]);
-          if (q_terms == 2)
-            tma_load_2d(qd + kQAtom, &q_map, 0, (n_rows + cur.G.x) * kIdxHeads,
-                        &q_full[gi % kQBufs]);
+          if constexpr (kMx) {                        // codes, then the group's scale rows
+            mbar_arrive_expect_tx(&q_full[gi % kQBufs], kMxQAtom + kSfRowBytes);
+            tma_load_2d(qd, &q_map, 0, cur.G.x * kIdxHeads, &q_full[gi % kQBufs]);
+            bulk_g2s(qd + kMxQAtom, ws.q8 + (size_t)cur.g * kSfRowBytes, kSfRowBytes,
+                     &q_full[gi % kQBufs]);
+          } else {
+            mbar_arrive_expect_tx(&q_full[gi % kQBufs], q_terms * kQAtom);
+            tma_load_2d(qd, &q_map, 0, cur.G.x * kIdxHeads, &q_full[gi % kQBufs]);
+            if (q_terms == 2)
+              tma_load_2d(qd + kQAtom, &q_map, 0, (n_rows + cur.G.x) * kIdxHeads,
+                          &q_full[gi % kQBufs]);
+          }
         }
       }
       if (i % kProdWarps != pw) {
@@ -583,19 +717,23 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
         const bool v1 = need1 && page_ok(p1, num_pages);
         if ((need0 && !v0) || (need1 && !v1)) raise_dev(status, DSA_DEV_BAD_PAGE);
         pv_s[x] = (v0 ? 1u : 0u) | (v1 ? 2u : 0u);
-        uint8_t* kd = smem + kOffKeys + s * kKeyTileBytes;
+        // key codes of the two pages, and their scales in token order (fp32
+        // per token, or the four E8M0 bytes per token of MXFP4 keys)
+        constexpr int kStage = kMx ? kMxKeyTileBytes : kKeyTileBytes;
+        constexpr int kHalf = kMx ? kMxPageKeyBytes : kPageKeyBytes;
+        constexpr int kPg = kMx ? kMxKeyPageBytes : kPageBytes;
+        uint8_t* kd = smem + kOffKeys + s * kStage;
         uint8_t* sd = smem + kOffScale + x * kTileTok * 4;
         const uint32_t nv = (v0 ? 1u : 0u) + (v1 ? 1u : 0u);
-        mbar_arrive_expect_tx(&full[s], nv * kPageKeyBytes);
+        mbar_arrive_expect_tx(&full[s], nv * kHalf);
         mbar_arrive_expect_tx(&sc_full[x], nv * kPage * 4);
         if (v0) {
           tma_load_3d(kd, &key_map, 0, 0, p0, &full[s]);
-          bulk_g2s(sd, key_cache + (size_t)p0 * kPageBytes + kPageKeyBytes, kPage * 4, &sc_full[x]);
+          bulk_g2s(sd, key_cache + (size_t)p0 * kPg + kHalf, kPage * 4, &sc_full[x]);
         }
         if (v1) {
-          tma_load_3d(kd + kPageKeyBytes, &key_map, 0, 0, p1, &full[s]);
-          bulk_g2s(sd + kPage * 4, key_cache + (size_t)p1 * kPageBytes + kPageKeyBytes,
-                   kPage * 4, &sc_full[x]);
+          tma_load_3d(kd + kHalf, &key_map, 0, 0, p1, &full[s]);
+          bulk_g2s(sd + kPage * 4, key_cache + (size_t)p1 * kPg + kHalf, kPage * 4, &sc_full[x]);
         }
       }
       __syncwarp();
@@ -619,8 +757,9 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
     int cur_group = -1;
     int len[kEpiRows];
     if (eg > 0) cur.advance(eg);
+    constexpr int kDB = kMx ? kMxDBufs : kDBufs;
     for (int i = eg; i < ntiles; i += kEpiGroups) {
-      const int x = i % kScRing, db = i % kDBufs;
+      const int x = i % kScRing, db = i % kDB;
       if (cur.g != cur_group) {                       // this warp's rows of the new group
         cur_group = cur.g;
 #pragma unroll
@@ -631,11 +770,11 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
         }
         __syncwarp();
       }
-      if (!warp_wait(&d_full[db], (uint32_t)(i / kDBufs) & 1, status)) break;
+      if (!warp_wait(&d_full[db], (uint32_t)(i / kDB) & 1, status)) break;
       if (!warp_wait(&sc_full[x], (uint32_t)(i / kScRing) & 1, status)) break;
       tc_fence_after();
       const bool page_valid = (pv_s[x] >> (tok_in >> 6)) & 1u;
-      const float ks = scale_s[x * kTileTok + tok_in];
+      const float ks = kMx ? 1.f : scale_s[x * kTileTok + tok_in];   // MXFP4: scaled in the MMA
       const int tok = cur.t * kTileTok + tok_in;
 #pragma unroll
       for (int rr = 0; rr < kEpiRows; ++rr) {
@@ -689,7 +828,9 @@ size_t scan_scratch_bytes(int R) {
 
 cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st) {
   if (a.R == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const bool mx = a.q_dtype == kQMxfp4;
+  const auto kernel = mx ? scan_kernel<true> : scan_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemAlloc);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
@@ -701,23 +842,26 @@ cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st) {
   // keys: [page][64 tokens][128 B] inside pages of 8448 bytes; a box is one
   // page's key block.  Queries: [2 terms x R x 32 rows][128 B]; a box is 128
   // rows (one term of a group of up to 4 rows; rows past the group are never
-  // multiplied).
+  // multiplied).  MXFP4: [page][64 tokens][64 B] inside pages of 4352 bytes
+  // and the caller's [R x 32 rows][64 B] query codes, 64-byte swizzle.
   alignas(64) CUtensorMap kmap, qmap;
-  const uint64_t kdims[3] = {(uint64_t)kIdxDim, (uint64_t)kPage,
+  const uint64_t row_bytes = mx ? kMxKeyBytes : kIdxDim;
+  const uint64_t kdims[3] = {row_bytes, (uint64_t)kPage,
                              (uint64_t)(a.num_pages > 0 ? a.num_pages : 1)};
-  const uint64_t kstr[2] = {(uint64_t)kIdxDim, (uint64_t)kPageBytes};
-  const uint32_t kbox[3] = {(uint32_t)kIdxDim, (uint32_t)kPage, 1};
-  e = encode_tensor_map_u8(&kmap, 3, a.key_cache, kdims, kstr, kbox);
+  const uint64_t kstr[2] = {row_bytes, (uint64_t)(mx ? kMxKeyPageBytes : kPageBytes)};
+  const uint32_t kbox[3] = {(uint32_t)row_bytes, (uint32_t)kPage, 1};
+  const int swz = mx ? 64 : 128;
+  e = encode_tensor_map_u8(&kmap, 3, a.key_cache, kdims, kstr, kbox, swz);
   if (e != cudaSuccess) return e;
-  const uint64_t qdims[2] = {(uint64_t)kIdxDim, (uint64_t)2 * a.R * kIdxHeads};
-  const uint64_t qstr[1] = {(uint64_t)kIdxDim};
-  const uint32_t qbox[2] = {(uint32_t)kIdxDim, (uint32_t)(kMaxGroupRows * kIdxHeads)};
-  e = encode_tensor_map_u8(&qmap, 2, ws.q8, qdims, qstr, qbox);
+  const uint64_t qdims[2] = {row_bytes, (uint64_t)(mx ? 1 : 2) * a.R * kIdxHeads};
+  const uint64_t qstr[1] = {row_bytes};
+  const uint32_t qbox[2] = {(uint32_t)row_bytes, (uint32_t)(kMaxGroupRows * kIdxHeads)};
+  e = encode_tensor_map_u8(&qmap, 2, mx ? a.q_idx : ws.q8, qdims, qstr, qbox, swz);
   if (e != cudaSuccess) return e;
-  scan_prep_kernel<<<a.R + 1, kPrepThreads, 0, st>>>(a.q_idx, a.q_dtype, a.q_scale, a.w, a.row_req,
-                                             a.row_len, a.R, a.B, a.max_pages, sms, ws,
-                                             a.status);
-  e = launch_kernel(scan_kernel, dim3(sms), dim3(kThreads), kSmemAlloc, st, true, kmap, qmap,
+  scan_prep_kernel<<<a.R + 1, kPrepThreads, 0, st>>>(a.q_idx, a.q_dtype, a.q_scale, a.q_sf, a.w,
+                                             a.row_req, a.row_len, a.R, a.B, a.max_pages, sms,
+                                             ws, a.status);
+  e = launch_kernel(kernel, dim3(sms), dim3(kThreads), kSmemAlloc, st, true, kmap, qmap,
                     a.key_cache, a.num_pages, a.block_table, a.max_pages, a.row_len, a.scores,
                     a.ld, a.R, a.q_dtype == DSA_E4M3 ? 1 : 2, ws, a.status);
   if (e != cudaSuccess) return e;

@@ -271,6 +271,56 @@ __device__ __forceinline__ void mma_e4m3_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// ---- block-scaled FP4 (MXFP4) -------------------------------------------------
+// Instruction descriptor of kind::mxf4 (block_scale, scale_vec::2X): E2M1 A and
+// B, packed two to a byte, both K-major; UE8M0 scale factors, one per 32
+// elements along K; f32 accumulator; shape M x N.  sf_a / sf_b (0 or 2) pick
+// which two of the four scale bytes in each 32-bit tensor-memory column this
+// instruction's K = 64 uses.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, int sf_a, int sf_b) {
+  return ((uint32_t)(sf_b & 3) << 4)        // B scale-factor byte
+         | (1u << 7)                        // A format: E2M1
+         | (1u << 10)                       // B format: E2M1
+         | ((uint32_t)(N >> 3) << 17)       // N / 8
+         | (1u << 23)                       // scale format: UE8M0
+         | ((uint32_t)(M >> 4) << 24)       // M / 16
+         | ((uint32_t)(sf_a & 3) << 29);    // A scale-factor byte
+}
+
+// Shared-memory descriptor of a scale-factor block for tcgen05.cp 32x128b:
+// 32 rows of 16 bytes, contiguous (no swizzle; 8-row groups 128 bytes apart).
+__device__ __forceinline__ uint64_t desc_sf_rows16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);   // start address, bits 0-13
+  d |= (uint64_t)(128 >> 4) << 16;            // leading byte offset, bits 16-29
+  d |= (uint64_t)(128 >> 4) << 32;            // stride byte offset, bits 32-45
+  d |= (uint64_t)1 << 46;                     // descriptor version for sm_100, bits 46-47
+  return d;                                   // layout (bits 61-63): no swizzle
+}
+
+// Copy 32 rows x 16 bytes of shared memory into tensor memory at taddr,
+// replicated into all four lane quarters: row i goes to lane i (+ 32 q) and
+// its four 32-bit words to columns taddr .. taddr + 3.  Ordered before the
+// issuing thread's later tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc)
+               : "memory");
+}
+
+// D[tmem] (+)= (A * 2^sfA) * (B * 2^sfB)^T, E2M1 operands from shared memory
+// (K = 64 per instruction), scale factors from tensor memory.
+__device__ __forceinline__ void mma_mxf4_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+      "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc]^T with 8-bit operands (A in tensor memory:
 // row i of A in lane i, four consecutive K elements per 32-bit column).
 __device__ __forceinline__ void mma_e4m3_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,

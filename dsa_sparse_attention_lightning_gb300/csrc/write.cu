@@ -20,6 +20,17 @@
 // and absmax are warp reductions, the codes one 4-byte store per lane) and
 // 16-byte chunks l and l + 32 of the 576-byte latent row.  Memory bound
 // (256 + 1152 bytes read, 132 + 576 written per token).
+//
+// MXFP4 index keys (vLLM Day-0 post on Kimi K3.1 Pro, "Hybrid KV cache without
+// padding": 68 bytes per key; one E8M0 scale per 32 values): the normalized
+// key is quantized per block of 32 dims (OCP Microscaling v1.0 conversion):
+//   e      = floor(log2(max |k|)) - 2, clamped to [-127, 127] (-127 for an
+//            all-zero block)
+//   codes  = E2M1(k / 2^e)   (round to nearest even on the grid 0, 0.5, 1,
+//            1.5, 2, 3, 4, 6, beyond 6 clamped to 6)
+// into page block_table[req][pos / 64] (4352 bytes): the 64 code bytes at
+// slot * 64 (dim 2j in the low nibble of byte j), the four scale bytes
+// e + 127 at 64 * 64 + slot * 4.  A block is 8 lanes.
 #include "dsa_common.cuh"
 
 namespace dsa {
@@ -46,9 +57,20 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
          ((uint32_t)__nv_cvt_float_to_fp8(d, __NV_SATFINITE, __NV_E4M3) << 24);
 }
 
+// E2M1 code of x (|x| < 8 after the block scaling): the grid's midpoints 0.25,
+// 0.75, 1.25, 1.75, 2.5, 3.5 and 5 are counted, a value at a midpoint going to
+// the neighbour with an even code.
+__device__ __forceinline__ uint32_t e2m1(float x) {
+  const float a = fabsf(x);
+  const uint32_t m = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+                     (a >= 3.5f) + (a > 5.f);
+  return m | (signbit(x) ? 8u : 0u);
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+template <bool kMx>
 __global__ void __launch_bounds__(kWarps * 32)
 write_kv_kernel(const uint16_t* __restrict__ k_raw, const float* __restrict__ gamma,
                 const float* __restrict__ beta, float eps, const uint16_t* __restrict__ latent,
@@ -85,12 +107,33 @@ write_kv_kernel(const uint16_t* __restrict__ k_raw, const float* __restrict__ ga
   const float4 bt = *reinterpret_cast<const float4*>(beta + 4 * lane);
   const float k[4] = {g.x * ((x[0] - mean) / sd) + bt.x, g.y * ((x[1] - mean) / sd) + bt.y,
                       g.z * ((x[2] - mean) / sd) + bt.z, g.w * ((x[3] - mean) / sd) + bt.w};
-  const float amax = warp_max(fmaxf(fmaxf(fabsf(k[0]), fabsf(k[1])), fmaxf(fabsf(k[2]), fabsf(k[3]))));
-  const float ks = amax > 0.f ? amax / 448.f : 1.f;
-  uint8_t* kp = key_cache + (size_t)page * kKeyPageBytes;
-  *reinterpret_cast<uint32_t*>(kp + slot * kIdxDim + 4 * lane) =
-      e4m3x4(k[0] / ks, k[1] / ks, k[2] / ks, k[3] / ks);
-  if (lane == 0) *reinterpret_cast<float*>(kp + kKeyScaleOffset + slot * 4) = ks;
+  const float lmax = fmaxf(fmaxf(fabsf(k[0]), fabsf(k[1])), fmaxf(fabsf(k[2]), fabsf(k[3])));
+  if constexpr (kMx) {
+    float bmax = lmax;                              // the 8 lanes of this lane's block
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, o));
+    // floor(log2(bmax)) is the exponent field of a normal bmax; a subnormal or
+    // zero bmax lands below -127 and is clamped
+    const int e = min(max((int)(__float_as_uint(bmax) >> 23) - 127 - 2, -127), 127);
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c |= e2m1(ldexpf(k[i], -e)) << (4 * i);
+    uint8_t* kp = key_cache + (size_t)page * kMxKeyPageBytes;
+    *reinterpret_cast<uint16_t*>(kp + slot * (kIdxDim / 2) + 2 * lane) = (uint16_t)c;
+    const uint32_t sc = (uint32_t)(e + 127);        // lanes 0, 8, 16, 24 hold blocks 0-3
+    const uint32_t word = __shfl_sync(0xffffffffu, sc, 0) | (__shfl_sync(0xffffffffu, sc, 8) << 8) |
+                          (__shfl_sync(0xffffffffu, sc, 16) << 16) |
+                          (__shfl_sync(0xffffffffu, sc, 24) << 24);
+    if (lane == 0)
+      *reinterpret_cast<uint32_t*>(kp + kPage * (kIdxDim / 2) + slot * 4) = word;
+  } else {
+    const float amax = warp_max(lmax);
+    const float ks = amax > 0.f ? amax / 448.f : 1.f;
+    uint8_t* kp = key_cache + (size_t)page * kKeyPageBytes;
+    *reinterpret_cast<uint32_t*>(kp + slot * kIdxDim + 4 * lane) =
+        e4m3x4(k[0] / ks, k[1] / ks, k[2] / ks, k[3] / ks);
+    if (lane == 0) *reinterpret_cast<float*>(kp + kKeyScaleOffset + slot * 4) = ks;
+  }
 
   // ---- latent row: 36 chunks of 16 codes (32 bytes of bf16 in each)
   const uint4* src = reinterpret_cast<const uint4*>(latent + (size_t)t * kLatDim);
@@ -112,7 +155,7 @@ write_kv_kernel(const uint16_t* __restrict__ k_raw, const float* __restrict__ ga
 cudaError_t launch_write_kv(const WriteArgs& a, cudaStream_t st) {
   if (a.T == 0) return cudaSuccess;
   const cudaError_t e =
-      launch_kernel(write_kv_kernel, dim3((a.T + kWarps - 1) / kWarps), dim3(kWarps * 32), 0, st,
+      launch_kernel(a.mx_keys ? write_kv_kernel<true> : write_kv_kernel<false>, dim3((a.T + kWarps - 1) / kWarps), dim3(kWarps * 32), 0, st,
                     a.chained, static_cast<const uint16_t*>(a.k_raw), a.gamma, a.beta, a.eps,
                     static_cast<const uint16_t*>(a.latent), a.latent_scale, a.block_table, a.B,
                     a.max_pages, a.tok_req, a.tok_pos, a.T, a.key_cache, a.latent_cache,

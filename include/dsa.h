@@ -80,6 +80,7 @@ extern "C" {
 #define DSA_INDEX_HEADS 32
 #define DSA_INDEX_DIM 128
 #define DSA_KEY_PAGE_BYTES 8448
+#define DSA_MXFP4_KEY_PAGE_BYTES 4352 /* 64 x 64 E2M1 code bytes, then 64 x 4 E8M0 scales */
 #define DSA_LATENT_DIM 576
 #define DSA_V_DIM 512
 #define DSA_MAX_TOPK 2048
@@ -127,6 +128,32 @@ int dsa_indexer_score(const void* q_idx, int q_dtype, const float* q_scale, cons
                       int B, int max_pages, const int32_t* row_req, const int32_t* row_len,
                       int R, float* scores, int64_t ld, void* workspace, size_t ws_bytes,
                       void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsa_indexer_score_mxfp4 -- step 1 over MXFP4 index keys and an MXFP4 query
+ * (vLLM Day-0 post on Kimi K3.1 Pro, "Hybrid KV cache without padding": index
+ * keys at 68 bytes in MXFP4; "Native MXFP4 indexer": FP4 products with FP32
+ * accumulation and a weighted reduction over heads).
+ *
+ * scores[r][s] = sum_{h<32} w[r][h] * max(0, q[r][h] . key[s]), where every
+ * value is an E2M1 element times the E8M0 scale of its block of 32 dims
+ * (OCP Microscaling v1.0 formats), on the block-scaled FP4 tensor cores.
+ *
+ *  q_codes  [R][32][64] bytes: E2M1 codes, dim 2j in the low nibble of byte j;
+ *           16-byte aligned.
+ *  q_scales [R][32][4] E8M0 bytes (byte b scales dims 32b .. 32b + 31).
+ *  w        fp32 [R][32] head weights (any sign).
+ *  key_cache pages of DSA_MXFP4_KEY_PAGE_BYTES: token slot t's 64 code bytes
+ *           at t * 64, its four scale bytes at 64 * 64 + t * 4; 16-byte aligned.
+ *  scores, row_req, row_len, block_table, workspace: as dsa_indexer_score
+ *  (workspace >= dsa_indexer_score_workspace_size(R)).
+ * Errors: as dsa_indexer_score.
+ * ---------------------------------------------------------------------- */
+int dsa_indexer_score_mxfp4(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
+                            const uint8_t* key_cache, int64_t num_pages,
+                            const int32_t* block_table, int B, int max_pages,
+                            const int32_t* row_req, const int32_t* row_len, int R, float* scores,
+                            int64_t ld, void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
  * dsa_indexer_score_noalloc -- dsa_indexer_score for callers that cannot
@@ -210,6 +237,24 @@ int dsa_write_kv(const void* k_raw, const float* gamma, const float* beta, float
                  int max_pages, const int32_t* tok_req, const int32_t* tok_pos, int T,
                  uint8_t* key_cache, uint8_t* latent_cache, int64_t num_pages,
                  uint32_t* dev_status, void* stream);
+
+/* ------------------------------------------------------------------------
+ * dsa_write_kv_mxfp4 -- the Write step with MXFP4 index keys (68 bytes per
+ * key: vLLM Day-0 post on Kimi K3.1 Pro, "Hybrid KV cache without padding";
+ * one E8M0 scale per 32 values: AMD Instinct post on Kimi K3.1 Pro,
+ * quantization list).  The key is normalized as in dsa_write_kv, then
+ * quantized per block of 32 dims by the OCP Microscaling v1.0 conversion:
+ * e = floor(log2(max |k|)) - 2 clamped to [-127, 127] (-127 for a zero
+ * block), codes = E2M1(k / 2^e) rounded to nearest even and clamped to 6,
+ * into key_cache pages of DSA_MXFP4_KEY_PAGE_BYTES (the layout of
+ * dsa_indexer_score_mxfp4).  The latent row is written as by dsa_write_kv.
+ * Arguments, alignment and errors as dsa_write_kv.
+ * ---------------------------------------------------------------------- */
+int dsa_write_kv_mxfp4(const void* k_raw, const float* gamma, const float* beta, float eps,
+                       const void* latent, float latent_scale, const int32_t* block_table,
+                       int B, int max_pages, const int32_t* tok_req, const int32_t* tok_pos,
+                       int T, uint8_t* key_cache, uint8_t* latent_cache, int64_t num_pages,
+                       uint32_t* dev_status, void* stream);
 
 /* ------------------------------------------------------------------------
  * dsa_topk_dcp -- step 2 as decode context parallelism runs it, the W GPUs

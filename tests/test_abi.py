@@ -124,6 +124,30 @@ def test_write_kv_rejects_bad_arguments(lib):
     assert call(T=0) == 0                            # nothing to write: no GPU work at all
 
 
+def test_write_kv_mxfp4_rejects_bad_arguments(lib):
+    odd = ctypes.c_void_p((1 << 20) + 4)
+    call = lambda T=2, ls=1.0, eps=1e-6, k=FAKE, kc=FAKE: lib.dsa_write_kv_mxfp4(
+        k, FAKE, FAKE, eps, FAKE, ls, FAKE, 1, 4, FAKE, FAKE, T, kc, FAKE, 4, None, None)
+    assert call(T=-1) == 1
+    assert call(ls=0.0) == 1 and call(eps=-1.0) == 1
+    assert call(k=None) == 1 and call(k=odd) == 1 and call(kc=odd) == 1
+    assert call(T=0) == 0
+
+
+def test_indexer_score_mxfp4_rejects_bad_arguments(lib):
+    ws = lib.dsa_indexer_score_workspace_size(3)
+    call = lambda R=3, qc=FAKE, qs=FAKE, ld=256, work=FAKE, ws_bytes=ws, mp=4: (
+        lib.dsa_indexer_score_mxfp4(qc, qs, FAKE, FAKE, 8, FAKE, 2, mp, FAKE, FAKE, R, FAKE, ld,
+                                    work, ws_bytes, None))
+    assert call(R=-1) == 1
+    assert call(R=70000) == 2
+    assert call(qc=None) == 1 and call(qs=None) == 1
+    assert call(qc=ctypes.c_void_p((1 << 20) + 8)) == 1    # codes must be 16-byte aligned
+    assert call(qs=ctypes.c_void_p((1 << 20) + 2)) == 1    # scales must be 4-byte aligned
+    assert call(ld=255) == 1 and call(ld=128) == 1          # ld % 4, ld < max_pages * 64
+    assert call(work=None) == 3 and call(ws_bytes=ws - 1) == 3
+
+
 def test_selftest_rejects_bad_arguments(lib):
     need = lib.dsa_selftest_workspace_size()
     assert need >= 768
