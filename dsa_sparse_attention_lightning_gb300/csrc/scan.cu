@@ -106,7 +106,8 @@ constexpr uint32_t kSfCol0 = kDCols * kMxDBufs;                     // scale col
 static_assert(kOffSfaMx + kScRing * kSfRowBytes <= kOffScale, "scale rows fit the key region");
 static_assert(kMxQAtom + kSfRowBytes <= kQBytes, "query codes and scale rows fit the query buffer");
 static_assert(kSfCol0 + 8 * kMxDBufs <= kTmemCols, "scale columns fit the allocation");
-static_assert(kMxDBufs % kEpiGroups == 0 && kMxDBufs % kMmaWarps == 0, "fixed accumulator owners");
+static_assert(kMxDBufs == kEpiGroups && kMxDBufs == kMmaWarps,
+              "accumulator db belongs to MMA warp db and epilogue group db");
 
 // group = {first row, rows, request, max row length}
 struct ScanWs {
@@ -445,6 +446,7 @@ __device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int
   const uint64_t sfb_desc = desc_sf_rows16(smem_u32(smem + kOffQ + kMxQAtom));
   int s = 0;
   uint32_t s_phase = 0;
+  int sfb_gi = -1;                                    // group whose query scales are in TMEM
   for (int i = 0; i < ntiles; ++i) {
     if (cur.g != cur_group) {
       cur_group = cur.g;
@@ -457,21 +459,26 @@ __device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int
     }
     if (i % kMmaWarps == m) {
       const int db = i % kMxDBufs, x = i % kScRing;
-      if (!warp_wait(&full[s], s_phase, status)) break;
+      // the scale rows are built before the accumulator wait, off the path
+      // from the previous epilogue to this tile's MMAs
       if (!warp_wait(&sc_full[x], (uint32_t)(i / kScRing) & 1, status)) break;
-      if (!warp_wait(&d_empty[db], ((uint32_t)(i / kMxDBufs) & 1) ^ 1, status)) break;
       const uint32_t* tok = reinterpret_cast<const uint32_t*>(smem + kOffScale + x * kTileTok * 4);
       uint8_t* sf_rows = smem + kOffSfaMx + x * kSfRowBytes;
       *reinterpret_cast<uint4*>(sf_rows + lane * 16) =
           make_uint4(tok[lane], tok[lane + 32], tok[lane + 64], tok[lane + 96]);
       fence_proxy_async_smem();                       // visible to the tensor core's copy
       __syncwarp();
+      if (!warp_wait(&full[s], s_phase, status)) break;
+      if (!warp_wait(&d_empty[db], ((uint32_t)(i / kMxDBufs) & 1) ^ 1, status)) break;
       if (lane == 0) {
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(db * kDCols);
         const uint32_t sfa = tmem_base + kSfCol0 + (uint32_t)(db * 8), sfb = sfa + 4;
         tmem_cp_32x128b_warpx4(sfa, desc_sf_rows16(smem_u32(sf_rows)));
-        tmem_cp_32x128b_warpx4(sfb, sfb_desc);
+        // accumulator db (= this warp) keeps its query scale rows for the
+        // whole group; the MMAs that read the previous group's have completed
+        // (the epilogue released db)
+        if (sfb_gi != gi) tmem_cp_32x128b_warpx4(sfb, sfb_desc);
         const uint64_t a_desc = a_desc_base + (uint64_t)((s * kMxKeyTileBytes) >> 4);
         mma_mxf4_ss(d_tmem, a_desc, b_desc, idesc0, sfa, sfb, 0u);
         mma_mxf4_ss(d_tmem, a_desc + 2, b_desc + 2, idesc1, sfa, sfb, 1u);   // + 32 bytes of K
@@ -480,6 +487,7 @@ __device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int
         mma_commit(&d_full[db]);
       }
       __syncwarp();
+      sfb_gi = gi;
       issued_in_group = true;
     }
     --left;

@@ -12,6 +12,7 @@ from __future__ import annotations
 from .inputs import IDX_DIM, IDX_HEADS, LAT_DIM, V_DIM, Workload
 
 KEY_BYTES = IDX_DIM + 4          # 132 B per token per layer
+MXFP4_KEY_BYTES = IDX_DIM // 2 + IDX_DIM // 32   # 68 B: E2M1 codes + one E8M0 scale per 32 dims
 LATENT_BYTES = LAT_DIM           # 576 B per token per layer (FP8)
 
 
@@ -28,6 +29,12 @@ def dsa_bytes(ctx: int, k: int = 2048) -> int:
 def scan_bytes(wl: Workload) -> int:
     """Index keys of every request's context (read once for all its rows)."""
     return int(sum(wl.ctx) * KEY_BYTES)
+
+
+def scan_bytes_mxfp4(wl: Workload) -> int:
+    """MXFP4 index keys of every request's context, the MXFP4 query (codes and
+    scales) and the head weights."""
+    return int(sum(wl.ctx) * MXFP4_KEY_BYTES + wl.R * IDX_HEADS * (MXFP4_KEY_BYTES + 4))
 
 
 def gather_bytes(wl: Workload) -> int:

@@ -20,6 +20,8 @@ def assert_scores_close(gpu, ora, row_len):
             continue
         g = np.asarray(gpu[r, :L], np.float64)
         o = np.asarray(ora[r, :L], np.float64)
+        assert np.isfinite(g).all(), f"row {r}: {np.count_nonzero(~np.isfinite(g))} non-finite scores"
+        assert np.isfinite(o).all(), f"row {r}: the oracle left scores unwritten"
         floor = 1e-3 * np.abs(o).max()
         tol = SCORE_RTOL * np.maximum(np.abs(o), floor)
         bad = np.abs(g - o) > tol
