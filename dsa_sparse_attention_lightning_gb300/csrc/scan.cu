@@ -39,6 +39,17 @@
 //    lane quarter w % 4, i.e. 32 tokens, of two of the group's rows).  A key
 //    stage is released by the MMA's completion alone; the key scales live in
 //    their own ring, held until the epilogue has used them.
+//
+// MXFP4 keys (scan_kernel<true>; vLLM Day-0 post, "Hybrid KV cache without
+// padding" and "Native MXFP4 indexer": 68-byte keys, FP4 products with FP32
+// accumulation): 64 bytes of E2M1 codes per token and one E8M0 scale per 32
+// dims, the query in the same format.  The contraction is two block-scaled
+// MMAs (kind::mxf4, K = 64) per tile with the scale factors in tensor memory,
+// so there is no per-token scale in the epilogue:
+//   score[r][s] = sum_h w[r][h] * ReLU(sum_b 2^(eq[r][h][b] + ek[s][b]) *
+//                 (q4[r][h][b] . k4[s][b]))          (b = 32-dim block)
+// The scale factors take tensor-memory columns, so this instance runs two
+// accumulators instead of four.
 #include <limits.h>
 #include <math.h>
 
@@ -422,7 +433,9 @@ __device__ __forceinline__ TilePages tile_pages(const TileCursor& c, const int32
 // scale-factor rows -- row l = the four scale bytes of tokens l, l + 32,
 // l + 64, l + 96 -- and lane 0 copies them and the group's query scale rows
 // into tensor memory, then issues the two K = 64 block-scaled MMAs (scale
-// bytes 0-1, then 2-3).  The copies and MMAs of one thread run in issue
+// bytes 0-1, then 2-3).  The MMA takes the scales of operand row m (a token,
+// or a (row, head) column) from lane m % 32, column base + m / 32, which is
+// where the replicated 32-row copy puts them.  The copies and MMAs of one thread run in issue
 // order; the scale columns of accumulator db are rewritten only after the
 // epilogue has released db, i.e. after the MMAs that read them completed.
 __device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int ntiles,
