@@ -745,3 +745,6 @@ def test_mx_byte_model_matches_pages(oracle_mod):
         "mxfp4_index_cache_saving"]
     assert 24 * (g["nvfp4_latent_bytes_per_token"] + MX_PAGE_BYTES // PAGE) == g[
         "kv_per_token_24_layers_k31_nvfp4_mxfp4"]
+    assert traffic.MXFP4_KEY_BYTES == g["mxfp4_index_key_bytes_per_token"]
+    wl = inputs.config(1)
+    assert traffic.scan_bytes_mxfp4(wl) == sum(wl.ctx) * 68 + wl.R * NH * (68 + 4)
