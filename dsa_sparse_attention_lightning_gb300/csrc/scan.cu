@@ -101,6 +101,7 @@ constexpr int kNumBars = 2 * kStages + 2 * kScRing + 2 * kDBufs + 2 * kQBufs + k
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffTmem + 16;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
+static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 
 // MXFP4 keys (68 bytes per token: 64 bytes of E2M1 codes, then one E8M0 scale
 // per 32 dims).  Page: 64 x 64 code bytes, then 64 x 4 scale bytes.  The same
