@@ -21,9 +21,13 @@
  *   - oracle_write_kv          the Write step: LayerNorm of a new token's index
  *                              key, FP8 quantization with one scale, paged
  *                              write; the latent row's FP8 write
- *   - oracle_e2m1_decode, oracle_e8m0_decode, oracle_mx_quantize_key,
- *     oracle_indexer_scores_mx  MXFP4 index keys (68 bytes per token) and the
+ *   - oracle_e2m1_decode, oracle_e2m1_encode, oracle_e8m0_decode,
+ *     oracle_mx_quantize, oracle_write_key_mx, oracle_indexer_scores_mx
+ *                              MXFP4 index keys (68 bytes per token) and the
  *                              indexer over them
+ *   - oracle_nvfp4_latent_decode, oracle_nvfp4_latent_encode,
+ *     oracle_sparse_mla_nvfp4  NVFP4 latent rows (352 bytes per token) and
+ *                              sparse MLA over them
  *
  * Sources (web pages on Kimi K3.1 Pro's sparse attention):
  *   [TS]   TokenSpeed post on Kimi K3.1 Pro (lightseek.org), sections
@@ -725,6 +729,149 @@ int oracle_sparse_mla(const uint16_t* q, int H, double softmax_scale, const uint
             if (lse) lse[(size_t)r * H + h] = m + log(Z);
             free(x);
         }
+    }
+    return ORA_OK;
+}
+
+/*
+ * ---- NVFP4 latent ----
+ * [VLLM] "Hybrid KV cache without padding": the MLA latent takes 352 bytes
+ * per token in NVFP4 against 576 in FP8; "What Kimi K3.1 Pro changes":
+ * FlashInfer's kernels serve an NVFP4 latent.  The pages give the size only.
+ * NVFP4 (NVIDIA's 4-bit format): E2M1 elements, one unsigned E4M3 scale per
+ * 16 elements, and a per-tensor fp32 scale (here the cache's latent_scale).
+ * The 352 bytes are read as the 512 compressed-KV dims in NVFP4 (256 code
+ * bytes + 32 scale bytes) and the 64 RoPE dims in E4M3 (64 bytes):
+ *   row = [codes: 256 B, dim 2j in the low nibble of byte j]
+ *         [block scales: 32 B, byte b scales dims 16b .. 16b + 15]
+ *         [RoPE: 64 E4M3 bytes, dims 512 .. 575]
+ */
+#define ORA_NV_BLOCK 16
+#define ORA_NV_ROW_BYTES (ORA_V_DIM / 2 + ORA_V_DIM / ORA_NV_BLOCK + (ORA_LAT_DIM - ORA_V_DIM))
+
+/*
+ * Decodes one NVFP4 latent row into its 576 real values:
+ *   L[d]        = e2m1(code d) * e4m3(scale[d / 16]) * latent_scale   (d < 512)
+ *   L[512 + j]  = e4m3(rope[j]) * latent_scale                          (j < 64)
+ * The scale byte is an unsigned E4M3 (its top bit is ignored).
+ * Pinned by: rows on the shared grid equal the FP8 row's decode exactly (the
+ * NVFP4 MLA then equals the pinned FP8 MLA), and the last dims of each part.
+ */
+void oracle_nvfp4_latent_decode(const uint8_t* row, double latent_scale, double* L) {
+    const uint8_t* codes = row;
+    const uint8_t* scales = row + ORA_V_DIM / 2;
+    const uint8_t* rope = scales + ORA_V_DIM / ORA_NV_BLOCK;
+    for (int d = 0; d < ORA_V_DIM; ++d) {
+        const uint8_t nib = (d % 2 == 0) ? (codes[d / 2] & 0xF) : (codes[d / 2] >> 4);
+        L[d] = oracle_e2m1_decode(nib) * oracle_e4m3_decode(scales[d / ORA_NV_BLOCK] & 0x7F) *
+               latent_scale;
+    }
+    for (int j = 0; j < ORA_LAT_DIM - ORA_V_DIM; ++j)
+        L[ORA_V_DIM + j] = oracle_e4m3_decode(rope[j]) * latent_scale;
+}
+
+/*
+ * NVFP4 quantization of one latent row (576 values already divided by the
+ * per-tensor scale): per block of 16 of the first 512 dims
+ *   s      = e4m3_encode(max |v| / 6)     (the block maximum onto E2M1's 6)
+ *   codes  = e2m1_encode(v / dec(s))       (all zero when dec(s) is 0)
+ * and the 64 RoPE dims as e4m3_encode(v).  Writes ORA_NV_ROW_BYTES bytes.
+ * Pinned by: exactness on the shared grid, the block error bound.
+ */
+void oracle_nvfp4_latent_encode(const double* v, uint8_t* row) {
+    uint8_t* codes = row;
+    uint8_t* scales = row + ORA_V_DIM / 2;
+    uint8_t* rope = scales + ORA_V_DIM / ORA_NV_BLOCK;
+    memset(codes, 0, ORA_V_DIM / 2);
+    for (int b = 0; b < ORA_V_DIM / ORA_NV_BLOCK; ++b) {
+        double amax = 0.0;
+        for (int i = 0; i < ORA_NV_BLOCK; ++i) {
+            const double a = fabs(v[b * ORA_NV_BLOCK + i]);
+            if (a > amax) amax = a;
+        }
+        scales[b] = oracle_e4m3_encode(amax / 6.0);
+        const double s = oracle_e4m3_decode(scales[b]);
+        for (int i = 0; i < ORA_NV_BLOCK; ++i) {
+            const int d = b * ORA_NV_BLOCK + i;
+            const uint8_t c = s > 0.0 ? oracle_e2m1_encode(v[d] / s) : 0;
+            codes[d / 2] |= (uint8_t)(d % 2 == 0 ? c : c << 4);
+        }
+    }
+    for (int j = 0; j < ORA_LAT_DIM - ORA_V_DIM; ++j) rope[j] = oracle_e4m3_encode(v[ORA_V_DIM + j]);
+}
+
+/*
+ * Sparse MLA over NVFP4 latent rows: the attention of oracle_sparse_mla with
+ * each selected row decoded by oracle_nvfp4_latent_decode.  Latent page
+ * layout: [page][64 tokens][352 bytes].
+ * Pinned by: equality with oracle_sparse_mla on rows both formats represent
+ * exactly, the dense case against float64 scaled_dot_product_attention.
+ */
+int oracle_sparse_mla_nvfp4(const uint16_t* q, int H, double softmax_scale,
+                            const uint8_t* latent_cache, int64_t num_pages, double latent_scale,
+                            const int32_t* block_table, int B, int max_pages,
+                            const int32_t* row_req, const int32_t* row_len, const int32_t* idx,
+                            int k, int R, double* out, double* lse) {
+    if (H <= 0 || k < 0) return ORA_BAD_ARG;
+    for (int r = 0; r < R; ++r) {
+        if (row_req[r] < 0 || row_req[r] >= B) return ORA_BAD_ARG;
+        if (row_len[r] < 0 || (int64_t)row_len[r] > (int64_t)max_pages * ORA_PAGE)
+            return ORA_BAD_ARG;
+        for (int j = 0; j < k; ++j) {
+            int32_t t = idx[(size_t)r * k + j];
+            if (t >= row_len[r]) return ORA_BAD_INDEX;
+            if (t >= 0) {
+                int64_t page = block_table[(size_t)row_req[r] * max_pages + t / ORA_PAGE];
+                if (page < 0 || page >= num_pages) return ORA_BAD_PAGE;
+            }
+        }
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < R; ++r) {
+        const int b = row_req[r];
+        /* the selected rows of this query row, decoded once for all heads */
+        double* L = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1) * ORA_LAT_DIM);
+        double* x = (double*)malloc(sizeof(double) * (size_t)(k > 0 ? k : 1));
+        for (int j = 0; j < k; ++j) {
+            int32_t t = idx[(size_t)r * k + j];
+            if (t < 0) continue;
+            int64_t page = block_table[(size_t)b * max_pages + t / ORA_PAGE];
+            oracle_nvfp4_latent_decode(
+                latent_cache + ((size_t)page * ORA_PAGE + (size_t)(t % ORA_PAGE)) * ORA_NV_ROW_BYTES,
+                latent_scale, L + (size_t)j * ORA_LAT_DIM);
+        }
+        for (int h = 0; h < H; ++h) {
+            double qh[ORA_LAT_DIM];
+            for (int d = 0; d < ORA_LAT_DIM; ++d)
+                qh[d] = bf16_to_double(q[((size_t)r * H + h) * ORA_LAT_DIM + d]);
+            double m = -INFINITY;
+            int any = 0;
+            for (int j = 0; j < k; ++j) {
+                if (idx[(size_t)r * k + j] < 0) continue;
+                double s = 0.0;
+                for (int d = 0; d < ORA_LAT_DIM; ++d) s += qh[d] * L[(size_t)j * ORA_LAT_DIM + d];
+                x[j] = softmax_scale * s;
+                if (x[j] > m) m = x[j];
+                any = 1;
+            }
+            double* o = out + ((size_t)r * H + h) * ORA_V_DIM;
+            for (int d = 0; d < ORA_V_DIM; ++d) o[d] = 0.0;
+            if (!any) {
+                if (lse) lse[(size_t)r * H + h] = -INFINITY;
+                continue;
+            }
+            double Z = 0.0;
+            for (int j = 0; j < k; ++j) {
+                if (idx[(size_t)r * k + j] < 0) continue;
+                const double pj = exp(x[j] - m);
+                Z += pj;
+                for (int d = 0; d < ORA_V_DIM; ++d) o[d] += pj * L[(size_t)j * ORA_LAT_DIM + d];
+            }
+            for (int d = 0; d < ORA_V_DIM; ++d) o[d] /= Z;
+            if (lse) lse[(size_t)r * H + h] = log(Z) + m;
+        }
+        free(L);
+        free(x);
     }
     return ORA_OK;
 }

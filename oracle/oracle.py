@@ -37,6 +37,8 @@ MX_SCALES = IDX_DIM // MX_BLOCK
 MX_KEY_PAGE_BYTES = PAGE * (MX_KEY_BYTES + MX_SCALES)
 LAT_DIM = 576
 V_DIM = 512
+NV_BLOCK = 16
+NV_ROW_BYTES = V_DIM // 2 + V_DIM // NV_BLOCK + (LAT_DIM - V_DIM)   # 352
 
 
 def build(force: bool = False) -> str:
@@ -91,6 +93,13 @@ def _load():
         lib.oracle_write_key_mx.restype = ctypes.c_int
         lib.oracle_indexer_scores_mx.argtypes = [P, P, P, P, i64, P, i32, i32, P, P, i32, P, i64]
         lib.oracle_indexer_scores_mx.restype = ctypes.c_int
+        lib.oracle_nvfp4_latent_decode.argtypes = [P, dbl, P]
+        lib.oracle_nvfp4_latent_decode.restype = None
+        lib.oracle_nvfp4_latent_encode.argtypes = [P, P]
+        lib.oracle_nvfp4_latent_encode.restype = None
+        lib.oracle_sparse_mla_nvfp4.argtypes = [P, i32, dbl, P, i64, dbl, P, i32, i32, P, P, P,
+                                                i32, i32, P, P]
+        lib.oracle_sparse_mla_nvfp4.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -269,6 +278,54 @@ def indexer_scores_mx(q_codes, q_scales, w, key_cache, block_table, row_req, row
     if st != 0:
         raise ValueError(f"oracle_indexer_scores_mx failed with status {st}")
     return scores
+
+
+def nvfp4_latent_encode(v):
+    """NVFP4 latent rows (uint8 [..., 352]) of float64 values [..., 576]
+    already divided by the per-tensor scale."""
+    lib = _load()
+    v = _c(v, np.float64)
+    flat = v.reshape(-1, LAT_DIM)
+    rows = np.zeros((flat.shape[0], NV_ROW_BYTES), dtype=np.uint8)
+    for i in range(flat.shape[0]):
+        lib.oracle_nvfp4_latent_encode(_ptr(flat[i]), _ptr(rows[i]))
+    return rows.reshape(v.shape[:-1] + (NV_ROW_BYTES,))
+
+
+def nvfp4_latent_decode(rows, latent_scale):
+    """float64 [..., 576] values of NVFP4 latent rows uint8 [..., 352]."""
+    lib = _load()
+    rows = _c(rows, np.uint8)
+    flat = rows.reshape(-1, NV_ROW_BYTES)
+    out = np.zeros((flat.shape[0], LAT_DIM))
+    for i in range(flat.shape[0]):
+        lib.oracle_nvfp4_latent_decode(_ptr(flat[i]), float(latent_scale), _ptr(out[i]))
+    return out.reshape(rows.shape[:-1] + (LAT_DIM,))
+
+
+def sparse_mla_nvfp4(q, softmax_scale, latent_cache, latent_scale, block_table, row_req,
+                     row_len, idx):
+    """(out float64 [R,H,512], lse float64 [R,H]) over NVFP4 latent pages
+    (uint8 [pages][64][352])."""
+    lib = _load()
+    q = _c(q, np.uint16)
+    R, H, _ = q.shape
+    idx = _c(idx, np.int32)
+    k = idx.shape[1]
+    latent_cache = _c(latent_cache, np.uint8)
+    num_pages = latent_cache.size // (PAGE * NV_ROW_BYTES)
+    block_table = _c(block_table, np.int32)
+    B, max_pages = block_table.shape
+    out = np.zeros((R, H, V_DIM))
+    lse = np.zeros((R, H))
+    st = lib.oracle_sparse_mla_nvfp4(_ptr(q), H, float(softmax_scale), _ptr(latent_cache),
+                                     num_pages, float(latent_scale), _ptr(block_table), B,
+                                     max_pages, _ptr(_c(row_req, np.int32)),
+                                     _ptr(_c(row_len, np.int32)), _ptr(idx), k, R, _ptr(out),
+                                     _ptr(lse))
+    if st != 0:
+        raise ValueError(f"oracle_sparse_mla_nvfp4 failed with status {st}")
+    return out, lse
 
 
 def topk_dcp(scores, row_len, k, W):

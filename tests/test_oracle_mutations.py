@@ -50,6 +50,13 @@ MUTATIONS = [
     ("mx_key_scales_next_slot", "(size_t)slot * ORA_MX_SCALES);",
      "(size_t)((slot + 1) % ORA_PAGE) * ORA_MX_SCALES);"),
     ("mx_relu_dropped", "(qk > 0.0 ? qk : 0.0)", "qk"),
+    ("nvfp4_scale_per_32", "scales[d / ORA_NV_BLOCK] & 0x7F", "scales[d / (2 * ORA_NV_BLOCK)] & 0x7F"),
+    ("nvfp4_rope_unscaled", "L[ORA_V_DIM + j] = oracle_e4m3_decode(rope[j]) * latent_scale;",
+     "L[ORA_V_DIM + j] = oracle_e4m3_decode(rope[j]);"),
+    ("nvfp4_value_from_wrong_dims", "o[d] += pj * L[(size_t)j * ORA_LAT_DIM + d];",
+     "o[d] += pj * L[(size_t)j * ORA_LAT_DIM + d + 64];"),
+    ("nvfp4_scale_from_block_max", "scales[b] = oracle_e4m3_encode(amax / 6.0);",
+     "scales[b] = oracle_e4m3_encode(amax / 4.0);"),
 ]
 
 PIN_TESTS = [
@@ -75,6 +82,9 @@ PIN_TESTS = [
     pins.test_indexer_mx_equals_fp8_scorer_on_shared_grid,
     pins.test_indexer_mx_last_dim_and_scale_slot,
     pins.test_write_key_mx_codes_and_placement,
+    pins.test_nvfp4_latent_layout_last_dims,
+    pins.test_nvfp4_encode_exact_on_shared_grid_and_error_bound,
+    pins.test_mla_nvfp4_equals_fp8_on_shared_grid,
 ]
 
 

@@ -748,3 +748,85 @@ def test_mx_byte_model_matches_pages(oracle_mod):
     assert traffic.MXFP4_KEY_BYTES == g["mxfp4_index_key_bytes_per_token"]
     wl = inputs.config(1)
     assert traffic.scan_bytes_mxfp4(wl) == sum(wl.ctx) * 68 + wl.R * NH * (68 + 4)
+
+
+# ------------------------------------------------------------ NVFP4 latent
+# Row of 352 bytes: 256 bytes of E2M1 codes of dims 0..511 (dim 2j in the low
+# nibble of byte j), 32 unsigned-E4M3 block scales (byte b: dims 16b..16b+15),
+# 64 E4M3 RoPE bytes (dims 512..575); every value times the per-tensor scale.
+NV_ROW = 352
+
+
+def test_nvfp4_latent_layout_last_dims(oracle_mod):
+    row = np.zeros(NV_ROW, np.uint8)
+    row[255] = 0x70                 # dim 510 = 0, dim 511 = E2M1 code 7 (6.0)
+    row[256 + 31] = 0x30            # block 31 scale: E4M3 0.5
+    row[256 + 32 + 63] = 0x40       # dim 575: E4M3 2.0
+    L = oracle_mod.nvfp4_latent_decode(row, 0.25)
+    want = np.zeros(LAT)
+    want[511] = 6.0 * 0.5 * 0.25
+    want[575] = 2.0 * 0.25
+    assert np.array_equal(L, want)
+    row[256 + 31] = 0xB0            # the scale is unsigned: its top bit is ignored
+    assert np.array_equal(oracle_mod.nvfp4_latent_decode(row, 0.25), want)
+    row[0] = 0x09                   # dim 0 = -0.5 (code 9), dim 1 = 0, block 0 scale still 0
+    assert np.array_equal(oracle_mod.nvfp4_latent_decode(row, 0.25), want)
+    row[256] = 0x38                 # block 0 scale 1.0
+    want[0] = -0.5 * 0.25
+    assert np.array_equal(oracle_mod.nvfp4_latent_decode(row, 0.25), want)
+
+
+def _nv_grid_rows(rng, n, lo=-3, hi=3):
+    """Latent rows every dim of which both NVFP4 and E4M3 hold exactly: per
+    16-dim block E2M1 magnitudes x sign x 2^p with one element +-6 x 2^p (so the
+    block scale is exactly 2^p), and E4M3 RoPE dims."""
+    grid = _e2m1_grid()
+    v = grid[rng.integers(0, 8, (n, 512))] * rng.choice([-1.0, 1.0], (n, 512))
+    blocks = v.reshape(n, 32, 16)
+    blocks[:, :, 0] = 6.0 * rng.choice([-1.0, 1.0], (n, 32))
+    blocks *= np.ldexp(1.0, rng.integers(lo, hi + 1, (n, 32, 1)))
+    rope = _e4m3_vals(_e4m3(rng.standard_normal((n, 64)) * 4))
+    return np.concatenate([blocks.reshape(n, 512), rope], axis=1)
+
+
+def test_nvfp4_encode_exact_on_shared_grid_and_error_bound(oracle_mod):
+    rng = np.random.default_rng(50)
+    v = _nv_grid_rows(rng, 20, lo=-6, hi=4)
+    assert np.array_equal(oracle_mod.nvfp4_latent_decode(oracle_mod.nvfp4_latent_encode(v), 1.0), v)
+    v = rng.standard_normal((20, LAT)) * rng.uniform(0.05, 20.0, (20, 1))
+    rows = oracle_mod.nvfp4_latent_encode(v)
+    d = oracle_mod.nvfp4_latent_decode(rows, 1.0)
+    s = _e4m3_vals(rows[:, 256:288] & 0x7F)                # block scales
+    amax = np.abs(v[:, :512]).reshape(20, 32, 16).max(-1)
+    # E2M1 half-spacing is at most 1 below 6; beyond 6 * s the clamp loses amax - 6 s
+    bound = s + np.maximum(0.0, amax - 6 * s)
+    err = np.abs(d[:, :512] - v[:, :512]).reshape(20, 32, 16).max(-1)
+    assert (err <= bound * (1 + 1e-12)).all()
+    assert np.array_equal(d[:, 512:], _e4m3_vals(_e4m3(v[:, 512:])))
+
+
+def test_mla_nvfp4_equals_fp8_on_shared_grid(oracle_mod):
+    """Latent rows on the shared grid: NVFP4 and FP8 caches hold the same
+    values, so the NVFP4 attention must equal the pinned FP8 attention."""
+    rng = np.random.default_rng(51)
+    n, H, k, ls = 150, 8, 96, 0.125
+    vals = _nv_grid_rows(rng, n)
+    fp8, bt = _latent_cache(_e4m3(vals))
+    assert np.array_equal(_e4m3_vals(_e4m3(vals)), vals)
+    nv = np.zeros((fp8.shape[0], PAGE, NV_ROW), np.uint8)
+    rows = oracle_mod.nvfp4_latent_encode(vals)
+    for t in range(n):
+        nv[t // PAGE, t % PAGE] = rows[t]
+    q = _bf16_bits(rng.standard_normal((2, H, LAT)) * 0.05)
+    idx = np.full((2, k), -1, np.int32)
+    idx[0, :90] = rng.choice(n, 90, replace=False)
+    idx[1, :k] = rng.choice(120, k, replace=False)
+    args = (ls, bt, [0, 0], [n, 120], idx)
+    o8, l8 = oracle_mod.sparse_mla(q, 1 / math.sqrt(192), fp8, *args)
+    o4, l4 = oracle_mod.sparse_mla_nvfp4(q, 1 / math.sqrt(192), nv, *args)
+    assert np.allclose(o4, o8, rtol=1e-13, atol=1e-15) and np.allclose(l4, l8, rtol=1e-14)
+
+
+def test_nvfp4_byte_model(oracle_mod):
+    g = {k: float(v[0]) for k, v in _read_golden("byte_model.txt").items()}
+    assert oracle_mod.NV_ROW_BYTES == NV_ROW == g["nvfp4_latent_bytes_per_token"]
