@@ -43,6 +43,11 @@
  *  - key_cache    uint8 [num_pages][8448]: 64 x 128 E4M3 key bytes (token
  *                 major), then 64 fp32 key scales (little endian).  132 B per
  *                 token: 128 FP8 values and one four-byte scale.
+ *  - key_cache (MXFP4 index keys, dsa_indexer_score_mxfp4 and
+ *                 dsa_write_kv_mxfp4) uint8 [num_pages][4352]: 64 x 64 bytes of
+ *                 E2M1 codes (dim 2j in the low nibble of byte j), then 64 x 4
+ *                 E8M0 block scales (byte b scales dims 32b .. 32b + 31).
+ *                 68 B per token.
  *  - latent_cache uint8 [num_pages][64][576]: E4M3 latent rows; one fp32
  *                 scale `latent_scale` for the whole cache.
  *  - block_table  int32 [B][max_pages], row-major.
