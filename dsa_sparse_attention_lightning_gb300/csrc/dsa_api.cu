@@ -45,15 +45,17 @@ cudaError_t encode_tensor_map_u8(CUtensorMap* map, int rank, const void* base, c
 
 using namespace dsa;
 
+namespace dsa {
+
 namespace {
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+}  // namespace
 
-constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
-
-inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
-
-inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
-
-inline int64_t score_ld(int max_pages) { return (int64_t)max_pages * kPage; }
+int to_status(cudaError_t e) {
+  if (e == cudaSuccess) return DSA_OK;
+  t_last_cuda_error = e;
+  return DSA_ERR_CUDA;
+}
 
 int check_rows(int B, int max_pages, const int32_t* block_table, const int32_t* row_req,
                const int32_t* row_len, int R) {
@@ -63,22 +65,37 @@ int check_rows(int B, int max_pages, const int32_t* block_table, const int32_t* 
   return DSA_OK;
 }
 
+int check_score_args(const void* q_idx, int q_dtype, const float* q_scale, const float* w,
+                     const uint8_t* key_cache, int64_t num_pages, const int32_t* block_table,
+                     int B, int max_pages, const int32_t* row_req, const int32_t* row_len, int R,
+                     const float* scores, int64_t ld) {
+  int s = check_rows(B, max_pages, block_table, row_req, row_len, R);
+  if (s) return s;
+  if (q_dtype != DSA_BF16 && q_dtype != DSA_E4M3) return DSA_ERR_UNSUPPORTED;
+  if (R > 0 && (!q_idx || !w || !key_cache || !scores)) return DSA_ERR_INVALID_ARG;
+  if (q_dtype == DSA_E4M3 && R > 0 && !q_scale) return DSA_ERR_INVALID_ARG;
+  if (num_pages < 0 || ld < score_ld(max_pages) || ld % 4 != 0) return DSA_ERR_INVALID_ARG;
+  if (scores && !is_aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
+  if (key_cache && !is_aligned(key_cache, 16)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+}  // namespace dsa
+
+namespace {
+
+constexpr int kVersion = 1 * 10000 + 1 * 100 + 0;
+
+inline bool aligned(const void* p, size_t a) { return is_aligned(p, a); }
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
 int check_workspace(void* ws, size_t have, size_t need) {
   if (!ws || have < need || !aligned(ws, kAlign)) return DSA_ERR_WORKSPACE;
   return DSA_OK;
 }
 
-int to_status(cudaError_t e);
-
 int clear_status(void* ws, cudaStream_t st) { return to_status(cudaMemsetAsync(ws, 0, 4, st)); }
-
-thread_local cudaError_t t_last_cuda_error = cudaSuccess;
-
-int to_status(cudaError_t e) {
-  if (e == cudaSuccess) return DSA_OK;
-  t_last_cuda_error = e;
-  return DSA_ERR_CUDA;
-}
 
 bool supported_heads(int H) { return H == 16 || H == 32 || H == 64 || H == 128; }
 
@@ -135,14 +152,9 @@ int dsa_indexer_score(const void* q_idx, int q_dtype, const float* q_scale, cons
                       int B, int max_pages, const int32_t* row_req, const int32_t* row_len,
                       int R, float* scores, int64_t ld, void* workspace, size_t ws_bytes,
                       void* stream) {
-  int s = check_rows(B, max_pages, block_table, row_req, row_len, R);
+  int s = check_score_args(q_idx, q_dtype, q_scale, w, key_cache, num_pages, block_table, B,
+                           max_pages, row_req, row_len, R, scores, ld);
   if (s) return s;
-  if (q_dtype != DSA_BF16 && q_dtype != DSA_E4M3) return DSA_ERR_UNSUPPORTED;
-  if (R > 0 && (!q_idx || !w || !key_cache || !scores)) return DSA_ERR_INVALID_ARG;
-  if (q_dtype == DSA_E4M3 && R > 0 && !q_scale) return DSA_ERR_INVALID_ARG;
-  if (num_pages < 0 || ld < score_ld(max_pages) || ld % 4 != 0) return DSA_ERR_INVALID_ARG;
-  if (scores && !aligned(scores, 16)) return DSA_ERR_INVALID_ARG;
-  if (key_cache && !aligned(key_cache, 16)) return DSA_ERR_INVALID_ARG;
   s = check_workspace(workspace, ws_bytes, dsa_indexer_score_workspace_size(R));
   if (s) return s;
   cudaStream_t st = as_stream(stream);

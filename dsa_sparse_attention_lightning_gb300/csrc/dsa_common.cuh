@@ -245,6 +245,25 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t st);
 cudaError_t launch_selftest_wait(void* workspace, long long limit_cycles, cudaStream_t st);
 size_t selftest_workspace_bytes();
 
+// ---- host-side argument checks and status codes (dsa_api.cu) ---------------
+inline bool is_aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+inline int64_t score_ld(int max_pages) { return (int64_t)max_pages * kPage; }
+
+// DSA_OK for cudaSuccess; otherwise DSA_ERR_CUDA, after recording the error as
+// the calling host thread's dsa_last_cuda_error.
+int to_status(cudaError_t e);
+
+// Row and block-table arguments shared by every call that reads the caches.
+int check_rows(int B, int max_pages, const int32_t* block_table, const int32_t* row_req,
+               const int32_t* row_len, int R);
+
+// Every argument check of the FP8 indexer scan (dsa_indexer_score and its
+// workspace-free form), workspace aside.
+int check_score_args(const void* q_idx, int q_dtype, const float* q_scale, const float* w,
+                     const uint8_t* key_cache, int64_t num_pages, const int32_t* block_table,
+                     int B, int max_pages, const int32_t* row_req, const int32_t* row_len, int R,
+                     const float* scores, int64_t ld);
+
 // Tiled TMA descriptor over a byte tensor of the given rank: dims[0] is the
 // contiguous extent, strides[i] the byte stride of dim i + 1, box the tile
 // copied per load; 128-byte swizzle, out-of-range elements read as zero.

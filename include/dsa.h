@@ -172,12 +172,16 @@ int dsa_indexer_score_mxfp4(const uint8_t* q_codes, const uint8_t* q_scales, con
  * Same arguments and results as dsa_indexer_score, minus the workspace; the
  * scratch is a fixed array inside the library (1 MiB per GPU, held until the
  * process exits), so R <= DSA_NOALLOC_MAX_ROWS (else DSA_ERR_UNSUPPORTED).
- *  dev_status optional device pointer to one uint32 that receives the
- *             DSA_DEV_* bits of this call (cleared first); NULL to ignore them.
+ *  dev_status optional device pointer to one uint32 (4-byte aligned, else
+ *             DSA_ERR_INVALID_ARG) that receives the DSA_DEV_* bits of this
+ *             call (cleared first); NULL to keep them in the array.
  * All calls on one GPU share the array: calls that may overlap on the GPU
- * race and must be ordered by the caller (one stream, or events).  The first
- * call on a device looks up the array's device address with that device
- * current; make it before any stream capture.  Nothing is allocated.
+ * race and must be ordered by the caller (one stream, or events).  A call
+ * made outside a stream capture looks up the array's device address with the
+ * calling device current (so a call after cudaDeviceReset finds the array's
+ * new address); a call made during a capture reuses the address found by the
+ * last call outside one, so make one call on the device before capturing.
+ * Nothing is allocated.
  * ---------------------------------------------------------------------- */
 #define DSA_NOALLOC_MAX_ROWS 64
 int dsa_indexer_score_noalloc(const void* q_idx, int q_dtype, const float* q_scale,

@@ -148,6 +148,17 @@ def test_indexer_score_mxfp4_rejects_bad_arguments(lib):
     assert call(work=None) == 3 and call(ws_bytes=ws - 1) == 3
 
 
+def test_indexer_score_noalloc_rejects_bad_arguments(lib):
+    call = lambda R=2, qt=0, st=None, ld=256, q=FAKE: lib.dsa_indexer_score_noalloc(
+        q, qt, None, FAKE, FAKE, 4, FAKE, 1, 4, FAKE, FAKE, R, FAKE, ld, st, None)
+    assert call(R=65) == 2                               # more rows than the fixed scratch holds
+    assert call(st=ctypes.c_void_p((1 << 20) + 2)) == 1  # status word not 4-byte aligned
+    assert call(qt=1) == 1                               # E4M3 query without its scales
+    assert call(qt=5) == 2
+    assert call(ld=255) == 1 and call(ld=128) == 1
+    assert call(q=None) == 1
+
+
 def test_selftest_rejects_bad_arguments(lib):
     need = lib.dsa_selftest_workspace_size()
     assert need >= 768
