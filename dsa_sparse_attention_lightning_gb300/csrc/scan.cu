@@ -48,7 +48,7 @@
 // so there is no per-token scale in the epilogue:
 //   score[r][s] = sum_h w[r][h] * ReLU(sum_b 2^(eq[r][h][b] + ek[s][b]) *
 //                 (q4[r][h][b] . k4[s][b]))          (b = 32-dim block)
-// The scale factors take tensor-memory columns, so this instance runs two
+// The scale factors take tensor-memory columns, so this instance runs three
 // accumulators instead of four.
 #include <limits.h>
 #include <math.h>
@@ -97,7 +97,8 @@ constexpr int kOffW = (kOffPv + kScRing * 4 + 15) / 16 * 16;       // [kEpiWarps
 constexpr int kOffBar = (kOffW + kEpiWarps * kEpiRows * kIdxHeads * 4 + 7) / 8 * 8;
 static_assert(kOffKeys % 1024 == 0 && kKeyTileBytes % 1024 == 0, "swizzled TMA tiles need 1024-byte alignment");
 static_assert(kOffScale % 16 == 0 && kOffW % 16 == 0 && kOffBar % 8 == 0, "vector and mbarrier alignment");
-constexpr int kNumBars = 2 * kStages + 2 * kScRing + 2 * kDBufs + 2 * kQBufs + kMmaWarps;
+constexpr int kDBars = 6;                                // accumulator barriers (MXFP4: tile mod 6)
+constexpr int kNumBars = 2 * kStages + 2 * kScRing + 2 * kDBars + 2 * kQBufs + kMmaWarps;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffTmem + 16;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
@@ -113,13 +114,18 @@ constexpr int kMxKeyTileBytes = kTileTok * kMxKeyBytes;             // 8192
 constexpr int kMxQAtom = kMaxGroupRows * kIdxHeads * kMxKeyBytes;   // 128 rows x 64 B
 constexpr int kSfRowBytes = 32 * 16;                                // 32 rows x 16 B
 constexpr int kOffSfaMx = kOffKeys + kStages * kMxKeyTileBytes;     // [kScRing] key scale rows
-constexpr int kMxDBufs = 2;                                         // accumulators (TMEM holds the scales too)
+constexpr int kMxDBufs = 3;                                         // accumulators (TMEM holds the scales too)
 constexpr uint32_t kSfCol0 = kDCols * kMxDBufs;                     // scale columns: 8 per accumulator
 static_assert(kOffSfaMx + kScRing * kSfRowBytes <= kOffScale, "scale rows fit the key region");
 static_assert(kMxQAtom + kSfRowBytes <= kQBytes, "query codes and scale rows fit the query buffer");
 static_assert(kSfCol0 + 8 * kMxDBufs <= kTmemCols, "scale columns fit the allocation");
-static_assert(kMxDBufs == kEpiGroups && kMxDBufs == kMmaWarps,
-              "accumulator db belongs to MMA warp db and epilogue group db");
+// Three accumulators, tile i in accumulator i % 3, signalled on barrier pair
+// i % 6: each barrier is waited on by one epilogue group (i % 2) in tile
+// order, and the MMA warp of tile i (i % 2) waits for tile i - 3's release on
+// a barrier whose previous phase (tile i - 9) it already waited for at tile
+// i - 6, so no parity wait can be satisfied by an older phase.
+static_assert(kDBars % kMxDBufs == 0 && kDBars % kEpiGroups == 0 && kDBars % kMmaWarps == 0 &&
+              kDBars >= kDBufs, "accumulator barrier indexing");
 
 // group = {first row, rows, request, max row length}
 struct ScanWs {
@@ -447,8 +453,8 @@ __device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int
   uint64_t* sc_full = bars + 2 * kStages;
   uint64_t* sc_empty = sc_full + kScRing;
   uint64_t* d_full = sc_empty + kScRing;
-  uint64_t* d_empty = d_full + kDBufs;
-  uint64_t* q_full = d_empty + kDBufs;
+  uint64_t* d_empty = d_full + kDBars;
+  uint64_t* q_full = d_empty + kDBars;
   uint64_t* q_empty = q_full + kQBufs;
   uint64_t* mma_done = q_empty + kQBufs;
   const int m = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -460,7 +466,6 @@ __device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int
   const uint64_t sfb_desc = desc_sf_rows16(smem_u32(smem + kOffQ + kMxQAtom));
   int s = 0;
   uint32_t s_phase = 0;
-  int sfb_gi = -1;                                    // group whose query scales are in TMEM
   for (int i = 0; i < ntiles; ++i) {
     if (cur.g != cur_group) {
       cur_group = cur.g;
@@ -472,7 +477,7 @@ __device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int
       if (!warp_wait(&q_full[gi % kQBufs], (uint32_t)(gi / kQBufs) & 1, status)) break;
     }
     if (i % kMmaWarps == m) {
-      const int db = i % kMxDBufs, x = i % kScRing;
+      const int db = i % kMxDBufs, x = i % kScRing, c = i % kDBars;
       // the scale rows are built before the accumulator wait, off the path
       // from the previous epilogue to this tile's MMAs
       if (!warp_wait(&sc_full[x], (uint32_t)(i / kScRing) & 1, status)) break;
@@ -483,25 +488,24 @@ __device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int
       fence_proxy_async_smem();                       // visible to the tensor core's copy
       __syncwarp();
       if (!warp_wait(&full[s], s_phase, status)) break;
-      if (!warp_wait(&d_empty[db], ((uint32_t)(i / kMxDBufs) & 1) ^ 1, status)) break;
+      // the previous user of accumulator db is tile i - 3 (barrier (i + 3) % 6)
+      if (!warp_wait(&d_empty[(i + kMxDBufs) % kDBars],
+                     ((uint32_t)((i + kMxDBufs) / kDBars) & 1) ^ 1, status))
+        break;
       if (lane == 0) {
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(db * kDCols);
         const uint32_t sfa = tmem_base + kSfCol0 + (uint32_t)(db * 8), sfb = sfa + 4;
         tmem_cp_32x128b_warpx4(sfa, desc_sf_rows16(smem_u32(sf_rows)));
-        // accumulator db (= this warp) keeps its query scale rows for the
-        // whole group; the MMAs that read the previous group's have completed
-        // (the epilogue released db)
-        if (sfb_gi != gi) tmem_cp_32x128b_warpx4(sfb, sfb_desc);
+        tmem_cp_32x128b_warpx4(sfb, sfb_desc);
         const uint64_t a_desc = a_desc_base + (uint64_t)((s * kMxKeyTileBytes) >> 4);
         mma_mxf4_ss(d_tmem, a_desc, b_desc, idesc0, sfa, sfb, 0u);
         mma_mxf4_ss(d_tmem, a_desc + 2, b_desc + 2, idesc1, sfa, sfb, 1u);   // + 32 bytes of K
         mma_commit(&empty[s]);
         mma_commit(&sc_empty[x]);
-        mma_commit(&d_full[db]);
+        mma_commit(&d_full[c]);
       }
       __syncwarp();
-      sfb_gi = gi;
       issued_in_group = true;
     }
     --left;
@@ -537,9 +541,9 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
   uint64_t* empty = bars + kStages;                 // [kStages] MMA done with a key stage
   uint64_t* sc_full = bars + 2 * kStages;           // [kScRing] scales landed
   uint64_t* sc_empty = sc_full + kScRing;           // [kScRing] epilogue done with them
-  uint64_t* d_full = sc_empty + kScRing;            // [kDBufs]
-  uint64_t* d_empty = d_full + kDBufs;              // [kDBufs]
-  uint64_t* q_full = d_empty + kDBufs;              // [kQBufs]
+  uint64_t* d_full = sc_empty + kScRing;            // [kDBars]
+  uint64_t* d_empty = d_full + kDBars;              // [kDBars]
+  uint64_t* q_full = d_empty + kDBars;              // [kQBufs]
   uint64_t* q_empty = q_full + kQBufs;              // [kQBufs]
   uint64_t* mma_done = q_empty + kQBufs;            // [kMmaWarps] every MMA of an issuer finished
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffTmem);
@@ -556,7 +560,7 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
       mbar_init(&sc_full[x], 1);
       mbar_init(&sc_empty[x], kEpiWarpsPerGroup + (kMx ? 1 : 0));   // MXFP4: + the MMA commit
     }
-    for (int b = 0; b < kDBufs; ++b) {
+    for (int b = 0; b < kDBars; ++b) {
       mbar_init(&d_full[b], 1);
       mbar_init(&d_empty[b], kEpiWarpsPerGroup);
     }
@@ -782,6 +786,8 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
     constexpr int kDB = kMx ? kMxDBufs : kDBufs;
     for (int i = eg; i < ntiles; i += kEpiGroups) {
       const int x = i % kScRing, db = i % kDB;
+      const int c = kMx ? i % kDBars : db;              // barrier pair of tile i
+      const uint32_t par = kMx ? (uint32_t)(i / kDBars) & 1 : (uint32_t)(i / kDB) & 1;
       if (cur.g != cur_group) {                       // this warp's rows of the new group
         cur_group = cur.g;
 #pragma unroll
@@ -792,7 +798,7 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
         }
         __syncwarp();
       }
-      if (!warp_wait(&d_full[db], (uint32_t)(i / kDB) & 1, status)) break;
+      if (!warp_wait(&d_full[c], par, status)) break;
       if (!warp_wait(&sc_full[x], (uint32_t)(i / kScRing) & 1, status)) break;
       tc_fence_after();
       const bool page_valid = (pv_s[x] >> (tok_in >> 6)) & 1u;
@@ -824,7 +830,7 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&d_empty[db]);
+        mbar_arrive(&d_empty[c]);
         mbar_arrive(&sc_empty[x]);
       }
       cur.advance(kEpiGroups);
