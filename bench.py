@@ -35,6 +35,10 @@ from dsa_sparse_attention_lightning_gb300 import inputs, traffic  # noqa: E402
 
 METRIC = "DSA decode-step µs/layer and achieved HBM GB/s vs 8 TB/s roofline, 1 GB300"
 L2_FLUSH_BYTES = 256 << 20
+CLOCK_WINDOW_S = 1.0
+# Decode workloads reported beside the headline one: 32K (16 x 4 rows) and 1M
+# (one row) beside the 256K headline.
+SIDE_CONFIGS = {2: (1, 3), 1: (2, 3), 3: (1, 2)}
 # Kernels one step launches: scan 2 (query split + grouping, scan); top-k 1
 # (one CTA per row, rows of at most 49,152 scores) or 3 (sample, collect,
 # finalize); sparse MLA 3 (query split, attention, combine of cut units).
@@ -45,14 +49,14 @@ def kernels_per_step(wl) -> int:
     return 2 + (1 if wl.max_pages * inputs.PAGE <= TOPK_ROW_CAP else 3) + 3
 
 # DRAM bytes (read + write) per call of a stage, summed over its kernels, from
-# the ncu launch list in profiles/ (taken on the current kernels; cold cache,
-# so L2-resident intermediates count as DRAM reads).  Stages and workloads not
-# captured report null.
+# one ncu capture of the current kernels (cold cache, so L2-resident
+# intermediates count as DRAM reads).  Stages and workloads not captured on the
+# current kernels report null.
 NCU_STAGE_TRAFFIC = {
     ("decode_16x4_ctx32768_h64", "indexer_scan"): 70.40e6,
     ("decode_16x4_ctx32768_h64", "topk"): 8.46e6,
     ("decode_16x4_ctx32768_h64", "sparse_mla"): 104.41e6,
-    # prefill chunk: scan_kernel alone (profiles/prefill_4096rows_ctx131072_tensor.md)
+    # prefill chunk: the scan kernel alone
     ("prefill_4096rows_ctx131072_h64", "indexer_scan"): 2098.86e6,
 }
 
@@ -193,56 +197,19 @@ def whole_job_gbs(bytes_per_step: int, world: int, steps: int, max_total_ms: flo
     return bytes_per_step * world * steps / (max_total_ms * 1e-3) / 1e9
 
 
-def run_gpu(args):
-    rank, world, local = _dist()
-    import dsa_sparse_attention_lightning_gb300 as dsa
-    dsa.load()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
-    wl = rank_workload(args.config, rank)
+def _step_buffers(dsa, wl, dev):
     inp = inputs.make_inputs(wl, device=dev)
-    R, H = wl.R, wl.H
-    out = torch.empty((R, H, inputs.V_DIM), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((R, H), dtype=torch.float32, device=dev)
-    ws = torch.empty(dsa.decode_step_workspace_size(wl.B, R, wl.max_pages, H, wl.k),
+    out = torch.empty((wl.R, wl.H, inputs.V_DIM), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.R, wl.H), dtype=torch.float32, device=dev)
+    ws = torch.empty(dsa.decode_step_workspace_size(wl.B, wl.R, wl.max_pages, wl.H, wl.k),
                      dtype=torch.uint8, device=dev)
-    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.Stream(dev)
-    torch.cuda.set_stream(stream)
-    step_eager = _step_fn(dsa, inp, wl, ws, out, lse)
-    step_graph = _graph(step_eager, stream)
-    step = step_graph.replay
+    return inp, out, lse, ws
 
-    def flush():
-        flush_buf.fill_(1)
 
-    for _ in range(args.warmup):
-        flush()
-        step()
-    torch.cuda.synchronize()
-    if dsa.check_device_status(ws) != 0:
-        raise RuntimeError("device status raised during warm-up")
-
-    # ---- timed region: K steps, L2 flushed (untimed) before each -------------
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clocks:
-        step_ms, _ = _time_launches(step, args.steps, flush, stream)
-        torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clock_info = clocks.summary()
-    total_ms = reduce_max_ms(step_ms * args.steps, dev)
-    bytes_step = traffic.algorithmic_bytes(wl)
-    value = whole_job_gbs(bytes_step, world, args.steps, total_ms)
-    ms_per_step = total_ms / args.steps
-
-    # ---- per-kernel timing of the step's stages (same inputs, same launches) --
+def _stage_fns(dsa, wl, inp, out, lse, dev):
+    """The step's three C-ABI calls, each on its own buffers, with the algorithmic
+    bytes of each (None for the selection, which moves no algorithmic bytes)."""
+    R, H = wl.R, wl.H
     scores = torch.empty((R, wl.max_pages * inputs.PAGE), dtype=torch.float32, device=dev)
     idx = torch.empty((R, wl.k), dtype=torch.int32, device=dev)
     ws_s = torch.empty(dsa.indexer_score_workspace_size(R), dtype=torch.uint8, device=dev)
@@ -262,13 +229,123 @@ def run_gpu(args):
             lse=lse, workspace=ws_m),
             traffic.gather_bytes(wl) + R * H * (inputs.LAT_DIM + inputs.V_DIM) * 2),
     }
+    return stages, scores, idx, ws_s
+
+
+def _time_stages(stages, n, flush, stream):
+    """Each stage graph-replayed alone, L2 flushed before every replay."""
     stage_ms = {}
     for name, (fn, _) in stages.items():
         g = _graph(fn, stream)
         for _ in range(3):
             g.replay()
-        stage_ms[name] = _time_launches(g.replay, max(20, min(args.steps, 200)), flush, stream)[0]
-    eager_ms = _time_launches(step_eager, max(20, min(args.steps, 200)), flush, stream)[0]
+        stage_ms[name] = _time_launches(g.replay, n, flush, stream)[0]
+    return stage_ms
+
+
+def _side_workload(dsa, config, rank, dev, stream, flush, steps, hbm_peak):
+    """Step and stage times of another decode workload (reported beside the headline)."""
+    wl = rank_workload(config, rank)
+    inp, out, lse, ws = _step_buffers(dsa, wl, dev)
+    g = _graph(_step_fn(dsa, inp, wl, ws, out, lse), stream)
+    for _ in range(3):
+        flush()
+        g.replay()
+    ms = _time_launches(g.replay, steps, flush, stream)[0]
+    if dsa.check_device_status(ws) != 0:
+        raise RuntimeError(f"device status raised on {wl.name}")
+    stages, *_ = _stage_fns(dsa, wl, inp, out, lse, dev)
+    stage_ms = _time_stages(stages, steps, flush, stream)
+    b = traffic.algorithmic_bytes(wl)
+    gbs = b / (ms * 1e-3) / 1e9
+    res = {"us_per_step": round(ms * 1e3, 2), "gbs": round(gbs, 1),
+           "frac_of_8TBs": round(gbs / 8000.0, 4), "frac_of_measured": round(gbs / hbm_peak, 4),
+           "tokens_per_s": round(wl.R / (ms * 1e-3), 1), "algorithmic_bytes": b,
+           "stage_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()}, "steps": steps}
+    del inp, out, lse, ws, g, stages
+    torch.cuda.empty_cache()
+    return wl.name, res
+
+
+def _packed(tensors, device, pin):
+    """One buffer holding every tensor (256-byte aligned slots) and a view of each."""
+    offs, o = {}, 0
+    for k, t in tensors.items():
+        offs[k] = o
+        o += (t.numel() * t.element_size() + 255) // 256 * 256
+    buf = torch.empty(max(o, 256), dtype=torch.uint8, device=device)
+    if pin:
+        buf = buf.pin_memory()
+    views = {}
+    for k, t in tensors.items():
+        n = t.numel() * t.element_size()
+        views[k] = buf[offs[k]:offs[k] + n].view(t.dtype).view(t.shape)
+    return buf, views
+
+
+def run_gpu(args):
+    rank, world, local = _dist()
+    import dsa_sparse_attention_lightning_gb300 as dsa
+    dsa.load()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    wl = rank_workload(args.config, rank)
+    inp, out, lse, ws = _step_buffers(dsa, wl, dev)
+    R, H = wl.R, wl.H
+    flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+    step_eager = _step_fn(dsa, inp, wl, ws, out, lse)
+    step_graph = _graph(step_eager, stream)
+    step = step_graph.replay
+
+    def flush():
+        flush_buf.fill_(1)
+
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    if dsa.check_device_status(ws) != 0:
+        raise RuntimeError("device status raised during warm-up")
+
+    # ---- timed region: K steps, L2 flushed (untimed) before each; the clock
+    # sampler keeps running over at least a second of back-to-back replays of
+    # the same step right after it (the timed region alone is shorter than the
+    # sampling interval)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        step_ms, _ = _time_launches(step, args.steps, flush, stream)
+        torch.cuda.synchronize()
+        t_end = time.perf_counter() + CLOCK_WINDOW_S
+        window_steps = 0
+        while time.perf_counter() < t_end:
+            for _ in range(256):
+                flush()
+                step()
+            window_steps += 256
+            torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clock_info = clocks.summary()
+    clock_info["window"] = (f"timed region plus {window_steps} more replays of the same step "
+                            f"(>= {CLOCK_WINDOW_S:g} s)")
+    total_ms = reduce_max_ms(step_ms * args.steps, dev)
+    bytes_step = traffic.algorithmic_bytes(wl)
+    value = whole_job_gbs(bytes_step, world, args.steps, total_ms)
+    ms_per_step = total_ms / args.steps
+
+    # ---- per-kernel timing of the step's stages (same inputs, same launches) --
+    n_stage = max(20, min(args.steps, 200))
+    stages, scores, idx, ws_s = _stage_fns(dsa, wl, inp, out, lse, dev)
+    stage_ms = _time_stages(stages, n_stage, flush, stream)
+    eager_ms = _time_launches(step_eager, n_stage, flush, stream)[0]
 
     # ---- the same selection by the decode-context-parallel exchange (8 token
     # shards emulated on this GPU), on the step's scores
@@ -282,11 +359,12 @@ def run_gpu(args):
     g = _graph(dcp_fn, stream)
     for _ in range(3):
         g.replay()
-    dcp_ms = _time_launches(g.replay, max(20, min(args.steps, 200)), flush, stream)[0]
+    dcp_ms = _time_launches(g.replay, n_stage, flush, stream)[0]
     torch.cuda.synchronize()
     dcp = {"shards": DCP_W, "us": round(dcp_ms * 1e3, 2), "topk_us": round(stage_ms["topk"] * 1e3, 2),
            "rows_with_resend": int((dcp_res != 0).sum().item()),
            "equals_topk": bool(torch.equal(dcp_idx, idx))}
+    del ws_d, dcp_idx, g
     dominant = max((n for n in stages if stages[n][1] is not None), key=lambda n: stage_ms[n])
     hbm_peak, bf16_peak, peak_kind = _peaks()
     fp8_peak = bf16_peak * FP8_PER_BF16
@@ -319,28 +397,38 @@ def run_gpu(args):
                     "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
                     "frac": round(achieved / hbm_peak, 4), **common}
 
-    # ---- end to end through the public API with host buffers -----------------
-    host = {k: v.cpu().pin_memory() for k, v in inp.items()
-            if k in ("q_idx", "q_idx_scale", "w", "q", "block_table", "row_req", "row_len")
-            and v is not None}
-    dev_in = {k: inp[k] for k in host}
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    # ---- end to end through the public API with host buffers: the step's
+    # per-step inputs are packed in one pinned host buffer, copied with one
+    # host-to-device copy into one device buffer that the call's tensors view;
+    # out and lse come back the same way
+    per_step = {k: inp[k] for k in ("q_idx", "q_idx_scale", "w", "q", "block_table", "row_req",
+                                    "row_len") if inp.get(k) is not None}
+    dev_buf, dev_in = _packed(per_step, dev, pin=False)
+    host_buf, host_in = _packed(per_step, "cpu", pin=True)
+    for k2, t in per_step.items():
+        host_in[k2].copy_(t.cpu())
+    outs = {"out": out, "lse": lse}
+    dev_obuf, dev_out = _packed(outs, dev, pin=False)
+    host_obuf, _ = _packed(outs, "cpu", pin=True)
+    e2e_inp = dict(inp)
+    e2e_inp.update(dev_in)
+    e2e_call = _step_fn(dsa, e2e_inp, wl, ws, dev_out["out"], dev_out["lse"])
+    h2d = host_buf.numel()
+    d2h = host_obuf.numel()
 
     def e2e_step():
-        for k2, t in host.items():
-            dev_in[k2].copy_(t, non_blocking=True)
-        step_eager()
-        out_h.copy_(out, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        dev_buf.copy_(host_buf, non_blocking=True)
+        e2e_call()
+        host_obuf.copy_(dev_obuf, non_blocking=True)
 
     for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_ms = _time_launches(e2e_step, max(20, min(args.steps, 200)), flush, stream)[0]
+    e2e_ms = _time_launches(e2e_step, n_stage, flush, stream)[0]
     e2e_value = bytes_step * world / (e2e_ms * 1e-3) / 1e9
+    if not torch.equal(host_obuf[:out.numel() * 2].view(torch.bfloat16).view(out.shape).to(dev),
+                       out):
+        raise RuntimeError("end-to-end output differs from the device-resident step")
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -358,7 +446,7 @@ def run_gpu(args):
                                         inp["latent_scale"], inp["block_table"], inp["row_req"],
                                         new_pos, inp["key_cache"], inp["latent_cache"])
     g = _graph(write_fn, stream)
-    write_ms = _time_launches(g.replay, max(20, min(args.steps, 200)), flush, stream)[0]
+    write_ms = _time_launches(g.replay, n_stage, flush, stream)[0]
     write = {"tokens": R, "us": round(write_ms * 1e3, 2),
              "bytes": R * (inputs.IDX_DIM * 2 + inputs.LAT_DIM * 2 + inputs.IDX_DIM + 4 +
                            inputs.LAT_DIM)}
@@ -382,7 +470,7 @@ def run_gpu(args):
         g = _graph(mx_fn, stream)
         for _ in range(3):
             g.replay()
-        mx_ms = _time_launches(g.replay, max(20, min(args.steps, 200)), flush, stream)[0]
+        mx_ms = _time_launches(g.replay, n_stage, flush, stream)[0]
         mx_bytes = traffic.scan_bytes_mxfp4(wl)
         mx_gbs = mx_bytes / (mx_ms * 1e-3) / 1e9
         mxfp4 = {"us": round(mx_ms * 1e3, 2), "fp8_scan_us": round(stage_ms["indexer_scan"] * 1e3, 2),
@@ -397,6 +485,18 @@ def run_gpu(args):
     except dsa.DSAError as e:                          # reported, never fatal to the step's line
         mxfp4 = {"error": str(e)}
 
+    # ---- the other decode workloads, each step graph-replayed with L2 flushed
+    del inp, out, lse, ws, stages, scores, idx, ws_s, step_graph, g, dev_buf, dev_obuf
+    torch.cuda.empty_cache()
+    side = {}
+    if not args.no_side_configs:
+        for ci in SIDE_CONFIGS.get(args.config, ()):
+            try:
+                name, res = _side_workload(dsa, ci, rank, dev, stream, flush, 50, hbm_peak)
+                side[name] = res
+            except (dsa.DSAError, RuntimeError) as e:
+                side[inputs.config(ci).name] = {"error": str(e)}
+
     if world > 1:
         torch.distributed.destroy_process_group()
     if rank != 0:
@@ -405,6 +505,7 @@ def run_gpu(args):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "us_per_layer_step": round(ms_per_step * 1e3, 2),
+        "tokens_per_s": round(R * world / (ms_per_step * 1e-3), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> f32 (tensor cores), f32 softmax and selection",
         "data": "synthetic",
@@ -416,11 +517,13 @@ def run_gpu(args):
         "clocks": clock_info,
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
-                "note": "per-step inputs (queries, head weights, block table, rows) copied from "
-                        "pinned host memory and outputs copied back inside the timed region; "
-                        "the KV caches are resident layer state"},
+                "note": "per-step inputs (queries, head weights, block table, rows) packed in "
+                        "one pinned host buffer and copied with one host-to-device copy, "
+                        "out and lse copied back with one device-to-host copy, inside the "
+                        "timed region; the KV caches are resident layer state"},
         "roofline": roofline,
         "tensor": tensor,
+        "other_workloads": side,
         "dcp_topk": dcp,
         "write": write,
         "mxfp4_indexer": mxfp4,
@@ -444,8 +547,20 @@ def _oracle_sample(wl, inp_host, requests):
     return h, sample
 
 
+def _one_row_sample(wl, inp_host):
+    """Host inputs of the first row alone (its request's caches whole)."""
+    h = dict(inp_host)
+    for key in ("q_idx", "q_idx_scale", "w", "row_req", "row_len", "q"):
+        if h.get(key) is not None:
+            h[key] = np.ascontiguousarray(h[key][:1])
+    n = int(h["row_len"][0])
+    sample = inputs.Workload(wl.name + "_row0", [n], [1], H=wl.H, k=wl.k, q_idx_fp8=wl.q_idx_fp8)
+    return h, sample
+
+
 def cpu_baseline(wl, inp, target_s=10.0):
-    """Oracle on the first n requests, n grown until the run takes about target_s."""
+    """Oracle on the first n requests, n grown until the run takes about target_s,
+    on every host core; then the first row alone on one core."""
     from oracle import oracle
     host = inputs.to_numpy(inp)
     requests = 1
@@ -458,10 +573,23 @@ def cpu_baseline(wl, inp, target_s=10.0):
             break
         requests = min(wl.B, max(requests + 1, int(requests * target_s / max(dt, 1e-3))))
     b = traffic.algorithmic_bytes(sample)
-    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
-            "kind": "oracle", "seconds": round(dt, 3),
-            "sample": f"{requests} of {wl.B} requests ({sample.R} rows) of {wl.name}, full "
-                      f"step (scores, top-{wl.k}, attention), float64 C + OpenMP"}
+    res = {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": oracle.num_threads(),
+           "kind": "oracle", "seconds": round(dt, 3),
+           "sample": f"{requests} of {wl.B} requests ({sample.R} rows) of {wl.name}, full "
+                     f"step (scores, top-{wl.k}, attention), float64 C + OpenMP"}
+    threads = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        h1, s1 = _one_row_sample(wl, host)
+        t0 = time.perf_counter()
+        oracle.decode_step(h1, k=wl.k)
+        dt1 = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(threads)
+    res["one_core"] = {"value": round(traffic.algorithmic_bytes(s1) / dt1 / 1e9, 4),
+                       "unit": "GB/s", "cores": 1, "seconds": round(dt1, 3),
+                       "sample": f"row 0 of {wl.name} ({s1.ctx[0]} tokens), full step"}
+    return res
 
 
 def run_reference(args):
@@ -505,11 +633,13 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1,
-                    help="0 tiny, 1 16x4 rows @32K (default), 2 16x4 @256K, 3 1 row @1M, "
+    ap.add_argument("--config", type=int, default=2,
+                    help="0 tiny, 1 16x4 rows @32K, 2 16x4 @256K (default), 3 1 row @1M, "
                          "4 prefill chunk of 4096 rows @128K")
     ap.add_argument("--impl", default="dsa", choices=["dsa", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side-configs", action="store_true",
+                    help="skip the other decode workloads reported beside the headline")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "dsa":
         args.warmup = 3
