@@ -79,7 +79,7 @@ dcp_shard_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __
 // ---- 3. mark the shared candidates in the member bitmap -----------------------
 __global__ void __launch_bounds__(kThreads)
 dcp_candidates_kernel(const int32_t* __restrict__ row_len, int R, int64_t max_len, int W,
-                      const int32_t* __restrict__ lc, int c, uint32_t* __restrict__ bits,
+                      const int32_t* lc, int c, uint32_t* bits,
                       int64_t nwords) {
   pdl_trigger();
   pdl_wait();
@@ -102,7 +102,7 @@ dcp_candidates_kernel(const int32_t* __restrict__ row_len, int R, int64_t max_le
 __global__ void __launch_bounds__(kCompactThreads)
 dcp_compact_kernel(const float* __restrict__ scores, int64_t ld,
                    const int32_t* __restrict__ row_len, int64_t max_len,
-                   const uint32_t* __restrict__ bits, int64_t nwords, int32_t* __restrict__ mpos,
+                   const uint32_t* bits, int64_t nwords, int32_t* __restrict__ mpos,
                    float* __restrict__ mscore, int64_t ld_m, int32_t* __restrict__ mlen) {
   __shared__ uint32_t s_warp[kCompactThreads / 32];
   __shared__ uint32_t s_base;
@@ -147,9 +147,9 @@ dcp_compact_kernel(const float* __restrict__ scores, int64_t ld,
 __global__ void __launch_bounds__(kThreads)
 dcp_suspects_kernel(const float* __restrict__ scores, int64_t ld,
                     const int32_t* __restrict__ row_len, int R, int64_t max_len, int W, int k,
-                    const int32_t* __restrict__ ck, const int32_t* __restrict__ mpos, int64_t ld_m,
-                    const int32_t* __restrict__ lc, int c, const int32_t* __restrict__ lk,
-                    uint32_t* __restrict__ bits, int64_t nwords, uint32_t* __restrict__ resend) {
+                    const int32_t* ck, const int32_t* mpos, int64_t ld_m, const int32_t* lc,
+                    int c, const int32_t* lk, uint32_t* bits, int64_t nwords,
+                    uint32_t* __restrict__ resend) {
   __shared__ u64 s_min[kThreads / 32];
   __shared__ uint32_t s_mask;
   pdl_trigger();
@@ -218,7 +218,7 @@ dcp_suspects_kernel(const float* __restrict__ scores, int64_t ld,
 
 // ---- the selected members' positions (ascending, as the members are) ----------
 __global__ void __launch_bounds__(kThreads)
-dcp_positions_kernel(const int32_t* __restrict__ sel, const int32_t* __restrict__ mpos,
+dcp_positions_kernel(const int32_t* sel, const int32_t* mpos,
                      int64_t ld_m, int k, int32_t* __restrict__ idx) {
   pdl_trigger();
   pdl_wait();

@@ -133,6 +133,16 @@ __device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Data an earlier kernel of the chain wrote is read with ld_dep(): an
+// ordinary (coherent, L1-cached) load through a pointer without __restrict__,
+// which the compiler keeps below pdl_wait() (its asm clobbers memory).  Loads
+// on the read-only path (__ldg, or plain loads through a const __restrict__
+// pointer, which the compiler may turn into them) count as loads of memory
+// that never changes during the kernel, so they may be scheduled above
+// pdl_wait() and read what was there before the earlier kernel wrote it.
+template <typename T>
+__device__ __forceinline__ T ld_dep(const T* p) { return *p; }
+
 // Launches `kernel` on `st`; `chained` = may overlap the previous kernel on
 // the stream (it must follow the pdl_wait() rule above).
 template <typename... KArgs, typename... Args>

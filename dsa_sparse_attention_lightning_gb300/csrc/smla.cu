@@ -226,11 +226,10 @@ struct TileIt {
 template <int HG>  // heads per CTA: 16, 32 or 64
 __global__ void __launch_bounds__(kThreads, 1)
 smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__ CUtensorMap rope_map,
-            const uint8_t* __restrict__ q8,
-            const float* __restrict__ qc, int H, int64_t num_pages, float latent_scale,
+            const uint8_t* q8, const float* qc, int H, int64_t num_pages, float latent_scale,
             const int32_t* __restrict__ block_table, int B, int max_pages,
             const int32_t* __restrict__ row_req, const int32_t* __restrict__ row_len,
-            const int32_t* __restrict__ idx, int k, int R, float* __restrict__ part_o,
+            const int32_t* idx, int k, int R, float* __restrict__ part_o,
             float* __restrict__ part_lse, __nv_bfloat16* __restrict__ out,
             float* __restrict__ lse_out, uint32_t* status) {
   using L = MlaSmem<HG>;
@@ -370,7 +369,7 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
         const int j = slot0 + 4 * g + u;
         int yy = -1;                                  // out of range: zero-filled by TMA
         if (row_valid && j < k) {
-          const int tok = idx[(size_t)r * k + j];
+          const int tok = ld_dep(idx + (size_t)r * k + j);
           if (tok >= len) {
             raise_dev(status, DSA_DEV_BAD_INDEX);
           } else if (tok >= 0) {
@@ -434,7 +433,7 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
         uint32_t v[16];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint4 x = head_ok ? __ldg(src + c8 * 4 + u) : z;
+          const uint4 x = head_ok ? ld_dep(src + c8 * 4 + u) : z;
           v[4 * u + 0] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
         }
         tmem_st_32x32b_x16(tmem_base + ((uint32_t)(quarter * 32) << 16) + kQCol + c8 * 16, v);
@@ -442,14 +441,14 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
       const int m = quarter * 32 + lane;
 #pragma unroll
       for (int c4 = 2 * th; c4 < 2 * th + 2; ++c4) {
-        const uint4 x = head_ok ? __ldg(src + 32 + c4) : z;
+        const uint4 x = head_ok ? ld_dep(src + 32 + c4) : z;
         *reinterpret_cast<uint4*>(qrope + m * 128 + ((c4 ^ (m & 7)) << 4)) = x;
       }
       tmem_wait_st();
       fence_proxy_async_smem();
     };
     auto load_qc = [&](int r, int hg0) {
-      return head_ok ? __ldg(qc + (size_t)r * H + hg0 + hl) : 0.f;
+      return head_ok ? ld_dep(qc + (size_t)r * H + hg0 + hl) : 0.f;
     };
 
     float m_run = -INFINITY, l_run = 0.f, qcf = 0.f;
@@ -469,8 +468,8 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
     auto load_ids = [&](const TileIt& t, int& ia, int& ib) {
       const int* rowp = idx + (size_t)t.row(groups) * k;
       const int j = t.lt * kMlaTile + th * 64 + lane;
-      ia = __ldg(rowp + min(j, k - 1));
-      ib = __ldg(rowp + min(j + 32, k - 1));
+      ia = ld_dep(rowp + min(j, k - 1));
+      ib = ld_dep(rowp + min(j + 32, k - 1));
     };
     auto valid_bits = [&](const TileIt& t, int ia, int ib, uint32_t& lo_bits, uint32_t& hi_bits) {
       const int j = t.lt * kMlaTile + th * 64 + lane;
@@ -692,7 +691,7 @@ constexpr int kCombHeads = 16;
 
 template <int W>
 __global__ void __launch_bounds__(32 * kCombHeads)
-mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_lse, int R,
+mla_combine_kernel(const float* part_o, const float* part_lse, int R,
                    int H, int k, __nv_bfloat16* __restrict__ out, float* __restrict__ lse) {
   constexpr int NQ = 4 / W;                         // 16-byte chunks per lane per split
   pdl_trigger();
@@ -716,7 +715,7 @@ mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ p
     const int c = c0 + sp;
     return 2 * c + (w.begin(c) / w.NT == u ? 0 : 1);
   };
-  auto lse_of = [&](int sp) { return __ldg(part_lse + (size_t)slot_of(sp) * HG + hl); };
+  auto lse_of = [&](int sp) { return ld_dep(part_lse + (size_t)slot_of(sp) * HG + hl); };
   float M = -INFINITY;
   for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, lse_of(sp));
 #pragma unroll
@@ -743,7 +742,7 @@ mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ p
     float my_w = 0.f;
     if (sp0 + lane < ns) {
       my_slot = slot_of(sp0 + lane);
-      const float l = __ldg(part_lse + (size_t)my_slot * HG + hl);
+      const float l = ld_dep(part_lse + (size_t)my_slot * HG + hl);
       my_w = (M == -INFINITY || l == -INFINITY) ? 0.f : __expf(l - M) * inv;
     }
     const int cnt = min(32, ns - sp0);
@@ -757,8 +756,8 @@ mla_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ p
       float4 va[NQ], vb[NQ];
 #pragma unroll
       for (int q = 0; q < NQ; ++q) {
-        va[q] = __ldg(pa + q0 + lane + 32 * q);
-        vb[q] = __ldg(pb + q0 + lane + 32 * q);
+        va[q] = ld_dep(pa + q0 + lane + 32 * q);
+        vb[q] = ld_dep(pb + q0 + lane + 32 * q);
       }
 #pragma unroll
       for (int q = 0; q < NQ; ++q) {

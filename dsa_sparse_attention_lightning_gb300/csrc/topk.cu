@@ -188,8 +188,8 @@ __device__ uint32_t sample_threshold(KeyOf key_of, int len, int k, uint32_t* h, 
 }
 
 __global__ void __launch_bounds__(kSampleThreads)
-topk_sample_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
-                   int64_t max_len, int k, uint32_t* __restrict__ tau, uint32_t* __restrict__ cnt) {
+topk_sample_kernel(const float* scores, int64_t ld, const int32_t* __restrict__ row_len,
+                   int64_t max_len, int k, uint32_t* tau, uint32_t* cnt) {
   pdl_trigger();
   pdl_wait();                                  // the scores
   const int r = blockIdx.x;
@@ -209,7 +209,7 @@ topk_sample_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
   for (int u = 0; u < kSamplePer; ++u) {
     const int64_t e = (int64_t)u * kSampleThreads + threadIdx.x;
     const int64_t pos = sample_pos(e, sb);
-    sk[u] = (e < ns && pos < len) ? ordered_key(__ldg(row + pos)) : 0u;
+    sk[u] = (e < ns && pos < len) ? ordered_key(ld_dep(row + pos)) : 0u;
   }
   const uint32_t t = sample_threshold([&](int u, int64_t) { return sk[u]; }, len, k, h, warp_sums,
                                       &s_d, &s_above, &s_n);
@@ -218,10 +218,9 @@ topk_sample_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* 
 
 // ---- 2. candidates: every key >= tau -------------------------------------------
 __global__ void __launch_bounds__(kCollectThreads)
-topk_collect_kernel(const float* __restrict__ scores, int64_t ld,
-                    const int32_t* __restrict__ row_len, int64_t max_len, int k,
-                    const uint32_t* __restrict__ tau, uint32_t* __restrict__ cnt,
-                    uint2* __restrict__ runs, int nchunks, uint2* __restrict__ items) {
+topk_collect_kernel(const float* scores, int64_t ld, const int32_t* __restrict__ row_len,
+                    int64_t max_len, int k, const uint32_t* tau, uint32_t* cnt, uint2* runs,
+                    int nchunks, uint2* items) {
   pdl_trigger();
   pdl_wait();                                  // tau and the zeroed counts
   const int r = blockIdx.y;
@@ -244,7 +243,7 @@ topk_collect_kernel(const float* __restrict__ scores, int64_t ld,
   for (int i = 0; i < PER; i += 4) {
     float4 v;
     if (base + i + 4 <= s1) {
-      v = __ldg(reinterpret_cast<const float4*>(row + base + i));
+      v = ld_dep(reinterpret_cast<const float4*>(row + base + i));
     } else {
       v.x = base + i + 0 < s1 ? row[base + i + 0] : 0.f;
       v.y = base + i + 1 < s1 ? row[base + i + 1] : 0.f;
@@ -367,10 +366,9 @@ struct CandSmem {
 };
 
 __global__ void __launch_bounds__(kFinalThreads)
-topk_finalize_kernel(const float* __restrict__ scores, int64_t ld,
-                     const int32_t* __restrict__ row_len, int64_t max_len, int k,
-                     const uint32_t* __restrict__ cnt, const uint2* __restrict__ runs,
-                     int nchunks, const uint2* __restrict__ items, int32_t* __restrict__ idx,
+topk_finalize_kernel(const float* scores, int64_t ld, const int32_t* __restrict__ row_len,
+                     int64_t max_len, int k, const uint32_t* cnt, const uint2* runs,
+                     int nchunks, const uint2* items, int32_t* __restrict__ idx,
                      uint32_t* status) {
   extern __shared__ __align__(16) uint8_t fin_smem[];
   SelectSmem& S = *reinterpret_cast<SelectSmem*>(fin_smem);
@@ -538,7 +536,7 @@ __device__ __forceinline__ void write_selected(const uint32_t* keys, PosAt pos_a
 }
 
 __global__ void __launch_bounds__(kFinalThreads, 1)
-topk_row_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __restrict__ row_len,
+topk_row_kernel(const float* scores, int64_t ld, const int32_t* __restrict__ row_len,
                 int64_t max_len, int k, int32_t* __restrict__ idx, uint32_t* status) {
   static_assert(kFinalThreads == kSampleThreads, "the sample threshold runs on this block");
   extern __shared__ __align__(16) uint8_t row_smem[];
@@ -568,7 +566,7 @@ topk_row_kernel(const float* __restrict__ scores, int64_t ld, const int32_t* __r
 #pragma unroll
   for (int u = 0; u < kVecPer; ++u) {
     const int g = u * kFinalThreads + (int)threadIdx.x;
-    v[u] = g < n4 ? __ldg(reinterpret_cast<const float4*>(row) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
+    v[u] = g < n4 ? ld_dep(reinterpret_cast<const float4*>(row) + g) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 #pragma unroll
   for (int u = 0; u < kVecPer; ++u) {

@@ -376,6 +376,30 @@ def test_decode_step_deterministic_and_batch_invariant(dsa):
     assert np.abs(c[1][0] - a[1][4]).max() <= 1e-2
 
 
+def test_step_attention_equals_standalone_call_on_reused_memory(dsa):
+    """The fused step launches its attention kernel while the selection kernel
+    is still finishing (programmatic dependent launch).  Two steps in a row,
+    each with freshly allocated selection, output and workspace buffers (so
+    they land on memory the previous calls used), must give exactly what the
+    standalone attention call gives on the step's own selection: a read of
+    the selection that ran ahead of its producer shows up here as stale data."""
+    wl = inputs.config(1)                        # 16 x 4 rows, 32K: units cut over CTAs
+    inp = inputs.make_inputs(wl, device=DEV)
+    for _ in range(3):
+        idx = torch.full((wl.R, wl.k), -7, dtype=torch.int32, device=DEV)
+        out, lse = dsa.dsa_decode_step(inp["q_idx"], inp["w"], inp["key_cache"],
+                                       inp["latent_cache"], inp["latent_scale"],
+                                       inp["block_table"], inp["row_req"], inp["row_len"],
+                                       inp["q"], softmax_scale=inp["softmax_scale"], k=wl.k,
+                                       idx_out=idx)
+        out2, lse2 = dsa.dsa_sparse_mla_decode(inp["q"], inp["latent_cache"], inp["latent_scale"],
+                                               inp["block_table"], inp["row_req"],
+                                               inp["row_len"], idx,
+                                               softmax_scale=inp["softmax_scale"])
+        torch.cuda.synchronize()
+        assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
 def test_device_checks_flag_bad_values(dsa):
     wl = inputs.Workload("bad", [300], [1], H=16, k=64, seed=13)
     inp = inputs.make_inputs(wl, device=DEV)
