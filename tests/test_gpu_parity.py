@@ -400,6 +400,71 @@ def test_step_attention_equals_standalone_call_on_reused_memory(dsa):
         assert torch.equal(out, out2) and torch.equal(lse, lse2)
 
 
+# ------------------------------------------------- selection on built rows
+# The step's selection must equal dsa_topk over the full scores of
+# dsa_indexer_score bit for bit (the same kernels run on the same inputs),
+# also on rows built against the top-k's sampled threshold.
+def _step_vs_full_scores(dsa, inp, k):
+    R = inp["row_len"].shape[0]
+    idx = torch.full((R, k), -7, dtype=torch.int32, device=DEV)
+    dsa.dsa_decode_step(inp["q_idx"], inp["w"], inp["key_cache"], inp["latent_cache"],
+                        inp["latent_scale"], inp["block_table"], inp["row_req"], inp["row_len"],
+                        inp["q"], softmax_scale=inp["softmax_scale"], k=k,
+                        q_scale=inp["q_idx_scale"], idx_out=idx)
+    scores = dsa.dsa_indexer_score(inp["q_idx"], inp["w"], inp["key_cache"], inp["block_table"],
+                                   inp["row_req"], inp["row_len"], q_scale=inp["q_idx_scale"])
+    ref = dsa.dsa_topk(scores, inp["row_len"], k)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, ref)
+    return idx.cpu().numpy(), scores
+
+
+def _set_keys(inp, scale_of_pos):
+    """Every token's index key = one fixed E4M3 code vector, its scale
+    scale_of_pos(position) (so the scores follow the scale)."""
+    kc = inp["key_cache"]
+    P = kc.shape[0]
+    codes = kc[:, :64 * 128].view(P, 64, 128)
+    scales = kc[:, 64 * 128:].view(torch.float32).view(P, 64)
+    g = torch.Generator(device=DEV).manual_seed(99)
+    vec = torch.randn(128, generator=g, device=DEV)
+    code = (vec / vec.abs().max() * 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    bt = inp["block_table"].long()
+    for b, L in enumerate(inp["ctx"]):
+        pos = torch.arange(L, device=DEV)
+        pg, sl = bt[b, pos // 64], pos % 64
+        codes[pg, sl] = code
+        scales[pg, sl] = scale_of_pos(pos).float()
+
+
+@pytest.mark.parametrize("pattern", ["equal", "rising", "rising_steps", "ties_at_cut"])
+def test_step_selection_adversarial_rows(dsa, oracle_mod, pattern):
+    """Rows built against the selection: all scores equal (ties broken by
+    position), scores rising along the context (the winners come last),
+    rising in steps (long runs of exact ties), and many exact ties at the
+    cut; rows long enough for the sample / collect / finalize path and short
+    ones for the one-CTA path."""
+    ctx = [300000, 70000, 5000, 2100]
+    wl = inputs.Workload("sel_adv", ctx, [2, 1, 1, 3], H=16, k=2048, seed=31)
+    inp = inputs.make_inputs(wl, device=DEV)
+    inp["ctx"] = ctx
+    f = {"equal": lambda p: torch.ones_like(p, dtype=torch.float64),
+         "rising": lambda p: 1.0 + p.double() * 1e-4,
+         "rising_steps": lambda p: 1.0 + (p // 4096).double(),
+         "ties_at_cut": lambda p: torch.where(p % 7 == 0, 2.0, 1.0).double()}[pattern]
+    _set_keys(inp, f)
+    idx, scores = _step_vs_full_scores(dsa, inp, wl.k)
+    lens = inp["row_len"].cpu().numpy()
+    s32 = scores.cpu().numpy()
+    o = oracle_mod.topk(s32.astype(np.float64), lens, wl.k)
+    for r, L in enumerate(lens):
+        n = min(wl.k, L)
+        assert np.all(np.diff(idx[r, :n]) > 0) and np.all(idx[r, n:] == -1)
+        assert np.array_equal(idx[r, :n], np.sort(o[r, :n])), f"row {r}"
+        if pattern == "equal":
+            assert np.array_equal(idx[r, :n], np.arange(n))
+
+
 def test_device_checks_flag_bad_values(dsa):
     wl = inputs.Workload("bad", [300], [1], H=16, k=64, seed=13)
     inp = inputs.make_inputs(wl, device=DEV)
