@@ -485,6 +485,34 @@ def run_gpu(args):
     except dsa.DSAError as e:                          # reported, never fatal to the step's line
         mxfp4 = {"error": str(e)}
 
+    # ---- sparse MLA over an NVFP4 latent cache (352 bytes per token) for the
+    # same rows and selection (timing only; the parity of this path is in the tests)
+    def _nvfp4_leg():
+        nv_cache, nv_scale = inputs.nvfp4_latent_cache(inp, wl)
+        ws_n = torch.empty(dsa.sparse_mla_workspace_size(R, H, wl.k), dtype=torch.uint8,
+                           device=dev)
+        nv_fn = lambda: dsa.dsa_sparse_mla_decode_nvfp4(  # noqa: E731
+            inp["q"], nv_cache, nv_scale, inp["block_table"], inp["row_req"], inp["row_len"],
+            idx, softmax_scale=inp["softmax_scale"], out=out, lse=lse, workspace=ws_n)
+        g = _graph(nv_fn, stream)
+        for _ in range(3):
+            g.replay()
+        nv_ms = _time_launches(g.replay, n_stage, flush, stream)[0]
+        if dsa.check_device_status(ws_n) != 0:
+            raise RuntimeError("device status raised by the NVFP4 attention")
+        nv_bytes = traffic.gather_bytes_nvfp4(wl) + R * H * (inputs.LAT_DIM + inputs.V_DIM) * 2
+        nv_gbs = nv_bytes / (nv_ms * 1e-3) / 1e9
+        res = {"us": round(nv_ms * 1e3, 2), "fp8_mla_us": round(stage_ms["sparse_mla"] * 1e3, 2),
+               "speedup_vs_fp8": round(stage_ms["sparse_mla"] / nv_ms, 3), "bytes": nv_bytes,
+               "achieved_gbs": round(nv_gbs, 1), "frac": round(nv_gbs / hbm_peak, 4)}
+        del nv_cache, ws_n, g
+        return res
+
+    try:
+        nvfp4 = _nvfp4_leg()
+    except (dsa.DSAError, RuntimeError) as e:
+        nvfp4 = {"error": str(e)}
+
     # ---- the other decode workloads, each step graph-replayed with L2 flushed
     del inp, out, lse, ws, stages, scores, idx, ws_s, step_graph, g, dev_buf, dev_obuf
     torch.cuda.empty_cache()
@@ -527,6 +555,7 @@ def run_gpu(args):
         "dcp_topk": dcp,
         "write": write,
         "mxfp4_indexer": mxfp4,
+        "nvfp4_sparse_mla": nvfp4,
         "eager_ms_per_step": round(eager_ms, 5),
         "cpu_baseline": cpu,
         "gpu_launches": kernels_per_step(wl) * args.steps,

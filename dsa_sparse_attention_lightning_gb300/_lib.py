@@ -29,6 +29,7 @@ KEY_PAGE_BYTES = 8448
 MXFP4_KEY_PAGE_BYTES = 4352   # 64 x 64 E2M1 code bytes, then 64 x 4 E8M0 scale bytes
 LAT_DIM = 576
 V_DIM = 512
+NVFP4_ROW_BYTES = 352
 
 # (name, restype, argtypes) of every exported symbol, in header order.
 P, I32, I64, SZ, F32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
@@ -52,6 +53,8 @@ SIGNATURES = [
     ("dsa_sparse_mla_workspace_size", SZ, [I32, I32, I32]),
     ("dsa_sparse_mla_decode", I32, [P, I32, F32, P, I64, F32, P, I32, I32, P, P, P, I32, I32, P,
                                     P, P, SZ, P]),
+    ("dsa_sparse_mla_decode_nvfp4", I32, [P, I32, F32, P, I64, F32, P, I32, I32, P, P, P, I32,
+                                          I32, P, P, P, SZ, P]),
     ("dsa_decode_step_workspace_size", SZ, [I32, I32, I32, I32, I32]),
     ("dsa_decode_step", I32, [P, I32, P, P, P, P, I64, F32, P, I32, I32, P, P, I32, P, I32, F32,
                               I32, P, P, P, P, SZ, P]),
@@ -282,6 +285,20 @@ def sparse_mla_workspace_size(R: int, H: int, k: int) -> int:
 def dsa_sparse_mla_decode(q, latent_cache, latent_scale, block_table, row_req, row_len, idx, *,
                           softmax_scale, out=None, lse=None, workspace=None):
     """bf16 out [R,H,512] and fp32 lse [R,H] of attention over the selected rows."""
+    return _sparse_mla("dsa_sparse_mla_decode", LAT_DIM, q, latent_cache, latent_scale,
+                       block_table, row_req, row_len, idx, softmax_scale, out, lse, workspace)
+
+
+def dsa_sparse_mla_decode_nvfp4(q, latent_cache, latent_scale, block_table, row_req, row_len,
+                                idx, *, softmax_scale, out=None, lse=None, workspace=None):
+    """As dsa_sparse_mla_decode over an NVFP4 latent cache uint8 [pages, 64, 352]."""
+    return _sparse_mla("dsa_sparse_mla_decode_nvfp4", NVFP4_ROW_BYTES, q, latent_cache,
+                       latent_scale, block_table, row_req, row_len, idx, softmax_scale, out, lse,
+                       workspace)
+
+
+def _sparse_mla(fn, row_bytes, q, latent_cache, latent_scale, block_table, row_req, row_len, idx,
+                softmax_scale, out, lse, workspace):
     dev = q.device
     _need(q, "q", torch.bfloat16, dev)
     _need(latent_cache, "latent_cache", torch.uint8, dev)
@@ -298,9 +315,9 @@ def dsa_sparse_mla_decode(q, latent_cache, latent_scale, block_table, row_req, r
     _need(out, "out", torch.bfloat16, dev)
     _need(lse, "lse", torch.float32, dev)
     ws = _workspace(sparse_mla_workspace_size(R, H, k), dev, workspace)
-    _check("dsa_sparse_mla_decode", load().dsa_sparse_mla_decode(
+    _check(fn, getattr(load(), fn)(
         _ptr(q), H, float(softmax_scale), _ptr(latent_cache),
-        latent_cache.numel() // (PAGE * LAT_DIM), float(latent_scale), _ptr(block_table), B,
+        latent_cache.numel() // (PAGE * row_bytes), float(latent_scale), _ptr(block_table), B,
         max_pages, _ptr(row_req), _ptr(row_len), _ptr(idx), k, R, _ptr(out), _ptr(lse), _ptr(ws),
         ws.numel(), _stream(dev)))
     return out, lse

@@ -293,11 +293,12 @@ size_t dsa_sparse_mla_workspace_size(int R, int H, int k) {
   return kStatusBytes + MlaLayout(R, H, k).bytes;
 }
 
-int dsa_sparse_mla_decode(const void* q, int H, float softmax_scale, const uint8_t* latent_cache,
-                          int64_t num_pages, float latent_scale, const int32_t* block_table,
-                          int B, int max_pages, const int32_t* row_req, const int32_t* row_len,
-                          const int32_t* idx, int k, int R, void* out, float* lse,
-                          void* workspace, size_t ws_bytes, void* stream) {
+namespace {
+int sparse_mla(bool nvfp4, const void* q, int H, float softmax_scale, const uint8_t* latent_cache,
+               int64_t num_pages, float latent_scale, const int32_t* block_table, int B,
+               int max_pages, const int32_t* row_req, const int32_t* row_len, const int32_t* idx,
+               int k, int R, void* out, float* lse, void* workspace, size_t ws_bytes,
+               void* stream) {
   int s = check_rows(B, max_pages, block_table, row_req, row_len, R);
   if (s) return s;
   if (!supported_heads(H)) return DSA_ERR_UNSUPPORTED;
@@ -316,7 +317,30 @@ int dsa_sparse_mla_decode(const void* q, int H, float softmax_scale, const uint8
   MlaArgs a{q, H, softmax_scale, latent_cache, num_pages, latent_scale, block_table, B,
             max_pages, row_req, row_len, idx, k, R, out, lse,
             static_cast<uint8_t*>(workspace) + kStatusBytes, static_cast<uint32_t*>(workspace)};
+  a.nvfp4 = nvfp4;
   return to_status(launch_sparse_mla(a, st));
+}
+}  // namespace
+
+int dsa_sparse_mla_decode(const void* q, int H, float softmax_scale, const uint8_t* latent_cache,
+                          int64_t num_pages, float latent_scale, const int32_t* block_table,
+                          int B, int max_pages, const int32_t* row_req, const int32_t* row_len,
+                          const int32_t* idx, int k, int R, void* out, float* lse,
+                          void* workspace, size_t ws_bytes, void* stream) {
+  return sparse_mla(false, q, H, softmax_scale, latent_cache, num_pages, latent_scale,
+                    block_table, B, max_pages, row_req, row_len, idx, k, R, out, lse, workspace,
+                    ws_bytes, stream);
+}
+
+int dsa_sparse_mla_decode_nvfp4(const void* q, int H, float softmax_scale,
+                                const uint8_t* latent_cache, int64_t num_pages,
+                                float latent_scale, const int32_t* block_table, int B,
+                                int max_pages, const int32_t* row_req, const int32_t* row_len,
+                                const int32_t* idx, int k, int R, void* out, float* lse,
+                                void* workspace, size_t ws_bytes, void* stream) {
+  return sparse_mla(true, q, H, softmax_scale, latent_cache, num_pages, latent_scale,
+                    block_table, B, max_pages, row_req, row_len, idx, k, R, out, lse, workspace,
+                    ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------- fused step

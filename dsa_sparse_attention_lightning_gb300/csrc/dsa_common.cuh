@@ -246,6 +246,7 @@ struct MlaArgs {
   uint8_t* scratch;  // MlaLayout(R, H, k).bytes bytes
   uint32_t* status;
   bool chained = false;   // the first kernel may overlap the previous one on the stream
+  bool nvfp4 = false;     // latent_cache holds 352-byte NVFP4 rows instead of 576-byte E4M3
 };
 cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t st);
 

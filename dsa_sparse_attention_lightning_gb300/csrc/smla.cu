@@ -49,6 +49,7 @@
 // tile i + 1 against the softmax and P.V of tile i through mbarriers.
 #include <limits.h>
 #include <math.h>
+#include <string.h>
 
 #include "dsa_common.cuh"
 #include "sm100_ptx.cuh"
@@ -62,7 +63,13 @@ constexpr int kLatAtoms = 5;                          // 576 B = 4 x 128 B + 64 
 constexpr int kAtom = kMlaTile * 128;                 // 128 token rows x 128 B (dims 0..511)
 constexpr int kRopeAtom = kMlaTile * 64;              // 128 token rows x 64 B (dims 512..575)
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kRescaleT = 8.f;                      // log2 headroom of P before a rescale
+// P = 2^(x - m + kPOff) with m the running maximum, raised only when a tile's
+// maximum passes m + kRescaleT, so P <= 2^(kPOff + kRescaleT) = 256 < 448.
+// The offset keeps the tokens near the maximum at P >= 16, where the two E4M3
+// terms of P hold 8 significant bits, instead of near 1, where the low term
+// reaches E4M3's subnormal step.
+constexpr float kRescaleT = 4.f;                      // log2 headroom of P before a rescale
+constexpr float kPOff = 4.f;
 constexpr uint32_t kTmemCols = 512;
 
 __device__ __forceinline__ void named_sync(int id, int n) {
@@ -165,10 +172,28 @@ constexpr uint32_t kQCol = 0;                          // A operand: Q (dims 0..
 constexpr uint32_t kSCol = 128;                        // S: [(head, term)] x [128 tokens]
 constexpr uint32_t kOCol = 256;                        // O^T: 4 blocks x HG cols
 
-template <int HG>
+// NVFP4 latent rows (352 bytes: 256 bytes of E2M1 codes, dim 2j in the low
+// nibble of byte j; 32 unsigned-E4M3 scales, one per 16 dims; 64 E4M3 RoPE
+// bytes).  A value c * s (c an E2M1 element, s its block scale) has at most
+// six significant bits, so v = c * s / 4 = hi + lo with hi = E4M3(v) and
+// lo = v - hi, both exact in E4M3 when v >= 2^-4, i.e. for every s >= 0.5
+// (above 448, hi saturates at 448 and lo = v - 448 <= 224 is still exact).
+// The 1/4 is folded into the latent scale, so the RoPE bytes r are fed as
+// E4M3(r / 4), exact for |r| >= 2^-4.  Below those bounds the terms round to
+// E4M3's subnormal step: at most 2^-8 of the latent scale per element.
+constexpr int kNvRowBytes = 352;
+constexpr int kNvCodes = 256, kNvScales = 32;
+constexpr int kNvGatherThreads = (kSmWarp0 - kGatherWarp0) * 32;     // 192
+
+template <int HG, bool kNv>
 struct MlaSmem {
-  static constexpr int lat = 0;                                      // [2][4][128][128] + [2][128][64]
-  static constexpr int qrope = 2 * kTileBytes;                       // [128 rows][128 B]
+  // FP8 rows: two buffers of 4 atoms (dims 0..511) + a RoPE atom, filled by
+  // TMA.  NVFP4 rows: one buffer of 4 hi atoms, 4 lo atoms and a RoPE atom,
+  // written by the gather warps, then the byte offsets of two tiles' rows.
+  static constexpr int lat = 0;
+  static constexpr int lat_bytes = kNv ? 8 * kAtom + kRopeAtom : 2 * kTileBytes;
+  static constexpr int rowoff = lat + lat_bytes;                     // NVFP4: [2][128] int64
+  static constexpr int qrope = rowoff + (kNv ? 2 * kMlaTile * 8 : 0);   // [128 rows][128 B]
   static constexpr int p = qrope + kMlaTile * 128;                   // [2 terms][HG][128]
   static constexpr int corr = p + 2 * HG * 128;                      // [64] f32
   static constexpr int red = corr + 64 * 4;                          // [2 halves][64] f32
@@ -178,6 +203,7 @@ struct MlaSmem {
   static constexpr int tmem = bar + 18 * 8;
   static constexpr int bytes = tmem + 16;
   static constexpr int alloc = bytes + 1024;
+  static_assert(qrope % 1024 == 0, "the swizzled query operand stays 1024-byte aligned");
 };
 
 // TMA gather of four rows (y0..y3) x one box of the 2-D tensor map starting at
@@ -206,6 +232,87 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// Eight E2M1 values (four code bytes, low nibble first) -> four f16x2 pairs, exact.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t x, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(x));
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hsub2_u32(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t f16x2_to_e4m3x2(uint32_t x) {   // RN, saturating; 16 bits
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(x));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"((uint16_t)x));
+  return r;
+}
+
+// 32 NVFP4 dims (16 code bytes in c, their two block-scale bytes in sc, low
+// byte first) -> the E4M3 terms hi and lo of c * s / 4, 16 bytes each per 16
+// dims: hi[0], lo[0] for the first 16 dims, hi[1], lo[1] for the next.
+__device__ __forceinline__ void nvfp4_split32(const uint4& c, uint32_t sc, uint4 (&hi)[2],
+                                              uint4 (&lo)[2]) {
+  // the two scales as f16 (unsigned E4M3: the top bit is ignored), times 1/4
+  const uint32_t s2 = hmul2_u32(e4m3x2_to_f16x2(sc & 0x7F7Fu), 0x34003400u);   // {s0, s1} / 4
+  const uint32_t sa = __byte_perm(s2, 0, 0x1010), sb = __byte_perm(s2, 0, 0x3232);
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  uint32_t ho[8], lw[8];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t h[4];
+    e2m1x8_to_f16x2(w[q], h);
+    const uint32_t sq = q < 2 ? sa : sb;
+#pragma unroll
+    for (int e = 0; e < 4; e += 2) {
+      const uint32_t v0 = hmul2_u32(h[e], sq), v1 = hmul2_u32(h[e + 1], sq);
+      const uint32_t h0 = f16x2_to_e4m3x2(v0), h1 = f16x2_to_e4m3x2(v1);
+      const uint32_t l0 = f16x2_to_e4m3x2(hsub2_u32(v0, e4m3x2_to_f16x2(h0)));
+      const uint32_t l1 = f16x2_to_e4m3x2(hsub2_u32(v1, e4m3x2_to_f16x2(h1)));
+      ho[2 * q + e / 2] = h0 | (h1 << 16);
+      lw[2 * q + e / 2] = l0 | (l1 << 16);
+    }
+  }
+  hi[0] = make_uint4(ho[0], ho[1], ho[2], ho[3]);
+  hi[1] = make_uint4(ho[4], ho[5], ho[6], ho[7]);
+  lo[0] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  lo[1] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+}
+
+// Sixteen E4M3 RoPE bytes -> E4M3(r / 4), the scale of the NVFP4 operands.
+// Exact for |r| >= 2^-4; below, r / 4 is rounded to E4M3's subnormal step.
+__device__ __forceinline__ uint4 e4m3x16_quarter(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint32_t a = hmul2_u32(e4m3x2_to_f16x2(w[q] & 0xFFFFu), 0x34003400u);
+    const uint32_t b = hmul2_u32(e4m3x2_to_f16x2(w[q] >> 16), 0x34003400u);
+    o[q] = f16x2_to_e4m3x2(a) | (f16x2_to_e4m3x2(b) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // Walks a CTA's tiles in order: unit u (row u / groups, head group u % groups)
 // and tile lt within the unit; `first` / `last` mark the ends of a segment (a
 // run of the CTA's tiles in one unit).
@@ -223,16 +330,17 @@ struct TileIt {
   __device__ __forceinline__ bool last(int n, int NT) const { return i == n - 1 || lt == NT - 1; }
 };
 
-template <int HG>  // heads per CTA: 16, 32 or 64
+template <int HG, bool kNv>  // heads per CTA: 16, 32 or 64; NVFP4 latent rows
 __global__ void __launch_bounds__(kThreads, 1)
 smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__ CUtensorMap rope_map,
+            const uint8_t* __restrict__ nv_cache,
             const uint8_t* q8, const float* qc, int H, int64_t num_pages, float latent_scale,
             const int32_t* __restrict__ block_table, int B, int max_pages,
             const int32_t* __restrict__ row_req, const int32_t* __restrict__ row_len,
             const int32_t* idx, int k, int R, float* __restrict__ part_o,
             float* __restrict__ part_lse, __nv_bfloat16* __restrict__ out,
             float* __restrict__ lse_out, uint32_t* status) {
-  using L = MlaSmem<HG>;
+  using L = MlaSmem<HG, kNv>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -265,9 +373,12 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    prefetch_tensor_map(&lat_map);
-    prefetch_tensor_map(&rope_map);
-    for (int b = 0; b < 2; ++b) mbar_init(&lat_full[b], 1);
+    if constexpr (!kNv) {
+      prefetch_tensor_map(&lat_map);
+      prefetch_tensor_map(&rope_map);
+    }
+    // NVFP4: the gather warps each arrive once the tile is written
+    for (int b = 0; b < 2; ++b) mbar_init(&lat_full[b], kNv ? kSmWarp0 - kGatherWarp0 : 1);
     for (int x = 0; x < 2 * kLatAtoms; ++x) mbar_init(&lat_empty[x], 1);
     mbar_init(s_full, 1);
     mbar_init(s_empty, 8);
@@ -297,21 +408,28 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
     // ================= MMA issuers: warp 0 issues S(i) once tile i has landed
     // and S(i - 1) has been read; warp 1 issues O(i) once P(i) is in place
     auto issue_s = [&](int i) {
-      const uint32_t lb = smem_u32(lat + (i & 1) * kTileBytes);
+      const uint32_t lb = smem_u32(lat + (kNv ? 0 : (i & 1) * kTileBytes));
 #pragma unroll
       for (int j = 0; j < kIdxDim * 4 / 32; ++j)      // dims 0..511 from TMEM
         mma_e4m3_ts(tmem_base + kSCol, tmem_base + kQCol + (uint32_t)(j * 8),
                     desc_kmajor_sw128(lb + (j >> 2) * kAtom + (j & 3) * 32), idesc_s,
                     j > 0 ? 1u : 0u);
+      if constexpr (kNv) {                            // + the lo term of dims 0..511
+#pragma unroll
+        for (int j = 0; j < kIdxDim * 4 / 32; ++j)
+          mma_e4m3_ts(tmem_base + kSCol, tmem_base + kQCol + (uint32_t)(j * 8),
+                      desc_kmajor_sw128(lb + (4 + (j >> 2)) * kAtom + (j & 3) * 32), idesc_s, 1u);
+      }
+      const uint32_t rope_atom = lb + (kNv ? 8 : 4) * kAtom;
 #pragma unroll
       for (int j = 0; j < 2; ++j)                     // dims 512..575 from shared
         mma_e4m3_ss(tmem_base + kSCol, desc_kmajor_sw128(smem_u32(qrope) + j * 32),
-                    desc_kmajor_sw64(lb + 4 * kAtom + j * 32), idesc_s, 1u);
+                    desc_kmajor_sw64(rope_atom + j * 32), idesc_s, 1u);
       mma_commit(s_full);
-      mma_commit(&lat_empty[(i & 1) * kLatAtoms + 4]);   // the RoPE atom is read by S only
+      mma_commit(&lat_empty[(kNv ? 0 : (i & 1)) * kLatAtoms + 4]);   // the RoPE atom is read by S only
     };
     auto issue_o = [&](int i, bool first) {
-      const uint32_t lb = smem_u32(lat + (i & 1) * kTileBytes);
+      const uint32_t lb = smem_u32(lat + (kNv ? 0 : (i & 1) * kTileBytes));
       const uint32_t pb = smem_u32(ps);
 #pragma unroll
       for (int a = 0; a < kVDim / kMlaTile; ++a) {
@@ -322,15 +440,23 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
           mma_e4m3_ss(d, ad, desc_kmajor_sw128(pb + kk * 32), idesc_o,
                       (!first || kk > 0) ? 1u : 0u);
           mma_e4m3_ss(d, ad, desc_kmajor_sw128(pb + HG * 128 + kk * 32), idesc_o, 1u);
+          if constexpr (kNv) {                        // the lo term of V
+            const uint64_t al = desc_kmajor_sw128(lb + (4 + a) * kAtom + kk * 4096);
+            mma_e4m3_ss(d, al, desc_kmajor_sw128(pb + kk * 32), idesc_o, 1u);
+            mma_e4m3_ss(d, al, desc_kmajor_sw128(pb + HG * 128 + kk * 32), idesc_o, 1u);
+          }
         }
-        mma_commit(&lat_empty[(i & 1) * kLatAtoms + a]);   // M-block a was the last reader of atom a
+        // M-block a was the last reader of atom a (NVFP4: hi and lo atoms a)
+        mma_commit(&lat_empty[(kNv ? 0 : (i & 1)) * kLatAtoms + a]);
       }
       mma_commit(p_empty);
     };
     if (lane == 0 && n > 0) {
       if (warp == 0) {
         for (int si = 0; si < n; ++si) {
-          if (!mbar_wait(&lat_full[si & 1], (uint32_t)(si >> 1) & 1, status)) break;
+          if (!mbar_wait(&lat_full[kNv ? 0 : si & 1],
+                         kNv ? (uint32_t)si & 1 : (uint32_t)(si >> 1) & 1, status))
+            break;
           if (!mbar_wait(s_empty, (uint32_t)si & 1, status)) break;
           tc_fence_after();
           issue_s(si);
@@ -348,6 +474,107 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
       mbar_wait(&mma_done[warp], 0, status);
     }
     __syncwarp();
+  } else if (warp < kSmWarp0 && kNv) {
+    // ================= NVFP4 gather: the six gather warps look up the tile's
+    // rows, load their bytes into registers while the buffer is still in use,
+    // then write the RoPE atom once S of the previous tile has read it and the
+    // hi/lo terms of atom a once M-block a of the previous P.V has finished.
+    // Piece (row, p) of an atom is 32 dims (16 code bytes + 2 scale bytes) or,
+    // for the RoPE atom, 16 bytes; thread gtid takes pieces gtid + 192 m.
+    const int gtid = tid - kGatherWarp0 * 32;
+    int64_t* rowoff = reinterpret_cast<int64_t*>(smem + L::rowoff);
+    constexpr int kPieces = kMlaTile * 4;                  // per atom
+    constexpr int kPer = (kPieces + kNvGatherThreads - 1) / kNvGatherThreads;   // 3
+    bool alive = true;
+    TileIt gt = it0;
+    for (int i = 0; i < n; ++i) {
+      int64_t* ro = rowoff + (i & 1) * kMlaTile;
+      if (gtid < kMlaTile) {
+        const int r = gt.row(groups);
+        const int req = row_req[r];
+        const int len = row_len[r];
+        const bool row_valid =
+            req >= 0 && req < B && len >= 0 && (int64_t)len <= (int64_t)max_pages * kPage;
+        if (!row_valid && gt.lt == 0 && gt.hg0(groups, HG) == 0 && gtid == 0)
+          raise_dev(status, DSA_DEV_BAD_ROW);
+        const int j = gt.lt * kMlaTile + gtid;
+        int64_t off = -1;                             // masked slot: zero operands
+        if (row_valid && j < k) {
+          const int tok = ld_dep(idx + (size_t)r * k + j);
+          if (tok >= len) {
+            raise_dev(status, DSA_DEV_BAD_INDEX);
+          } else if (tok >= 0) {
+            const int page = block_table[(size_t)req * max_pages + tok / kPage];
+            if (page < 0 || (int64_t)page >= num_pages)
+              raise_dev(status, DSA_DEV_BAD_PAGE);
+            else
+              off = ((int64_t)page * kPage + tok % kPage) * kNvRowBytes;
+          }
+        }
+        ro[gtid] = off;
+      }
+      gt.next(NT);
+      // the other half of rowoff was last read before this barrier's previous phase
+      named_sync(2, kNvGatherThreads);
+      uint4 cv[4][kPer], rv[kPer];
+      uint32_t sv[4][kPer];
+#pragma unroll
+      for (int m = 0; m < kPer; ++m) {
+        const int e = gtid + kNvGatherThreads * m;
+        const int64_t off = e < kPieces ? ro[e >> 2] : -1;
+        const uint8_t* src = nv_cache + (off >= 0 ? off : 0);
+        const int p = e & 3;
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          cv[a][m] = off >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + (4 * a + p) * 16))
+                              : make_uint4(0, 0, 0, 0);
+          sv[a][m] = off >= 0 ? __ldg(reinterpret_cast<const uint16_t*>(src + kNvCodes +
+                                                                        (4 * a + p) * 2))
+                              : 0u;
+        }
+        rv[m] = off >= 0 ? __ldg(reinterpret_cast<const uint4*>(src + kNvCodes + kNvScales + p * 16))
+                         : make_uint4(0, 0, 0, 0);
+      }
+      const uint32_t ep = ((uint32_t)i & 1) ^ 1;      // parity of "free again" for tile i
+      if (alive && !wwait(&lat_empty[4], ep, status)) alive = false;
+      if (alive) {
+        uint8_t* ra = lat + 8 * kAtom;                // RoPE atom, 64-byte rows, 64B swizzle
+#pragma unroll
+        for (int m = 0; m < kPer; ++m) {
+          const int e = gtid + kNvGatherThreads * m;
+          if (e < kPieces) {
+            const int row = e >> 2, p = e & 3;
+            *reinterpret_cast<uint4*>(ra + row * 64 + ((p ^ ((row >> 1) & 3)) << 4)) =
+                e4m3x16_quarter(rv[m]);
+          }
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        if (alive && !wwait(&lat_empty[a], ep, status)) alive = false;
+        if (!alive) continue;
+        uint8_t* ha = lat + a * kAtom;                // 128-byte rows, 128B swizzle
+        uint8_t* la = lat + (4 + a) * kAtom;
+#pragma unroll
+        for (int m = 0; m < kPer; ++m) {
+          const int e = gtid + kNvGatherThreads * m;
+          if (e < kPieces) {
+            const int row = e >> 2, p = e & 3;
+            uint4 hi[2], lo[2];
+            nvfp4_split32(cv[a][m], sv[a][m], hi, lo);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int o = row * 128 + (((2 * p + u) ^ (row & 7)) << 4);
+              *reinterpret_cast<uint4*>(ha + o) = hi[u];
+              *reinterpret_cast<uint4*>(la + o) = lo[u];
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();                       // generic-proxy writes -> tensor core
+      __syncwarp();
+      if (lane == 0 && alive) mbar_arrive(&lat_full[0]);
+    }
   } else if (warp < kSmWarp0) {
     // ================= TMA gather: lane op = (group g of 4 tile rows, box a of 5)
     const int op = (warp - kGatherWarp0) * kGatherLanes + lane;
@@ -554,7 +781,7 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const float v = y[4 * j4 + u];
-          p[u] = (m_run > -INFINITY && v > -INFINITY) ? fast_exp2(v - m_run) : 0.f;
+          p[u] = (m_run > -INFINITY && v > -INFINITY) ? fast_exp2(v - m_run + kPOff) : 0.f;
           psum += p[u];
         }
         whi[j4] = pack_e4m3x4(p[0], p[1], p[2], p[3]);
@@ -656,7 +883,7 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
       if (th == 0 && (lane & 16) == 0 && head_ok) {
         const float l = lsum_s[hl] + lsum_s[64 + hl];
         const float ls = (alive && l > 0.f && m_run > -INFINITY)
-                             ? (m_run + log2f(l)) * 0.6931471805599453f
+                             ? (m_run - kPOff + log2f(l)) * 0.6931471805599453f
                              : -INFINITY;
         if (!whole) part_lse[(size_t)slot * HG + hl] = ls;
         else if (lse_out) lse_out[(size_t)r * H + hg0 + hl] = ls;
@@ -790,20 +1017,27 @@ cudaError_t latent_tensor_map(CUtensorMap* map, const uint8_t* cache, int64_t nu
   return encode_tensor_map_u8(map, 2, cache, dims, strides, box, (int)box_bytes);
 }
 
-template <int HG>
-cudaError_t launch_smla(const MlaArgs& a, const MlaLayout& L, int G, cudaStream_t st) {
-  using S = MlaSmem<HG>;
+template <int HG, bool kNv>
+cudaError_t launch_smla(const MlaArgs& a, const MlaLayout& L, int G, float lat_scale,
+                        cudaStream_t st) {
+  using S = MlaSmem<HG, kNv>;
   alignas(64) CUtensorMap map, rope;
-  cudaError_t e = latent_tensor_map(&map, a.latent_cache, a.num_pages, 128);
+  memset(&map, 0, sizeof(map));                       // NVFP4 rows are read without TMA
+  memset(&rope, 0, sizeof(rope));
+  cudaError_t e = cudaSuccess;
+  if (!kNv) {
+    e = latent_tensor_map(&map, a.latent_cache, a.num_pages, 128);
+    if (e != cudaSuccess) return e;
+    e = latent_tensor_map(&rope, a.latent_cache, a.num_pages, 64);
+    if (e != cudaSuccess) return e;
+  }
+  e = cudaFuncSetAttribute(smla_kernel<HG, kNv>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           S::alloc);
   if (e != cudaSuccess) return e;
-  e = latent_tensor_map(&rope, a.latent_cache, a.num_pages, 64);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(smla_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, S::alloc);
-  if (e != cudaSuccess) return e;
-  e = launch_kernel(smla_kernel<HG>, dim3(G), dim3(kThreads), S::alloc, st, true, map, rope,
-                    (const uint8_t*)(a.scratch + L.q8),
+  e = launch_kernel(smla_kernel<HG, kNv>, dim3(G), dim3(kThreads), S::alloc, st, true, map, rope,
+                    a.latent_cache, (const uint8_t*)(a.scratch + L.q8),
                     reinterpret_cast<const float*>(a.scratch + L.qc), a.H, a.num_pages,
-                    a.latent_scale, a.block_table, a.B, a.max_pages, a.row_req, a.row_len, a.idx,
+                    lat_scale, a.block_table, a.B, a.max_pages, a.row_req, a.row_len, a.idx,
                     a.k, a.R, reinterpret_cast<float*>(a.scratch + L.part_o),
                     reinterpret_cast<float*>(a.scratch + L.part_lse),
                     static_cast<__nv_bfloat16*>(a.out), a.lse, a.status);
@@ -819,14 +1053,22 @@ cudaError_t launch_sparse_mla(const MlaArgs& a, cudaStream_t st) {
   const MlaWork w(a.R, a.H, a.k);
   if (w.G > 0) {
     const int warps = a.R * a.H;
+    // NVFP4 operands hold c * s / 4 (see nvfp4_split32): the 4 joins the scale
+    const float lat_scale = a.nvfp4 ? 4.f * a.latent_scale : a.latent_scale;
     cudaError_t e = launch_kernel(mla_qprep_kernel, dim3((warps + 7) / 8), dim3(256), 0, st,
                                   a.chained, static_cast<const __nv_bfloat16*>(a.q), a.R, a.H,
-                                  a.softmax_scale, a.latent_scale, a.scratch + L.q8,
+                                  a.softmax_scale, lat_scale, a.scratch + L.q8,
                                   reinterpret_cast<float*>(a.scratch + L.qc));
     if (e != cudaSuccess) return e;
-    if (a.H == 16) e = launch_smla<16>(a, L, w.G, st);
-    else if (a.H == 32) e = launch_smla<32>(a, L, w.G, st);
-    else e = launch_smla<64>(a, L, w.G, st);
+    if (a.nvfp4) {
+      if (a.H == 16) e = launch_smla<16, true>(a, L, w.G, lat_scale, st);
+      else if (a.H == 32) e = launch_smla<32, true>(a, L, w.G, lat_scale, st);
+      else e = launch_smla<64, true>(a, L, w.G, lat_scale, st);
+    } else {
+      if (a.H == 16) e = launch_smla<16, false>(a, L, w.G, lat_scale, st);
+      else if (a.H == 32) e = launch_smla<32, false>(a, L, w.G, lat_scale, st);
+      else e = launch_smla<64, false>(a, L, w.G, lat_scale, st);
+    }
     if (e != cudaSuccess) return e;
   }
   // chained after the main kernel, or (no slots at all) after the caller's work

@@ -233,6 +233,50 @@ def make_inputs(wl: Workload, device="cpu", chunk_tokens: int = 1 << 20) -> Dict
     }
 
 
+NVFP4_ROW_BYTES = 352        # 256 code bytes + 32 block scales + 64 RoPE bytes
+NVFP4_SCALE_BYTES = (0x38, 0x48)   # block scales drawn from E4M3 codes 1.0 .. 3.75
+NVFP4_LATENT_SCALE = 0.15
+
+
+def nvfp4_latent_cache(inp: Dict[str, object], wl: Workload,
+                       scale_bytes=NVFP4_SCALE_BYTES, latent_scale: float = NVFP4_LATENT_SCALE):
+    """An NVFP4 latent cache for ``inp``'s block table: uint8 [num_pages, 64, 352].
+
+    Random bytes in the row layout of dsa_sparse_mla_decode_nvfp4: uniform
+    E2M1 code bytes (every nibble equally likely), block-scale bytes uniform
+    in [scale_bytes[0], scale_bytes[1]), and RoPE bytes that are the E4M3
+    codes of N(0, 1) / latent_scale.  The default scale range spreads each
+    block's magnitude over two binades, as the absmax / 6 scales of Gaussian
+    blocks do; with the default latent_scale the values have a mean square
+    of about 1, as the FP8 latent's have.  Slots outside every request's
+    context hold 0x7F, whose scale byte decodes to NaN, so a stray read shows
+    up.  Seeded by ``wl.seed``.  Returns (cache, latent_scale).
+    """
+    bt = inp["block_table"]
+    dev = bt.device
+    num_pages = inp["latent_cache"].shape[0]
+    g = torch.Generator(device=dev)
+    g.manual_seed(1_000_003 * int(wl.seed) + 12_345)
+    cache = torch.empty((num_pages, PAGE, NVFP4_ROW_BYTES), dtype=torch.uint8, device=dev)
+    cache[:, :, :256] = torch.randint(0, 256, (num_pages, PAGE, 256), generator=g, device=dev,
+                                      dtype=torch.int32).to(torch.uint8)
+    cache[:, :, 256:288] = torch.randint(int(scale_bytes[0]), int(scale_bytes[1]),
+                                         (num_pages, PAGE, 32), generator=g, device=dev,
+                                         dtype=torch.int32).to(torch.uint8)
+    rope = torch.randn(num_pages, PAGE, 64, generator=g, device=dev, dtype=torch.float32)
+    cache[:, :, 288:] = _e4m3_codes(rope / latent_scale)
+    valid = torch.zeros((num_pages, PAGE), dtype=torch.bool, device=dev)
+    for b, c in enumerate(wl.ctx):
+        n = (c + PAGE - 1) // PAGE
+        if n == 0:
+            continue
+        pages = bt[b, :n].to(torch.int64)
+        valid[pages[:-1]] = True
+        valid[pages[-1], :c - (n - 1) * PAGE] = True
+    cache[~valid] = E4M3_NAN
+    return cache, float(latent_scale)
+
+
 def to_numpy(inp: Dict[str, object]) -> Dict[str, object]:
     """Host copies for the oracle: bf16 as uint16 bits, E4M3 as uint8 codes."""
     out = {}

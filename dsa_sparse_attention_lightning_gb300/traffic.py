@@ -14,6 +14,7 @@ from .inputs import IDX_DIM, IDX_HEADS, LAT_DIM, V_DIM, Workload
 KEY_BYTES = IDX_DIM + 4          # 132 B per token per layer
 MXFP4_KEY_BYTES = IDX_DIM // 2 + IDX_DIM // 32   # 68 B: E2M1 codes + one E8M0 scale per 32 dims
 LATENT_BYTES = LAT_DIM           # 576 B per token per layer (FP8)
+NVFP4_LATENT_BYTES = 352         # the same row in NVFP4 + E4M3 RoPE
 
 
 def dense_mla_bytes_per_token() -> int:
@@ -40,6 +41,11 @@ def scan_bytes_mxfp4(wl: Workload) -> int:
 def gather_bytes(wl: Workload) -> int:
     """Latent rows gathered for every row (no credit for rows shared by rows)."""
     return int(sum(min(wl.k, n) for n in wl.row_lengths()) * LATENT_BYTES)
+
+
+def gather_bytes_nvfp4(wl: Workload) -> int:
+    """352 B NVFP4 latent row per selected token (256 B codes, 32 B scales, 64 B RoPE)."""
+    return int(sum(min(wl.k, n) for n in wl.row_lengths()) * NVFP4_LATENT_BYTES)
 
 
 def query_output_bytes(wl: Workload) -> int:

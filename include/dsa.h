@@ -320,6 +320,37 @@ int dsa_sparse_mla_decode(const void* q, int H, float softmax_scale, const uint8
                           void* workspace, size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
+ * dsa_sparse_mla_decode_nvfp4 -- step 3 over an NVFP4 latent cache: 352 bytes
+ * per token instead of 576 (vLLM Day-0 post on Kimi K3.1 Pro, "A packed KV
+ * cache for three kinds of state": the MLA latent is 576 bytes in FP8 or 352
+ * in NVFP4, and FlashInfer's PrimsTS kernels serve an NVFP4 latent).
+ *
+ * The pages give the row size only.  Row layout read here (the one split of
+ * 576 dims that gives 352 bytes): 256 bytes of E2M1 codes for dims 0..511
+ * (dim 2j in the low nibble of byte j), then 32 block scales in unsigned
+ * E4M3 (byte b scales dims 16b .. 16b + 15; its top bit is ignored), then the
+ * 64 RoPE dims as E4M3 bytes; latent_scale is the per-tensor fp32 scale:
+ *   L[d] = e2m1(code d) * ue4m3(scale d / 16) * latent_scale   (d < 512)
+ *   L[d] = e4m3(rope byte d - 512) * latent_scale              (d >= 512)
+ * The attention is then the one of dsa_sparse_mla_decode, with the same
+ * arguments, sizes, workspace (dsa_sparse_mla_workspace_size) and errors.
+ *
+ *  latent_cache  uint8 [num_pages][64][352], 16-byte aligned.
+ * Accuracy: the kernel feeds the tensor cores c * s / 4 (c the E2M1 value,
+ * s its block scale) as two E4M3 terms and a RoPE byte r as E4M3(r / 4).
+ * Both are exact for s >= 0.5 (scale byte >= 0x30) and |r| >= 2^-4; below,
+ * an element loses at most 2^-8 * latent_scale.  A scale byte 0x7F (or 0xFF)
+ * is NaN, as in E4M3.
+ * ---------------------------------------------------------------------- */
+#define DSA_NVFP4_LATENT_ROW_BYTES 352
+int dsa_sparse_mla_decode_nvfp4(const void* q, int H, float softmax_scale,
+                                const uint8_t* latent_cache, int64_t num_pages,
+                                float latent_scale, const int32_t* block_table, int B,
+                                int max_pages, const int32_t* row_req, const int32_t* row_len,
+                                const int32_t* idx, int k, int R, void* out, float* lse,
+                                void* workspace, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * dsa_decode_step -- the whole step (Score -> Select -> Attend), fused into
  * one launch sequence on `stream` with no host round trip.  Arguments mean
  * what they mean above; the scores never leave the workspace.

@@ -26,7 +26,8 @@ def declared_symbols():
 def test_header_declares_entry_points():
     names = declared_symbols()
     for n in ("dsa_indexer_score", "dsa_topk", "dsa_sparse_mla_decode", "dsa_decode_step",
-              "dsa_topk_workspace_size", "dsa_check_device_status"):
+              "dsa_sparse_mla_decode_nvfp4", "dsa_topk_workspace_size",
+              "dsa_check_device_status"):
         assert n in names
 
 
@@ -85,6 +86,11 @@ def test_mla_and_step_reject_bad_shapes(lib):
     assert lib.dsa_sparse_mla_decode(*args(48, 64)) == 2       # H not built
     assert lib.dsa_sparse_mla_decode(*args(64, 4096)) == 2     # k > 2048
     assert lib.dsa_sparse_mla_decode(*args(64, 0)) == 1
+    for f in (lib.dsa_sparse_mla_decode, lib.dsa_sparse_mla_decode_nvfp4):
+        assert f(*args(48, 64)) == 2
+        assert f(*args(64, 4096)) == 2
+        assert f(*args(64, 0)) == 1
+        assert f(*args(64, 64)[:-3], FAKE, ws - 1, None) == 3          # workspace too small
     wss = lib.dsa_decode_step_workspace_size(1, 1, 4, 64, 64)
     step = lambda qt, H: (FAKE, qt, None, FAKE, FAKE, FAKE, 4, 1.0, FAKE, 1, 4, FAKE, FAKE, 1,
                           FAKE, H, 0.1, 64, FAKE, None, None, FAKE, wss, None)

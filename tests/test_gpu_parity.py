@@ -456,6 +456,7 @@ def test_step_selection_adversarial_rows(dsa, oracle_mod, pattern):
     idx, scores = _step_vs_full_scores(dsa, inp, wl.k)
     lens = inp["row_len"].cpu().numpy()
     s32 = scores.cpu().numpy()
+    s32 = np.where(np.arange(s32.shape[1])[None, :] < lens[:, None], s32, 0)   # past len: unset
     o = oracle_mod.topk(s32.astype(np.float64), lens, wl.k)
     for r, L in enumerate(lens):
         n = min(wl.k, L)
