@@ -175,10 +175,15 @@ def _time_launches(fn, n, flush, stream):
     return statistics.mean(times), times
 
 
-def rank_workload(config: int, rank: int) -> inputs.Workload:
-    """Rank r steps its own replica: same shape, its own seed (independent requests)."""
+def rank_workload(config: int, rank: int, requests: int = 0) -> inputs.Workload:
+    """Rank r steps its own replica: same shape, its own seed (independent requests).
+    requests > 0 keeps only the first `requests` requests (a smaller device
+    footprint with the same per-request shape, for profiler captures)."""
     wl = inputs.config(config)
     wl.seed = wl.seed + 1000 * rank
+    if 0 < requests < wl.B:
+        wl.ctx, wl.rows = wl.ctx[:requests], wl.rows[:requests]
+        wl.name = f"{wl.name}_first{requests}requests"
     return wl
 
 
@@ -293,10 +298,14 @@ def run_gpu(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    wl = rank_workload(args.config, rank)
+    wl = rank_workload(args.config, rank, args.requests)
     inp, out, lse, ws = _step_buffers(dsa, wl, dev)
     R, H = wl.R, wl.H
     flush_buf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    # everything below runs on its own stream: the inputs' generation on the
+    # default stream (and the temporaries it freed, whose memory the buffers
+    # above may reuse) must be finished before that stream touches them
+    torch.cuda.synchronize()
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
     step_eager = _step_fn(dsa, inp, wl, ws, out, lse)
@@ -669,6 +678,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-side-configs", action="store_true",
                     help="skip the other decode workloads reported beside the headline")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="keep only the first N requests of the workload (profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "dsa":
         args.warmup = 3

@@ -199,8 +199,8 @@ struct MlaSmem {
   static constexpr int red = corr + 64 * 4;                          // [2 halves][64] f32
   static constexpr int lsum = red + 2 * 64 * 4;                      // [2 halves][64] f32
   static constexpr int flag = lsum + 2 * 64 * 4;                     // [2] int
-  static constexpr int bar = (flag + 8 + 7) / 8 * 8;                 // 18 mbarriers
-  static constexpr int tmem = bar + 18 * 8;
+  static constexpr int bar = (flag + 8 + 7) / 8 * 8;                 // 23 mbarriers
+  static constexpr int tmem = bar + 23 * 8;
   static constexpr int bytes = tmem + 16;
   static constexpr int alloc = bytes + 1024;
   static_assert(qrope % 1024 == 0, "the swizzled query operand stays 1024-byte aligned");
@@ -360,6 +360,7 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
   uint64_t* p_full = bars + 14;       // P in shared memory, O rescaled
   uint64_t* p_empty = bars + 15;      // P.V finished (O complete up to this tile)
   uint64_t* mma_done = bars + 16;     // [2] every MMA of an issuer finished
+  uint64_t* nv_full = bars + 18;      // NVFP4 [5]: hi/lo atom a (a < 4) or the RoPE atom written
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::tmem);
 
   const int groups = H / HG;
@@ -378,7 +379,8 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
       prefetch_tensor_map(&rope_map);
     }
     // NVFP4: the gather warps each arrive once the tile is written
-    for (int b = 0; b < 2; ++b) mbar_init(&lat_full[b], kNv ? kSmWarp0 - kGatherWarp0 : 1);
+    for (int b = 0; b < 2; ++b) mbar_init(&lat_full[b], 1);
+    for (int a = 0; a < kLatAtoms; ++a) mbar_init(&nv_full[a], kSmWarp0 - kGatherWarp0);
     for (int x = 0; x < 2 * kLatAtoms; ++x) mbar_init(&lat_empty[x], 1);
     mbar_init(s_full, 1);
     mbar_init(s_empty, 8);
@@ -407,18 +409,31 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
   if (warp < kGatherWarp0) {
     // ================= MMA issuers: warp 0 issues S(i) once tile i has landed
     // and S(i - 1) has been read; warp 1 issues O(i) once P(i) is in place
-    auto issue_s = [&](int i) {
+    // returns false when a wait ran out (NVFP4 waits for each atom in turn)
+    auto issue_s = [&](int i) -> bool {
       const uint32_t lb = smem_u32(lat + (kNv ? 0 : (i & 1) * kTileBytes));
+      if constexpr (!kNv) {
 #pragma unroll
-      for (int j = 0; j < kIdxDim * 4 / 32; ++j)      // dims 0..511 from TMEM
-        mma_e4m3_ts(tmem_base + kSCol, tmem_base + kQCol + (uint32_t)(j * 8),
-                    desc_kmajor_sw128(lb + (j >> 2) * kAtom + (j & 3) * 32), idesc_s,
-                    j > 0 ? 1u : 0u);
-      if constexpr (kNv) {                            // + the lo term of dims 0..511
-#pragma unroll
-        for (int j = 0; j < kIdxDim * 4 / 32; ++j)
+        for (int j = 0; j < kIdxDim * 4 / 32; ++j)    // dims 0..511 from TMEM
           mma_e4m3_ts(tmem_base + kSCol, tmem_base + kQCol + (uint32_t)(j * 8),
-                      desc_kmajor_sw128(lb + (4 + (j >> 2)) * kAtom + (j & 3) * 32), idesc_s, 1u);
+                      desc_kmajor_sw128(lb + (j >> 2) * kAtom + (j & 3) * 32), idesc_s,
+                      j > 0 ? 1u : 0u);
+      } else {
+        // hi and lo terms of atom a as soon as the gather warps have written them
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          if (!mbar_wait(&nv_full[a], (uint32_t)i & 1, status)) return false;
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+              mma_e4m3_ts(tmem_base + kSCol, tmem_base + kQCol + (uint32_t)((4 * a + jj) * 8),
+                          desc_kmajor_sw128(lb + (4 * t + a) * kAtom + jj * 32), idesc_s,
+                          (a | t | jj) ? 1u : 0u);
+        }
+        if (!mbar_wait(&nv_full[4], (uint32_t)i & 1, status)) return false;
+        tc_fence_after();
       }
       const uint32_t rope_atom = lb + (kNv ? 8 : 4) * kAtom;
 #pragma unroll
@@ -427,6 +442,7 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
                     desc_kmajor_sw64(rope_atom + j * 32), idesc_s, 1u);
       mma_commit(s_full);
       mma_commit(&lat_empty[(kNv ? 0 : (i & 1)) * kLatAtoms + 4]);   // the RoPE atom is read by S only
+      return true;
     };
     auto issue_o = [&](int i, bool first) {
       const uint32_t lb = smem_u32(lat + (kNv ? 0 : (i & 1) * kTileBytes));
@@ -454,12 +470,10 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
     if (lane == 0 && n > 0) {
       if (warp == 0) {
         for (int si = 0; si < n; ++si) {
-          if (!mbar_wait(&lat_full[kNv ? 0 : si & 1],
-                         kNv ? (uint32_t)si & 1 : (uint32_t)(si >> 1) & 1, status))
-            break;
+          if (!kNv && !mbar_wait(&lat_full[si & 1], (uint32_t)(si >> 1) & 1, status)) break;
           if (!mbar_wait(s_empty, (uint32_t)si & 1, status)) break;
           tc_fence_after();
-          issue_s(si);
+          if (!issue_s(si)) break;
         }
       } else {
         TileIt ot = it0;                              // tile of the next O
@@ -548,6 +562,9 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
                 e4m3x16_quarter(rv[m]);
           }
         }
+        fence_proxy_async_smem();                     // generic-proxy writes -> tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&nv_full[4]);
       }
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
@@ -570,10 +587,10 @@ smla_kernel(const __grid_constant__ CUtensorMap lat_map, const __grid_constant__
             }
           }
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&nv_full[a]);
       }
-      fence_proxy_async_smem();                       // generic-proxy writes -> tensor core
-      __syncwarp();
-      if (lane == 0 && alive) mbar_arrive(&lat_full[0]);
     }
   } else if (warp < kSmWarp0) {
     // ================= TMA gather: lane op = (group g of 4 tile rows, box a of 5)
