@@ -158,11 +158,11 @@ int dsa_indexer_score(const void* q_idx, int q_dtype, const float* q_scale, cons
   s = check_workspace(workspace, ws_bytes, dsa_indexer_score_workspace_size(R));
   if (s) return s;
   cudaStream_t st = as_stream(stream);
-  if ((s = clear_status(workspace, st))) return s;
-  if (R == 0) return DSA_OK;
+  if (R == 0) return clear_status(workspace, st);
   ScanArgs a{q_idx, q_dtype, q_scale, w, key_cache, num_pages, block_table, B, max_pages,
              row_req, row_len, R, scores, ld, static_cast<uint8_t*>(workspace) + kStatusBytes,
              static_cast<uint32_t*>(workspace)};
+  a.clear_status = true;                           // the prep kernel clears the word
   return to_status(launch_indexer_scan(a, st));
 }
 
@@ -387,8 +387,7 @@ int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const 
   s = check_workspace(workspace, ws_bytes, L.bytes);
   if (s) return s;
   cudaStream_t st = as_stream(stream);
-  if ((s = clear_status(workspace, st))) return s;
-  if (R == 0) return DSA_OK;
+  if (R == 0) return clear_status(workspace, st);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint32_t* status = reinterpret_cast<uint32_t*>(ws);
   float* scores = reinterpret_cast<float*>(ws + L.scores);
@@ -397,6 +396,7 @@ int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const 
 
   ScanArgs sa{q_idx, q_dtype, q_scale, w, key_cache, num_pages, block_table, B, max_pages,
               row_req, row_len, R, scores, ld, ws + L.scan, status};
+  sa.clear_status = true;                          // the step's first kernel clears the word
   cudaError_t e = launch_indexer_scan(sa, st);
   if (e != cudaSuccess) return to_status(e);
   TopkArgs ta{scores, ld, row_len, R, ld, k, idx, ws + L.topk, status, true};

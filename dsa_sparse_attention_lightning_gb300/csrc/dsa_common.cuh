@@ -202,6 +202,7 @@ struct ScanArgs {
   uint8_t* scratch;  // scan_scratch_bytes(R) bytes
   uint32_t* status;
   const uint8_t* q_sf = nullptr;   // kQMxfp4 only
+  bool clear_status = false;       // the prep kernel zeroes *status (no separate memset)
 };
 size_t scan_scratch_bytes(int R);
 cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st);

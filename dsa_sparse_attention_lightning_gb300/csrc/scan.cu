@@ -208,13 +208,18 @@ scan_prep_kernel(const void* __restrict__ q_idx, int q_dtype, const float* __res
                  const uint8_t* __restrict__ q_sf, const float* __restrict__ w,
                  const int32_t* __restrict__ row_req,
                  const int32_t* __restrict__ row_len, int R, int B, int max_pages, int nctas,
-                 ScanWs ws, uint32_t* status) {
+                 ScanWs ws, uint32_t* status, int clear_status) {
   pdl_wait();
   pdl_trigger();
   if (blockIdx.x == (unsigned)R) {
     __shared__ int warp_buf[32];
     __shared__ int s_carry[3];   // run start of the last row, groups so far, tiles so far
-    if (threadIdx.x == 0) { s_carry[0] = -1; s_carry[1] = 0; s_carry[2] = 0; }
+    if (threadIdx.x == 0) {
+      s_carry[0] = -1; s_carry[1] = 0; s_carry[2] = 0;
+      // the first writer of the step's status word: every raise comes after
+      // this (below in this block, or in kernels that wait for this grid)
+      if (clear_status) *status = 0u;
+    }
     __syncthreads();
     for (int base = 0; base < R; base += kPrepThreads) {
       const int r = base + threadIdx.x;
@@ -897,7 +902,7 @@ cudaError_t launch_indexer_scan(const ScanArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   scan_prep_kernel<<<a.R + 1, kPrepThreads, 0, st>>>(a.q_idx, a.q_dtype, a.q_scale, a.q_sf, a.w,
                                              a.row_req, a.row_len, a.R, a.B, a.max_pages, sms,
-                                             ws, a.status);
+                                             ws, a.status, a.clear_status ? 1 : 0);
   e = launch_kernel(kernel, dim3(sms), dim3(kThreads), kSmemAlloc, st, true, kmap, qmap,
                     a.key_cache, a.num_pages, a.block_table, a.max_pages, a.row_len, a.scores,
                     a.ld, a.R, a.q_dtype == DSA_E4M3 ? 1 : 2, ws, a.status);
