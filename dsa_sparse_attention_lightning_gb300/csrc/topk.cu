@@ -9,7 +9,7 @@
 // candidates); longer rows take three launches:
 //
 //   1. sample   (one CTA per row): a fixed sample of the row (every sb-th
-//               block of 32 scores, sb >= 16, at most 16384 scores) gives a
+//               block of 32 scores, sb >= 16, at most 8192 scores) gives a
 //               threshold tau low enough that the row should hold about
 //               1.25 k + 16 sb keys >= tau: the key of the sample's rank-rho
 //               element, rounded down to its 22-bit prefix (two radix digits
@@ -118,7 +118,7 @@ __device__ __forceinline__ void hist_add(uint32_t* h, uint32_t bin, bool valid) 
 // ---- 1. threshold from a fixed sample ----------------------------------------
 // Every sb-th block of 32 scores, sb >= 16 chosen so that the sample holds at
 // most kSampleBlocks blocks.
-constexpr int kSampleBlocks = 512;
+constexpr int kSampleBlocks = 256;
 
 __device__ __forceinline__ int64_t sample_stride(int len) {
   const int64_t blocks = ((int64_t)len + 31) / 32;
