@@ -53,11 +53,9 @@ def kernels_per_step(wl) -> int:
 # intermediates count as DRAM reads).  Stages and workloads not captured on the
 # current kernels report null.
 NCU_STAGE_TRAFFIC = {
-    ("decode_16x4_ctx32768_h64", "indexer_scan"): 70.40e6,
-    ("decode_16x4_ctx32768_h64", "topk"): 8.46e6,
-    ("decode_16x4_ctx32768_h64", "sparse_mla"): 104.41e6,
-    # prefill chunk: the scan kernel alone
-    ("prefill_4096rows_ctx131072_h64", "indexer_scan"): 2098.86e6,
+    # the scan kernel on the first 4 of the 16 requests (same per-request shape),
+    # its read + write bytes scaled by 4: its traffic grows with the tiles it reads
+    ("decode_16x4_ctx262144_h64", "indexer_scan"): 4 * (138.66e6 + 5.42e6),
 }
 
 
