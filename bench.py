@@ -372,6 +372,31 @@ def run_gpu(args):
            "rows_with_resend": int((dcp_res != 0).sum().item()),
            "equals_topk": bool(torch.equal(dcp_idx, idx))}
     del ws_d, dcp_idx, g
+    # What one of the W GPUs would run (communication aside): the local top-k
+    # and top-c of its own shard (every W-th token of each row), then the top-k
+    # of the W x c gathered candidates.  Timed with the library's top-k on a
+    # shard of the step's scores and on W x c of a row's scores as stand-ins.
+    c_dcp = min(2048, -(-3 * wl.k // (2 * DCP_W)))
+    shard = scores[:, 0::DCP_W].contiguous()
+    shard_len = ((inp["row_len"] + DCP_W - 1) // DCP_W).to(torch.int32)
+    cand = scores[:, :DCP_W * c_dcp].contiguous()
+    cand_len = torch.minimum(inp["row_len"], torch.full_like(inp["row_len"], DCP_W * c_dcp))
+    torch.cuda.synchronize()
+    rank_fns = {
+        "local_topk": lambda: dsa.dsa_topk(shard, shard_len, wl.k),
+        "local_topc": lambda: dsa.dsa_topk(shard, shard_len, c_dcp),
+        "merge_topk": lambda: dsa.dsa_topk(cand, cand_len, wl.k),
+    }
+    rank_us = {}
+    for name, fn in rank_fns.items():
+        g = _graph(fn, stream)
+        for _ in range(3):
+            g.replay()
+        rank_us[name] = round(_time_launches(g.replay, n_stage, flush, stream)[0] * 1e3, 2)
+        del g
+    dcp["per_rank_us"] = {**rank_us, "sum": round(sum(rank_us.values()), 2),
+                          "candidates_per_shard": c_dcp}
+    del shard, cand
     dominant = max((n for n in stages if stages[n][1] is not None), key=lambda n: stage_ms[n])
     hbm_peak, bf16_peak, peak_kind = _peaks()
     fp8_peak = bf16_peak * FP8_PER_BF16
