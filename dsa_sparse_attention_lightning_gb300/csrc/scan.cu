@@ -167,6 +167,7 @@ ScanWs scan_ws(uint8_t* base, int R) {
 //    scales as the tensor core's scale-factor rows (in the q8 area): row h,
 //    32-bit word j = the four E8M0 scales of head h of the group's row j.
 constexpr int kPrepThreads = 1024;
+constexpr int kPrepGroupCache = 4096;          // group starts kept in shared memory
 
 template <typename T, typename Op>
 __device__ __forceinline__ T block_scan_incl(T v, T* warp_buf, Op op, T identity) {
@@ -214,6 +215,7 @@ scan_prep_kernel(const void* __restrict__ q_idx, int q_dtype, const float* __res
   if (blockIdx.x == (unsigned)R) {
     __shared__ int warp_buf[32];
     __shared__ int s_carry[3];   // run start of the last row, groups so far, tiles so far
+    __shared__ int s_gstart[kPrepGroupCache + 1];   // group tile starts, for the CTA-range search
     if (threadIdx.x == 0) {
       s_carry[0] = -1; s_carry[1] = 0; s_carry[2] = 0;
       // the first writer of the step's status word: every raise comes after
@@ -249,6 +251,7 @@ scan_prep_kernel(const void* __restrict__ q_idx, int q_dtype, const float* __res
         const int g = carry_groups + g_incl - 1;
         ws.groups[g] = make_int4(r, nrows, req, maxlen);
         ws.gstart[g] = carry_tiles + t_incl - tiles;
+        if (g < kPrepGroupCache) s_gstart[g] = carry_tiles + t_incl - tiles;
       }
       __syncthreads();                                    // everyone has read the carries
       if (threadIdx.x == kPrepThreads - 1) {
@@ -266,6 +269,9 @@ scan_prep_kernel(const void* __restrict__ q_idx, int q_dtype, const float* __res
     // each scan CTA's tile range and the group holding its first tile (the
     // last group whose first tile is <= it, as TileCursor::seek finds it)
     const int ngroups = s_carry[1], total = s_carry[2];
+    // the search reads the group starts from shared memory when they fit (one
+    // dependent global load per step otherwise)
+    const int* gs = ngroups <= kPrepGroupCache ? s_gstart : ws.gstart;
     if (nctas <= kMaxScanCtas) {
       for (int c = threadIdx.x; c < nctas; c += kPrepThreads) {
         const int tb = (int)((int64_t)total * c / nctas);
@@ -273,7 +279,7 @@ scan_prep_kernel(const void* __restrict__ q_idx, int q_dtype, const float* __res
         int lo = 0, hi = ngroups;
         while (hi - lo > 1) {
           const int mid = (lo + hi) >> 1;
-          if (ws.gstart[mid] <= tb) lo = mid; else hi = mid;
+          if (gs[mid] <= tb) lo = mid; else hi = mid;
         }
         ws.cta[c] = make_int4(lo, tb, te, ngroups);
       }

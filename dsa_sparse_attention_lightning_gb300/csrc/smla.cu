@@ -990,6 +990,29 @@ mla_combine_kernel(const float* part_o, const float* part_lse, int R,
       my_w = (M == -INFINITY || l == -INFINITY) ? 0.f : __expf(l - M) * inv;
     }
     const int cnt = min(32, ns - sp0);
+    if constexpr (W == 4) {
+      // few heads, many splits (one long row): eight splits in flight, one
+      // memory round trip for most of them; missing ones weigh 0
+      constexpr int NB = 8;
+      for (int j = 0; j < cnt; j += NB) {
+        float4 v[NB];
+        float wv[NB];
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const bool has = j + b < cnt;
+          const int sl = __shfl_sync(0xffffffffu, my_slot, (j + b) & 31);
+          const float wt = __shfl_sync(0xffffffffu, my_w, (j + b) & 31);
+          const int s0 = __shfl_sync(0xffffffffu, my_slot, j);
+          wv[b] = has ? wt : 0.f;
+          const float4* p =
+              reinterpret_cast<const float4*>(part_o + ((size_t)(has ? sl : s0) * HG + hl) * kVDim);
+          v[b] = ld_dep(p + q0 + lane);
+        }
+#pragma unroll
+        for (int b = 0; b < NB; ++b) add(wv[b], v[b], acc[0]);
+      }
+      continue;
+    }
     for (int j = 0; j < cnt; j += 2) {              // two splits in flight (the second may be empty)
       const int sa = __shfl_sync(0xffffffffu, my_slot, j);
       const float wa = __shfl_sync(0xffffffffu, my_w, j);
