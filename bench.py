@@ -598,6 +598,46 @@ def run_gpu(args):
     except (dsa.DSAError, RuntimeError) as e:
         nvfp4 = {"error": str(e)}
 
+    # ---- the whole step over MXFP4 index keys and NVFP4 latent rows (the
+    # pages' 10,080-byte-per-token caches) on the same pages and rows: random
+    # MXFP4 keys and query, random NVFP4 rows (timing only; parity in the tests)
+    def _fp4_step_leg():
+        num_pages = inp["key_cache"].shape[0]
+        kc = torch.randint(0, 256, (num_pages, 4352), dtype=torch.uint8, device=dev,
+                           generator=gen)
+        kc[:, 4096:] = torch.randint(124, 131, (num_pages, 256), dtype=torch.uint8, device=dev,
+                                     generator=gen)
+        qc4 = torch.randint(0, 256, (R, inputs.IDX_HEADS, 64), dtype=torch.uint8, device=dev,
+                            generator=gen)
+        qs4 = torch.randint(124, 131, (R, inputs.IDX_HEADS, 4), dtype=torch.uint8, device=dev,
+                            generator=gen)
+        nv_cache, nv_scale = inputs.nvfp4_latent_cache(inp, wl)
+        ws4 = torch.empty(dsa.decode_step_workspace_size(wl.B, R, wl.max_pages, H, wl.k),
+                          dtype=torch.uint8, device=dev)
+        fn = lambda: dsa.dsa_decode_step_fp4(  # noqa: E731
+            qc4, qs4, inp["w"], kc, nv_cache, nv_scale, inp["block_table"], inp["row_req"],
+            inp["row_len"], inp["q"], softmax_scale=inp["softmax_scale"], k=wl.k, out=out,
+            lse=lse, workspace=ws4)
+        g = _graph(fn, stream)
+        for _ in range(3):
+            flush()
+            g.replay()
+        ms = _time_launches(g.replay, n_stage, flush, stream)[0]
+        if dsa.check_device_status(ws4) != 0:
+            raise RuntimeError("device status raised by the FP4 step")
+        b4 = traffic.algorithmic_bytes_fp4(wl)
+        gbs = b4 / (ms * 1e-3) / 1e9
+        res = {"us_per_step": round(ms * 1e3, 2), "fp8_us_per_step": round(ms_per_step * 1e3, 2),
+               "algorithmic_bytes": b4, "gbs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+               "kv_bytes_per_token": {"index_key": 68, "latent": 352}}
+        del kc, nv_cache, ws4, g
+        return res
+
+    try:
+        fp4_step = _fp4_step_leg()
+    except (dsa.DSAError, RuntimeError) as e:
+        fp4_step = {"error": str(e)}
+
     # ---- the other decode workloads, each step graph-replayed with L2 flushed
     del inp, out, lse, ws, stages, scores, idx, ws_s, step_graph, g, dev_buf, dev_obuf, bufs
     torch.cuda.empty_cache()
@@ -646,6 +686,7 @@ def run_gpu(args):
         "write": write,
         "mxfp4_indexer": mxfp4,
         "nvfp4_sparse_mla": nvfp4,
+        "fp4_step": fp4_step,
         "eager_ms_per_step": round(eager_ms, 5),
         "cpu_baseline": cpu,
         "gpu_launches": kernels_per_step(wl) * args.steps,

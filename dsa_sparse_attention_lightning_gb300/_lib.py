@@ -58,6 +58,8 @@ SIGNATURES = [
     ("dsa_decode_step_workspace_size", SZ, [I32, I32, I32, I32, I32]),
     ("dsa_decode_step", I32, [P, I32, P, P, P, P, I64, F32, P, I32, I32, P, P, I32, P, I32, F32,
                               I32, P, P, P, P, SZ, P]),
+    ("dsa_decode_step_fp4", I32, [P, P, P, P, P, I64, F32, P, I32, I32, P, P, I32, P, I32, F32,
+                                  I32, P, P, P, P, SZ, P]),
     ("dsa_check_device_status", I32, [P, P, P]),
     ("dsa_selftest_workspace_size", SZ, []),
     ("dsa_selftest_bounded_wait", I32, [I32, P, SZ, P]),
@@ -356,6 +358,41 @@ def dsa_decode_step(q_idx, w, key_cache, latent_cache, latent_scale, block_table
     ws = _workspace(decode_step_workspace_size(B, R, max_pages, H, k), dev, workspace)
     _check("dsa_decode_step", load().dsa_decode_step(
         _ptr(q_idx), qt, _ptr(q_scale), _ptr(w), _ptr(key_cache), _ptr(latent_cache), num_pages,
+        float(latent_scale), _ptr(block_table), B, max_pages, _ptr(row_req), _ptr(row_len), R,
+        _ptr(q), H, float(softmax_scale), int(k), _ptr(out), _ptr(lse), _ptr(idx_out), _ptr(ws),
+        ws.numel(), _stream(dev)))
+    return out, lse
+
+
+def dsa_decode_step_fp4(q_codes, q_scales, w, key_cache, latent_cache, latent_scale, block_table,
+                        row_req, row_len, q, *, softmax_scale, k=2048, out=None, lse=None,
+                        idx_out=None, workspace=None):
+    """The whole step over MXFP4 index keys (pages of MXFP4_KEY_PAGE_BYTES) and
+    NVFP4 latent rows (uint8 [pages, 64, 352]) with an MXFP4 indexer query
+    (``q_codes`` uint8 [R,32,64], ``q_scales`` uint8 [R,32,4]); returns (out, lse)."""
+    dev = q.device
+    _need(q_codes, "q_codes", torch.uint8, dev)
+    _need(q_scales, "q_scales", torch.uint8, dev)
+    _need(q, "q", torch.bfloat16, dev)
+    _need(w, "w", torch.float32, dev)
+    _need(key_cache, "key_cache", torch.uint8, dev)
+    _need(latent_cache, "latent_cache", torch.uint8, dev)
+    for n, t in (("block_table", block_table), ("row_req", row_req), ("row_len", row_len)):
+        _need(t, n, torch.int32, dev)
+    R, H, _ = q.shape
+    B, max_pages = block_table.shape
+    num_pages = key_cache.numel() // MXFP4_KEY_PAGE_BYTES
+    if latent_cache.numel() != num_pages * PAGE * NVFP4_ROW_BYTES:
+        raise ValueError("key_cache and latent_cache must hold the same number of pages")
+    if out is None:
+        out = torch.empty((R, H, V_DIM), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((R, H), dtype=torch.float32, device=dev)
+    if idx_out is not None:
+        _need(idx_out, "idx_out", torch.int32, dev)
+    ws = _workspace(decode_step_workspace_size(B, R, max_pages, H, k), dev, workspace)
+    _check("dsa_decode_step_fp4", load().dsa_decode_step_fp4(
+        _ptr(q_codes), _ptr(q_scales), _ptr(w), _ptr(key_cache), _ptr(latent_cache), num_pages,
         float(latent_scale), _ptr(block_table), B, max_pages, _ptr(row_req), _ptr(row_len), R,
         _ptr(q), H, float(softmax_scale), int(k), _ptr(out), _ptr(lse), _ptr(idx_out), _ptr(ws),
         ws.numel(), _stream(dev)))

@@ -364,15 +364,19 @@ size_t dsa_decode_step_workspace_size(int B, int R, int max_pages, int H, int k)
   return StepLayout(R, max_pages, H, k).bytes;
 }
 
-int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const float* w,
-                    const uint8_t* key_cache, const uint8_t* latent_cache, int64_t num_pages,
-                    float latent_scale, const int32_t* block_table, int B, int max_pages,
-                    const int32_t* row_req, const int32_t* row_len, int R, const void* q, int H,
-                    float softmax_scale, int k, void* out, float* lse, int32_t* idx_out,
-                    void* workspace, size_t ws_bytes, void* stream) {
+namespace {
+// The fused step for both cache formats: q_dtype DSA_BF16 / DSA_E4M3 with FP8
+// keys and FP8 latent rows, or kQMxfp4 (q_idx = E2M1 codes, q_sf = E8M0
+// scales) with MXFP4 keys and NVFP4 latent rows.
+int decode_step(const void* q_idx, int q_dtype, const float* q_scale, const uint8_t* q_sf,
+                const float* w, const uint8_t* key_cache, const uint8_t* latent_cache,
+                int64_t num_pages, float latent_scale, const int32_t* block_table, int B,
+                int max_pages, const int32_t* row_req, const int32_t* row_len, int R,
+                const void* q, int H, float softmax_scale, int k, void* out, float* lse,
+                int32_t* idx_out, void* workspace, size_t ws_bytes, void* stream) {
+  const bool fp4 = q_dtype == kQMxfp4;
   int s = check_rows(B, max_pages, block_table, row_req, row_len, R);
   if (s) return s;
-  if (q_dtype != DSA_BF16 && q_dtype != DSA_E4M3) return DSA_ERR_UNSUPPORTED;
   if (!supported_heads(H)) return DSA_ERR_UNSUPPORTED;
   if (k < 1) return DSA_ERR_INVALID_ARG;
   if (k > kMaxTopk) return DSA_ERR_UNSUPPORTED;
@@ -380,8 +384,10 @@ int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const 
   if (R > 0 && (!q_idx || !w || !key_cache || !latent_cache || !q || !out))
     return DSA_ERR_INVALID_ARG;
   if (q_dtype == DSA_E4M3 && R > 0 && !q_scale) return DSA_ERR_INVALID_ARG;
+  if (fp4 && R > 0 && !q_sf) return DSA_ERR_INVALID_ARG;
   if ((key_cache && !aligned(key_cache, 16)) || (latent_cache && !aligned(latent_cache, 16)) ||
-      (q && !aligned(q, 16)) || (out && !aligned(out, 16)))
+      (q && !aligned(q, 16)) || (out && !aligned(out, 16)) ||
+      (fp4 && q_idx && !aligned(q_idx, 16)) || (fp4 && q_sf && !aligned(q_sf, 4)))
     return DSA_ERR_INVALID_ARG;
   const StepLayout L(R, max_pages, H, k);
   s = check_workspace(workspace, ws_bytes, L.bytes);
@@ -396,6 +402,7 @@ int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const 
 
   ScanArgs sa{q_idx, q_dtype, q_scale, w, key_cache, num_pages, block_table, B, max_pages,
               row_req, row_len, R, scores, ld, ws + L.scan, status};
+  sa.q_sf = q_sf;
   sa.clear_status = true;                          // the step's first kernel clears the word
   cudaError_t e = launch_indexer_scan(sa, st);
   if (e != cudaSuccess) return to_status(e);
@@ -404,7 +411,32 @@ int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const 
   if (e != cudaSuccess) return to_status(e);
   MlaArgs ma{q, H, softmax_scale, latent_cache, num_pages, latent_scale, block_table, B,
              max_pages, row_req, row_len, idx, k, R, out, lse, ws + L.mla, status, true};
+  ma.nvfp4 = fp4;
   return to_status(launch_sparse_mla(ma, st));
+}
+}  // namespace
+
+int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const float* w,
+                    const uint8_t* key_cache, const uint8_t* latent_cache, int64_t num_pages,
+                    float latent_scale, const int32_t* block_table, int B, int max_pages,
+                    const int32_t* row_req, const int32_t* row_len, int R, const void* q, int H,
+                    float softmax_scale, int k, void* out, float* lse, int32_t* idx_out,
+                    void* workspace, size_t ws_bytes, void* stream) {
+  if (q_dtype != DSA_BF16 && q_dtype != DSA_E4M3) return DSA_ERR_UNSUPPORTED;
+  return decode_step(q_idx, q_dtype, q_scale, nullptr, w, key_cache, latent_cache, num_pages,
+                     latent_scale, block_table, B, max_pages, row_req, row_len, R, q, H,
+                     softmax_scale, k, out, lse, idx_out, workspace, ws_bytes, stream);
+}
+
+int dsa_decode_step_fp4(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
+                        const uint8_t* key_cache, const uint8_t* latent_cache, int64_t num_pages,
+                        float latent_scale, const int32_t* block_table, int B, int max_pages,
+                        const int32_t* row_req, const int32_t* row_len, int R, const void* q,
+                        int H, float softmax_scale, int k, void* out, float* lse,
+                        int32_t* idx_out, void* workspace, size_t ws_bytes, void* stream) {
+  return decode_step(q_codes, kQMxfp4, nullptr, q_scales, w, key_cache, latent_cache, num_pages,
+                     latent_scale, block_table, B, max_pages, row_req, row_len, R, q, H,
+                     softmax_scale, k, out, lse, idx_out, workspace, ws_bytes, stream);
 }
 
 size_t dsa_selftest_workspace_size(void) { return selftest_workspace_bytes(); }

@@ -65,6 +65,11 @@ def algorithmic_bytes(wl: Workload) -> int:
     return scan_bytes(wl) + gather_bytes(wl) + query_output_bytes(wl)
 
 
+def algorithmic_bytes_fp4(wl: Workload) -> int:
+    """The same for the step over MXFP4 index keys and NVFP4 latent rows."""
+    return scan_bytes_mxfp4(wl) + gather_bytes_nvfp4(wl) + wl.R * wl.H * (LAT_DIM + V_DIM) * 2
+
+
 def scan_flops(wl: Workload) -> int:
     """2 * 32 heads * 128 dims per (row, visible token)."""
     return int(2 * IDX_HEADS * IDX_DIM * sum(wl.row_lengths()))

@@ -366,6 +366,27 @@ int dsa_decode_step(const void* q_idx, int q_dtype, const float* q_scale, const 
                     float softmax_scale, int k, void* out, float* lse, int32_t* idx_out,
                     void* workspace, size_t ws_bytes, void* stream);
 
+/* ------------------------------------------------------------------------
+ * dsa_decode_step_fp4 -- the whole step over the pages' smaller caches:
+ * MXFP4 index keys (68 bytes per token, as dsa_indexer_score_mxfp4) and NVFP4
+ * latent rows (352 bytes per token, as dsa_sparse_mla_decode_nvfp4), 10,080
+ * bytes per token over 24 layers against 16,992 with both in FP8 (vLLM Day-0
+ * post on Kimi K3.1 Pro, "KV cache footprint per token").  Same order of
+ * kernels, workspace (dsa_decode_step_workspace_size) and outputs as
+ * dsa_decode_step; the query of the indexer is MXFP4 (q_codes [R][32][64],
+ * q_scales [R][32][4], as dsa_indexer_score_mxfp4), the MLA query bf16.
+ *  key_cache     uint8 [num_pages][4352] (MXFP4 pages), 16-byte aligned.
+ *  latent_cache  uint8 [num_pages][64][352] (NVFP4 rows), 16-byte aligned.
+ * Errors: as dsa_decode_step; q_codes must be 16-byte aligned, q_scales
+ * 4-byte aligned.
+ * ---------------------------------------------------------------------- */
+int dsa_decode_step_fp4(const uint8_t* q_codes, const uint8_t* q_scales, const float* w,
+                        const uint8_t* key_cache, const uint8_t* latent_cache, int64_t num_pages,
+                        float latent_scale, const int32_t* block_table, int B, int max_pages,
+                        const int32_t* row_req, const int32_t* row_len, int R, const void* q,
+                        int H, float softmax_scale, int k, void* out, float* lse,
+                        int32_t* idx_out, void* workspace, size_t ws_bytes, void* stream);
+
 /* Synchronises `stream`, then reads the device status word in `workspace`
  * (bits DSA_DEV_*, written by the kernels of the last call that used this
  * workspace) into *bits (may be NULL).  Returns DSA_OK when no bit is set,

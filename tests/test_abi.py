@@ -97,6 +97,10 @@ def test_mla_and_step_reject_bad_shapes(lib):
     assert lib.dsa_decode_step(*step(7, 64)) == 2              # unknown q dtype
     assert lib.dsa_decode_step(*step(1, 64)) == 1              # E4M3 without q_scale
     assert lib.dsa_decode_step(*step(0, 24)) == 2
+    step4 = lambda qs, H: (FAKE, qs, FAKE, FAKE, FAKE, 4, 1.0, FAKE, 1, 4, FAKE, FAKE, 1, FAKE,
+                           H, 0.1, 64, FAKE, None, None, FAKE, wss, None)
+    assert lib.dsa_decode_step_fp4(*step4(FAKE, 24)) == 2      # H not built
+    assert lib.dsa_decode_step_fp4(*step4(None, 64)) == 1      # no MXFP4 query scales
     assert lib.dsa_indexer_score(FAKE, 0, None, FAKE, FAKE, 4, FAKE, 1, 4, FAKE, FAKE, 1, FAKE,
                                  100, FAKE, 1 << 20, None) == 1   # ld < max_pages * 64
 
