@@ -30,11 +30,11 @@
 //  * Each TMEM lane holds one token's (row, head) logits, so the
 //    ReLU-weighted head sum is a per-thread loop: no shuffles.
 //  * Persistent CTAs, one per SM, each taking a contiguous run of (group,
-//    tile) work items; warp roles: 0-1 MMA issuers (tile i by warp i % 2;
-//    warp 0 owns TMEM), 2-5 TMA producers (keys, key scales, group queries;
+//    tile) work items; warp roles: 0-3 MMA issuers (tile i by warp i % 4;
+//    warp 0 owns TMEM), 4-7 TMA producers (keys, key scales, group queries;
 //    page ids looked up 32 tiles ahead; tile i is loaded by producer i % 4
 //    -- the TMA loads one thread issues complete at well under the HBM
-//    rate, so each SM runs four streams), 6-21 epilogue in two groups of
+//    rate, so each SM runs four streams), 8-23 epilogue in two groups of
 //    eight that take alternate tiles (TMEM -> scores; a warp takes TMEM
 //    lane quarter w % 4, i.e. 32 tokens, of two of the group's rows).  A key
 //    stage is released by the MMA's completion alone; the key scales live in
@@ -71,9 +71,9 @@ constexpr int kKeyTileBytes = kTileTok * kIdxDim;       // 2 pages x 64 x 128 B
 constexpr int kPageKeyBytes = kPage * kIdxDim;          // 8192
 constexpr int kPageBytes = kPage * (kIdxDim + 4);       // 8448: keys, then 64 f32 scales
 constexpr int kScRing = 16;                             // key-scale slots (outlive their key stage)
-constexpr int kMmaWarps = 2;                            // warps 0-1: lane 0 issues tiles i % 2 == warp
-constexpr int kProdWarps = 4;                           // warps 2-5: one TMA stream per warp
-constexpr int kEpiWarp0 = kMmaWarps + kProdWarps;       // warps 6-21
+constexpr int kMmaWarps = 4;                            // warps 0-3: lane 0 issues tiles i % 4 == warp
+constexpr int kProdWarps = 4;                           // warps 4-7: one TMA stream per warp
+constexpr int kEpiWarp0 = kMmaWarps + kProdWarps;       // warps 8-23
 constexpr int kEpiGroups = 2;                           // epilogue group g takes tiles i % 2 == g
 constexpr int kEpiWarpsPerGroup = 8;
 constexpr int kEpiWarps = kEpiGroups * kEpiWarpsPerGroup;
@@ -84,7 +84,8 @@ static_assert(kScRing % kProdWarps == 0 && kScRing % kEpiGroups == 0, "fixed slo
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
 constexpr int kDBufs = 4;
 static_assert(kDBufs % kEpiGroups == 0, "a TMEM accumulator always belongs to the same group");
-static_assert(kDBufs % kMmaWarps == 0 && kEpiGroups == kMmaWarps, "one epilogue group per MMA issuer");
+static_assert(kDBufs % kMmaWarps == 0 && kMmaWarps % kEpiGroups == 0,
+              "an accumulator always belongs to the same MMA issuer and epilogue group");
 constexpr int kDCols = kMaxGroupRows * kIdxHeads;       // 128 f32 columns per accumulator
 constexpr uint32_t kTmemCols = kDCols * kDBufs;
 
@@ -97,7 +98,7 @@ constexpr int kOffW = (kOffPv + kScRing * 4 + 15) / 16 * 16;       // [kEpiWarps
 constexpr int kOffBar = (kOffW + kEpiWarps * kEpiRows * kIdxHeads * 4 + 7) / 8 * 8;
 static_assert(kOffKeys % 1024 == 0 && kKeyTileBytes % 1024 == 0, "swizzled TMA tiles need 1024-byte alignment");
 static_assert(kOffScale % 16 == 0 && kOffW % 16 == 0 && kOffBar % 8 == 0, "vector and mbarrier alignment");
-constexpr int kDBars = 6;                                // accumulator barriers (MXFP4: tile mod 6)
+constexpr int kDBars = 12;                               // accumulator barriers (MXFP4: tile mod 12)
 constexpr int kNumBars = 2 * kStages + 2 * kScRing + 2 * kDBars + 2 * kQBufs + kMmaWarps;
 constexpr int kOffTmem = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffTmem + 16;
@@ -120,10 +121,10 @@ static_assert(kOffSfaMx + kScRing * kSfRowBytes <= kOffScale, "scale rows fit th
 static_assert(kMxQAtom + kSfRowBytes <= kQBytes, "query codes and scale rows fit the query buffer");
 static_assert(kSfCol0 + 8 * kMxDBufs <= kTmemCols, "scale columns fit the allocation");
 // Three accumulators, tile i in accumulator i % 3, signalled on barrier pair
-// i % 6: each barrier is waited on by one epilogue group (i % 2) in tile
-// order, and the MMA warp of tile i (i % 2) waits for tile i - 3's release on
-// a barrier whose previous phase (tile i - 9) it already waited for at tile
-// i - 6, so no parity wait can be satisfied by an older phase.
+// i % 12: each barrier is waited on by one epilogue group (i % 2) in tile
+// order, and the MMA warp of tile i (i % 4) waits for tile i - 3's release on
+// barrier (i - 3) % 12, whose previous phase (tile i - 15) it already waited
+// for at tile i - 12, so no parity wait can be satisfied by an older phase.
 static_assert(kDBars % kMxDBufs == 0 && kDBars % kEpiGroups == 0 && kDBars % kMmaWarps == 0 &&
               kDBars >= kDBufs, "accumulator barrier indexing");
 
@@ -447,7 +448,7 @@ __device__ __forceinline__ TilePages tile_pages(const TileCursor& c, const int32
   return t;
 }
 
-// MXFP4 MMA issuers (warps 0-1, tiles i % 2 == warp): the whole warp turns
+// MXFP4 MMA issuers (warps 0-3, tiles i % 4 == warp): the whole warp turns
 // the tile's key scales (landed in token order) into the tensor core's
 // scale-factor rows -- row l = the four scale bytes of tokens l, l + 32,
 // l + 64, l + 96 -- and lane 0 copies them and the group's query scale rows
@@ -500,9 +501,10 @@ __device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int
       fence_proxy_async_smem();                       // visible to the tensor core's copy
       __syncwarp();
       if (!warp_wait(&full[s], s_phase, status)) break;
-      // the previous user of accumulator db is tile i - 3 (barrier (i + 3) % 6)
-      if (!warp_wait(&d_empty[(i + kMxDBufs) % kDBars],
-                     ((uint32_t)((i + kMxDBufs) / kDBars) & 1) ^ 1, status))
+      // the previous user of accumulator db is tile i - 3 (barrier (i - 3) % 12;
+      // for i < 3 the wait is on a fresh barrier's preceding phase)
+      if (!warp_wait(&d_empty[(i + kDBars - kMxDBufs) % kDBars],
+                     ((uint32_t)((i + kDBars - kMxDBufs) / kDBars) & 1) ^ 1, status))
         break;
       if (lane == 0) {
         tc_fence_after();
@@ -625,9 +627,10 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
       // ---------------- MMA issuers: lane 0 of warp m issues the tiles i with
       // i % kMmaWarps == m.  An issuing thread is held at every tcgen05.mma
       // until the tensor core takes it, and its barrier waits and commits cost
-      // about as much again per tile; with two issuers one thread's
-      // bookkeeping overlaps the other's MMAs.  Both walk every tile to follow
-      // the group, stage and accumulator sequence.
+      // about as much again per tile; with four issuers the others'
+      // bookkeeping overlaps one thread's MMAs (256K scan: 141.5 -> 138.8 us
+      // against two issuers).  All walk every tile to follow the group, stage
+      // and accumulator sequence.
       if (lane == 0) {
         const int m = warp;
         int cur_group = -1, gi = -1, left = 0;          // tiles left in the current group
