@@ -116,15 +116,23 @@ constexpr int kMxQAtom = kMaxGroupRows * kIdxHeads * kMxKeyBytes;   // 128 rows 
 constexpr int kSfRowBytes = 32 * 16;                                // 32 rows x 16 B
 constexpr int kOffSfaMx = kOffKeys + kStages * kMxKeyTileBytes;     // [kScRing] key scale rows
 constexpr int kMxDBufs = 3;                                         // accumulators (TMEM holds the scales too)
-constexpr uint32_t kSfCol0 = kDCols * kMxDBufs;                     // scale columns: 8 per accumulator
+constexpr uint32_t kSfCol0 = kDCols * kMxDBufs;                     // scale columns: 8 per slot
+constexpr int kSfSlots = 12;                                        // tile i's scales in slot i % 12
 static_assert(kOffSfaMx + kScRing * kSfRowBytes <= kOffScale, "scale rows fit the key region");
 static_assert(kMxQAtom + kSfRowBytes <= kQBytes, "query codes and scale rows fit the query buffer");
-static_assert(kSfCol0 + 8 * kMxDBufs <= kTmemCols, "scale columns fit the allocation");
+static_assert(kSfCol0 + 8 * kSfSlots <= kTmemCols, "scale columns fit the allocation");
+static_assert(kSfSlots == kDBars, "a scale slot is tracked by the tile's accumulator barrier");
 // Three accumulators, tile i in accumulator i % 3, signalled on barrier pair
 // i % 12: each barrier is waited on by one epilogue group (i % 2) in tile
 // order, and the MMA warp of tile i (i % 4) waits for tile i - 3's release on
 // barrier (i - 3) % 12, whose previous phase (tile i - 15) it already waited
 // for at tile i - 12, so no parity wait can be satisfied by an older phase.
+// Tile i's scale factors go to their own TMEM slot i % 12, which tile i - 12
+// last read: the same warp waits for that tile's MMA completion (barrier
+// d_full[i % 12], previous phase; tile i - 24's phase completed before the
+// warp's own wait at tile i - 12 returned) and copies the scales in before
+// its key and accumulator waits, off the path from an epilogue release to the
+// next MMA.
 static_assert(kDBars % kMxDBufs == 0 && kDBars % kEpiGroups == 0 && kDBars % kMmaWarps == 0 &&
               kDBars >= kDBufs, "accumulator barrier indexing");
 
@@ -406,6 +414,25 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint32
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
+// Lane 0 polls without suspending (bounded); the outcome is the same for the
+// whole warp.  Used where the waiter must resume as soon as the phase completes.
+__device__ __forceinline__ bool warp_wait_spin(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) {
+    if (!mbar_test(bar, parity)) {
+      const long long t0 = clock64();
+      while (!mbar_test(bar, parity)) {
+        if (clock64() - t0 > kWaitCycles) {
+          raise_dev(status, DSA_DEV_TIMEOUT);
+          ok = false;
+          break;
+        }
+      }
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
 // ---- TMA: tensor-map tile loads completing on an mbarrier -------------------
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
                                             uint64_t* bar) {
@@ -455,9 +482,9 @@ __device__ __forceinline__ TilePages tile_pages(const TileCursor& c, const int32
 // into tensor memory, then issues the two K = 64 block-scaled MMAs (scale
 // bytes 0-1, then 2-3).  The MMA takes the scales of operand row m (a token,
 // or a (row, head) column) from lane m % 32, column base + m / 32, which is
-// where the replicated 32-row copy puts them.  The copies and MMAs of one thread run in issue
-// order; the scale columns of accumulator db are rewritten only after the
-// epilogue has released db, i.e. after the MMAs that read them completed.
+// where the replicated 32-row copy puts them.  The accumulator barriers are
+// polled without suspending the waiting thread (256K scan: 147 -> 142 us
+// against a suspending try_wait).
 __device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int ntiles,
                                               uint32_t tmem_base, uint64_t* bars,
                                               uint32_t* status) {
@@ -500,18 +527,26 @@ __device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int
           make_uint4(tok[lane], tok[lane + 32], tok[lane + 64], tok[lane + 96]);
       fence_proxy_async_smem();                       // visible to the tensor core's copy
       __syncwarp();
+      // scale slot c was last read by the MMAs of tile i - 12, which completed
+      // on barrier c's previous phase; the copies into it go out before the
+      // key and accumulator waits
+      if (i >= kSfSlots && !warp_wait(&d_full[c], (uint32_t)((i - kSfSlots) / kDBars) & 1, status))
+        break;
+      const uint32_t sfa = tmem_base + kSfCol0 + (uint32_t)(c * 8), sfb = sfa + 4;
+      if (lane == 0) {
+        tc_fence_after();
+        tmem_cp_32x128b_warpx4(sfa, desc_sf_rows16(smem_u32(sf_rows)));
+        tmem_cp_32x128b_warpx4(sfb, sfb_desc);
+      }
       if (!warp_wait(&full[s], s_phase, status)) break;
       // the previous user of accumulator db is tile i - 3 (barrier (i - 3) % 12;
       // for i < 3 the wait is on a fresh barrier's preceding phase)
-      if (!warp_wait(&d_empty[(i + kDBars - kMxDBufs) % kDBars],
+      if (!warp_wait_spin(&d_empty[(i + kDBars - kMxDBufs) % kDBars],
                      ((uint32_t)((i + kDBars - kMxDBufs) / kDBars) & 1) ^ 1, status))
         break;
       if (lane == 0) {
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(db * kDCols);
-        const uint32_t sfa = tmem_base + kSfCol0 + (uint32_t)(db * 8), sfb = sfa + 4;
-        tmem_cp_32x128b_warpx4(sfa, desc_sf_rows16(smem_u32(sf_rows)));
-        tmem_cp_32x128b_warpx4(sfb, sfb_desc);
         const uint64_t a_desc = a_desc_base + (uint64_t)((s * kMxKeyTileBytes) >> 4);
         mma_mxf4_ss(d_tmem, a_desc, b_desc, idesc0, sfa, sfb, 0u);
         mma_mxf4_ss(d_tmem, a_desc + 2, b_desc + 2, idesc1, sfa, sfb, 1u);   // + 32 bytes of K
@@ -820,21 +855,37 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
         }
         __syncwarp();
       }
-      if (!warp_wait(&d_full[c], par, status)) break;
+      if (!(kMx ? warp_wait_spin(&d_full[c], par, status) : warp_wait(&d_full[c], par, status))) break;
       if (!warp_wait(&sc_full[x], (uint32_t)(i / kScRing) & 1, status)) break;
       tc_fence_after();
       const bool page_valid = (pv_s[x] >> (tok_in >> 6)) & 1u;
       const float ks = kMx ? 1.f : scale_s[x * kTileTok + tok_in];   // MXFP4: scaled in the MMA
       const int tok = cur.t * kTileTok + tok_in;
+      // MXFP4: the accumulator and the scale slot are released as soon as
+      // this warp's last tensor-memory load of the tile has completed, before
+      // the last row's head sum and the score stores (256K: 155 -> 149 us);
+      // the FP8 instance releases after its stores (the early release measured
+      // 137.6 -> 144.0 us there)
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&d_empty[c]);
+          mbar_arrive(&sc_empty[x]);
+        }
+      };
+      const int nr = min(kEpiRows, cur.G.y - r0);       // this warp's rows in the group (warp-uniform)
+      if (nr <= 0 && kMx) release();
 #pragma unroll
       for (int rr = 0; rr < kEpiRows; ++rr) {
         const int r = r0 + rr;
-        if (r < cur.G.y) {
+        if (rr < nr) {
           uint32_t xv[32];
           const uint32_t ta = tmem_base + ((uint32_t)(quarter * 32) << 16) +
                               (uint32_t)(db * kDCols + r * kIdxHeads);
           tmem_ld_32x32b_x32(ta, xv);
           tmem_wait_ld();
+          if (kMx && rr == nr - 1) release();
           const float4* wr = reinterpret_cast<const float4*>(w_s + rr * kIdxHeads);
           float acc[4] = {0.f, 0.f, 0.f, 0.f};          // four independent FMA chains
 #pragma unroll
@@ -850,12 +901,7 @@ scan_kernel(const __grid_constant__ CUtensorMap key_map, const __grid_constant__
             scores[(size_t)(cur.G.x + r) * ld + tok] = sc * ks;
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&d_empty[c]);
-        mbar_arrive(&sc_empty[x]);
-      }
+      if (!kMx) release();
       cur.advance(kEpiGroups);
     }
   }
