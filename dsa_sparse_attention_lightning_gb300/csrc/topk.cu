@@ -392,8 +392,19 @@ topk_finalize_kernel(const float* scores, int64_t ld, const int32_t* __restrict_
   uint32_t T, need_eq, n_eq;
   if (n >= (uint32_t)k && n <= (uint32_t)kTopkCandCap && nch <= kMaxRunChunks) {
     // ---- candidates in shared memory, ranked by position through their runs
+    // every candidate load is issued before the first store: one memory round trip
     const uint2* src = items + (size_t)r * kTopkCandCap;
-    for (uint32_t i = threadIdx.x; i < n; i += kFinalThreads) C.cand[i] = src[i];
+    uint2 cv[kCandPer];
+#pragma unroll
+    for (int u = 0; u < kCandPer; ++u) {
+      const uint32_t i = (uint32_t)u * kFinalThreads + threadIdx.x;
+      cv[u] = i < n ? ld_dep(src + i) : make_uint2(0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kCandPer; ++u) {
+      const uint32_t i = (uint32_t)u * kFinalThreads + threadIdx.x;
+      if (i < n) C.cand[i] = cv[u];
+    }
     __syncthreads();
     kth_key([&](uint32_t i) { return C.cand[i].x; }, n, k, S, T, need_eq, n_eq);
     const uint2* rr = runs + (size_t)r * nchunks;
