@@ -226,13 +226,13 @@ topk_collect_kernel(const float* scores, int64_t ld, const int32_t* __restrict__
   const int r = blockIdx.y;
   const int c = blockIdx.x;
   const int len = row_len[r];
+  const uint32_t t = ld_dep(tau + r);            // issued with the row length: one round trip
   if (!row_ok(len, max_len) || len <= k) return;
   const int64_t s0 = (int64_t)c * kTopkChunk;
   if (s0 >= len) return;
   const int64_t s1 = min((int64_t)len, s0 + kTopkChunk);
   __shared__ uint32_t warp_sums[32];
   __shared__ uint32_t s_base;
-  const uint32_t t = tau[r];
 
   // each thread owns 16 consecutive positions
   constexpr int PER = kTopkChunk / kCollectThreads;
@@ -359,13 +359,14 @@ constexpr int kMaxRunChunks = 4096;                       // chunk table held in
 
 struct CandSmem {
   uint2 cand[kTopkCandCap];
+  uint2 run[kMaxRunChunks];                     // each chunk's {start, count} in the list
   uint16_t ex_tie[kTopkCandCap + kFinalThreads];
   uint16_t ex_sel[kTopkCandCap + kFinalThreads];
   uint32_t base_tie[kMaxRunChunks];
   uint32_t base_sel[kMaxRunChunks];
 };
 
-__global__ void __launch_bounds__(kFinalThreads)
+__global__ void __launch_bounds__(kFinalThreads, 1)
 topk_finalize_kernel(const float* scores, int64_t ld, const int32_t* __restrict__ row_len,
                      int64_t max_len, int k, const uint32_t* cnt, const uint2* runs,
                      int nchunks, const uint2* items, int32_t* __restrict__ idx,
@@ -377,6 +378,7 @@ topk_finalize_kernel(const float* scores, int64_t ld, const int32_t* __restrict_
   pdl_wait();                                  // the candidate lists
   const int r = blockIdx.x;
   const int len = row_len[r];
+  const uint32_t n = ld_dep(cnt + r);            // issued with the row length: one round trip
   int32_t* out = idx + (size_t)r * k;
   if (!row_ok(len, max_len)) {
     if (threadIdx.x == 0) raise_dev(status, DSA_DEV_BAD_ROW);
@@ -387,27 +389,38 @@ topk_finalize_kernel(const float* scores, int64_t ld, const int32_t* __restrict_
     for (int j = threadIdx.x; j < k; j += kFinalThreads) out[j] = j < len ? j : -1;
     return;
   }
-  const uint32_t n = cnt[r];
   const int nch = (int)((len + kTopkChunk - 1) / kTopkChunk);
   uint32_t T, need_eq, n_eq;
   if (n >= (uint32_t)k && n <= (uint32_t)kTopkCandCap && nch <= kMaxRunChunks) {
     // ---- candidates in shared memory, ranked by position through their runs
     // every candidate load is issued before the first store: one memory round trip
     const uint2* src = items + (size_t)r * kTopkCandCap;
+    const uint2* runs_r = runs + (size_t)r * nchunks;
     uint2 cv[kCandPer];
+    uint2 rv[kMaxRunChunks / kFinalThreads];
 #pragma unroll
     for (int u = 0; u < kCandPer; ++u) {
       const uint32_t i = (uint32_t)u * kFinalThreads + threadIdx.x;
       cv[u] = i < n ? ld_dep(src + i) : make_uint2(0u, 0u);
     }
 #pragma unroll
+    for (int u = 0; u < kMaxRunChunks / kFinalThreads; ++u) {
+      const int ch = u * kFinalThreads + (int)threadIdx.x;
+      rv[u] = ch < nch ? ld_dep(runs_r + ch) : make_uint2(0u, 0u);
+    }
+#pragma unroll
     for (int u = 0; u < kCandPer; ++u) {
       const uint32_t i = (uint32_t)u * kFinalThreads + threadIdx.x;
       if (i < n) C.cand[i] = cv[u];
     }
+#pragma unroll
+    for (int u = 0; u < kMaxRunChunks / kFinalThreads; ++u) {
+      const int ch = u * kFinalThreads + (int)threadIdx.x;
+      if (ch < nch) C.run[ch] = rv[u];
+    }
     __syncthreads();
     kth_key([&](uint32_t i) { return C.cand[i].x; }, n, k, S, T, need_eq, n_eq);
-    const uint2* rr = runs + (size_t)r * nchunks;
+    const uint2* rr = C.run;
     const uint32_t i0 = threadIdx.x * kCandPer;
     uint8_t f[kCandPer];
     const bool all_ties = need_eq == n_eq;           // every key equal to T is kept
