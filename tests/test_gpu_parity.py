@@ -173,6 +173,31 @@ def test_topk_long_row_split_over_chunks(dsa, oracle_mod):
     _topk_bitexact(dsa, oracle_mod, s, [L], 2048)
 
 
+def test_topk_many_long_rows_full_size(dsa, oracle_mod):
+    """64 rows of up to 262144 scores (16 requests x 4 rows at 256K context),
+    the sample / collect / finalize path: random rows, exact ties straddling the cut,
+    winners only at the end of the row, all scores equal, rising in steps,
+    thresholds from the sample far too low (more candidates than the list
+    holds) and too high (fewer than k), both taking the whole-row select, and
+    ragged lengths."""
+    rng = np.random.default_rng(5)
+    R, L = 64, 262144
+    pos = np.arange(L)
+    s = rng.standard_normal((R, L)).astype(np.float32)
+    s[1, rng.choice(L, 3000, replace=False)] = 5.5
+    s[2] = (pos * 1e-3).astype(np.float32)                 # rising: the last 2048 win
+    s[3] = 1.0                                             # all equal: the first 2048
+    s[4] = (pos // 4096).astype(np.float32)                # rising in steps of exact ties
+    s[5, :] = 1.0
+    s[5, (pos // 32) % 64 == 0] = 2.0                      # half the sampled blocks: 4096 ties
+    sampled = (pos // 32) % 32 == 0                        # the blocks the sample reads at 256K
+    s[6, ~sampled] += 10.0                                 # threshold far too low: the list
+    s[10, sampled & (pos < 16384)] += 10.0                 # overflows; too high: < k candidates
+    lens = [L] * R
+    lens[7], lens[8], lens[9] = 49153, 100001, 2048
+    _topk_bitexact(dsa, oracle_mod, s, lens, 2048)
+
+
 # ------------------------------------------------------------------ the Write step
 def test_write_kv_matches_oracle(dsa, oracle_mod):
     rng = np.random.default_rng(11)
@@ -437,15 +462,16 @@ def _set_keys(inp, scale_of_pos):
         scales[pg, sl] = scale_of_pos(pos).float()
 
 
+@pytest.mark.parametrize("rows", [[2, 1, 1, 3], [8, 8, 8, 8]], ids=["7_rows", "32_rows"])
 @pytest.mark.parametrize("pattern", ["equal", "rising", "rising_steps", "ties_at_cut"])
-def test_step_selection_adversarial_rows(dsa, oracle_mod, pattern):
+def test_step_selection_adversarial_rows(dsa, oracle_mod, pattern, rows):
     """Rows built against the selection: all scores equal (ties broken by
     position), scores rising along the context (the winners come last),
     rising in steps (long runs of exact ties), and many exact ties at the
-    cut; rows long enough for the sample / collect / finalize path and short
-    ones for the one-CTA path."""
+    cut; rows long enough for the sample / collect / finalize path (7 or 32
+    rows) and short ones for the one-CTA path."""
     ctx = [300000, 70000, 5000, 2100]
-    wl = inputs.Workload("sel_adv", ctx, [2, 1, 1, 3], H=16, k=2048, seed=31)
+    wl = inputs.Workload("sel_adv", ctx, rows, H=16, k=2048, seed=31)
     inp = inputs.make_inputs(wl, device=DEV)
     inp["ctx"] = ctx
     f = {"equal": lambda p: torch.ones_like(p, dtype=torch.float64),
