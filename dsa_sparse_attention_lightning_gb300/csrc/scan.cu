@@ -544,7 +544,7 @@ __device__ __forceinline__ void mx_mma_issuer(uint8_t* smem, TileCursor cur, int
       // the previous user of accumulator db is tile i - 3 (barrier (i - 3) % 12;
       // for i < 3 the wait is on a fresh barrier's preceding phase)
       if (!warp_wait_spin(&d_empty[(i + kDBars - kMxDBufs) % kDBars],
-                     ((uint32_t)((i + kDBars - kMxDBufs) / kDBars) & 1) ^ 1, status))
+                          ((uint32_t)((i + kDBars - kMxDBufs) / kDBars) & 1) ^ 1, status))
         break;
       if (lane == 0) {
         tc_fence_after();
