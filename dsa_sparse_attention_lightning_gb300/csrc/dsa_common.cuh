@@ -28,7 +28,7 @@ constexpr size_t kAlign = 256;
 constexpr size_t kStatusBytes = 256;           // device status word lives here
 
 // ---- top-k partitioning ------------------------------------------------
-constexpr int kTopkChunk = 4096;               // scores per collecting CTA
+constexpr int kTopkChunk = 2048;               // scores per collecting CTA
 constexpr int kTopkBins1 = 2048;               // first radix digit: key bits 31..21
 constexpr int kTopkBins2 = 2048;               // second digit: bits 20..10
 constexpr int kTopkBins3 = 1024;               // third digit: bits 9..0
@@ -37,7 +37,7 @@ inline size_t align_up(size_t x, size_t a = kAlign) { return (x + a - 1) / a * a
 
 // Byte offsets of the top-k scratch inside a workspace region: per row a
 // candidate threshold, a candidate count (zeroed by a memset before every
-// selection), where each 4096-score chunk put its candidates, and room for
+// selection), where each 2048-score chunk put its candidates, and room for
 // kTopkCandCap (key, position) candidates.
 constexpr int kTopkCandCap = 8192;
 struct TopkLayout {

@@ -14,7 +14,7 @@
 //               1.25 k + 16 sb keys >= tau: the key of the sample's rank-rho
 //               element, rounded down to its 22-bit prefix (two radix digits
 //               over the sample).
-//   2. collect  (row x 4096-score chunk CTAs): every key >= tau is appended,
+//   2. collect  (row x 2048-score chunk CTAs): every key >= tau is appended,
 //               with its position, to the row's candidate list (one global
 //               reservation per CTA, so each chunk's candidates form one run in
 //               position order; the run's place is recorded); the count is

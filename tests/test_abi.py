@@ -47,12 +47,12 @@ def test_version_and_status_strings(lib):
 
 
 def test_workspace_sizes(lib):
-    # per row: a threshold, a count, one (offset, count) pair per 4096-score
+    # per row: a threshold, a count, one (offset, count) pair per 2048-score
     # chunk and room for 8192 (key, position) candidates (longer candidate
     # lists fall back to a pass over the scores)
     assert lib.dsa_topk_workspace_size(4, 1000, 64) >= 4 * 8192 * 8
     grow = lib.dsa_topk_workspace_size(8, 1 << 20, 2048) - lib.dsa_topk_workspace_size(8, 1 << 10, 2048)
-    assert 0 < grow <= 8 * 256 * 8 + 256
+    assert 0 < grow <= 8 * 512 * 8 + 256
     assert lib.dsa_sparse_mla_workspace_size(64, 64, 2048) >= 64 * 64 * 512 * 4
     assert lib.dsa_decode_step_workspace_size(16, 64, 512, 64, 2048) >= \
         lib.dsa_topk_workspace_size(64, 512 * 64, 2048)
